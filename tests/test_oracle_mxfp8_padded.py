@@ -1,0 +1,148 @@
+"""Pins for the oracle's MXFP8 codec and the padded-capacity reference (CPU only)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import layer as ol
+from oracle import mxfp8 as mx
+from oracle import padded as pd
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "mxfp8_format.json")
+
+
+def test_format_constants_from_the_pages():
+    gold = json.load(open(GOLDEN))
+    assert mx.E4M3_MAX == gold["e4m3_max"]
+    assert mx.BLOCK == gold["block_elements"]
+    # storage of one block: BLOCK E4M3 bytes + one E8M0 byte
+    q, s = mx.quantize_blocks(np.ones((1, 4 * mx.BLOCK)))
+    bits = 8 * (q.size + s.size) / q.size
+    assert bits == gold["bits_per_element"]
+    assert np.nanmax(mx.e4m3_decode(np.arange(256))) == gold["e4m3_max"]
+
+
+def test_e4m3_decode_matches_library_on_all_codes():
+    c = np.arange(256, dtype=np.uint8)
+    ours = mx.e4m3_decode(c)
+    lib = torch.from_numpy(c).view(torch.float8_e4m3fn).double().numpy()
+    same = (ours == lib) | (np.isnan(ours) & np.isnan(lib))
+    assert same.all()
+    assert np.isnan(ours[[0x7F, 0xFF]]).all() and np.isfinite(np.delete(ours, [0x7F, 0xFF])).all()
+
+
+def test_e4m3_encode_roundtrip_and_library_rounding():
+    c = np.arange(256)
+    finite = ~np.isnan(mx.e4m3_decode(c))
+    assert np.array_equal(mx.e4m3_encode(mx.e4m3_decode(c[finite])), c[finite])
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.standard_normal(50000) * 60, rng.standard_normal(50000) * 1e-2,
+                        # exact midpoints between neighbouring codes (tie cases)
+                        (mx.e4m3_decode(np.arange(1, 126)) + mx.e4m3_decode(np.arange(2, 127))) / 2])
+    v = np.clip(v, -448, 448)
+    lib = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mx.e4m3_encode(v), lib)
+
+
+def test_block_exponent_is_smallest_fitting_power():
+    rng = np.random.default_rng(1)
+    amax = np.concatenate([np.exp2(rng.uniform(-60, 60, 20000)),
+                           448.0 * np.exp2(np.arange(-20, 20)),              # exact fits
+                           np.nextafter(448.0 * np.exp2(np.arange(-20, 20)), np.inf)])
+    e = mx.block_exponent(amax)
+    assert np.all(amax <= 448.0 * np.exp2(e.astype(float)))
+    assert np.all(amax > 448.0 * np.exp2(e.astype(float) - 1))
+    assert mx.block_exponent(0.0) == -127
+
+
+def test_qdq_error_bound():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((64, 256)) * np.exp2(rng.integers(-8, 8, (64, 1)))
+    q, s = mx.quantize_blocks(v, axis=1)
+    assert q.dtype == np.uint8 and s.shape == (64, 8)
+    back = mx.dequantize_blocks(q, s, axis=1)
+    e = (s.astype(float) - 127).repeat(32, axis=1)
+    # half an E4M3 ulp: 2^-4 relative for normals, 2^-10 * 2^e absolute below
+    bound = np.maximum(np.abs(v) * 2.0 ** -4, np.exp2(e - 10))
+    assert np.all(np.abs(back - v) <= bound)
+    # the scaled block maximum always fits: no code decodes above 448
+    assert np.nanmax(np.abs(mx.e4m3_decode(q))) <= 448
+
+
+def test_quantize_along_axis0_matches_transposed():
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((64, 5))
+    q0, s0 = mx.quantize_blocks(w, axis=0)
+    q1, s1 = mx.quantize_blocks(w.T, axis=1)
+    assert np.array_equal(q0, q1.T) and np.array_equal(s0, s1.T)
+
+
+def test_padded_with_enough_capacity_equals_unpadded():
+    T, d, E, k, h = 30, 8, 4, 2, 6
+    rng = np.random.default_rng(4)
+    inp = dict(x=rng.standard_normal((T, d)), W1=rng.standard_normal((E, d, h)),
+               W3=rng.standard_normal((E, d, h)), W2=rng.standard_normal((E, h, d)),
+               idx=np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32),
+               glogit=rng.standard_normal((T, k)))
+    ref = ol.layer_forward(inp, k, E)
+    C = int(ref["counts"].max())
+    p = pd.padded_forward(inp["x"], inp["idx"], ref["g"], inp["W1"], inp["W3"], inp["W2"], E, C)
+    assert p["dropped"] == 0
+    np.testing.assert_allclose(p["out"], ref["out"], rtol=1e-12, atol=1e-12)
+    assert p["padded_rows"] == E * C and p["unpadded_rows"] == T * k
+
+
+def test_padded_drops_overflow_by_hand():
+    # T=4, k=1, E=2: expert 0 gets tokens 0,1,2 and expert 1 gets token 3.
+    # Capacity 2 keeps tokens 0 and 1 at expert 0 and drops token 2.
+    T, d, E, h = 4, 3, 2, 2
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((T, d))
+    W1 = rng.standard_normal((E, d, h)); W3 = rng.standard_normal((E, d, h))
+    W2 = rng.standard_normal((E, h, d))
+    idx = np.array([[0], [0], [0], [1]])
+    assert pd.capacity(T, 1, E, factor=1.0) == 2
+    assert pd.capacity(16384, 4, 128) == 640
+    p = pd.padded_forward(x, idx, np.ones((T, 1)), W1, W3, W2, E, 2)
+    assert p["dropped"] == 1 and p["dropped_fraction"] == 0.25
+    assert list(p["kept"][:, 0]) == [True, True, False, True]
+    assert np.all(p["out"][2] == 0)
+    for t, e in ((0, 0), (1, 0), (3, 1)):
+        ref = (ol.silu(x[t] @ W1[e]) * (x[t] @ W3[e])) @ W2[e]
+        np.testing.assert_allclose(p["out"][t], ref, rtol=1e-12)
+
+
+def test_qdq_is_exact_on_representable_blocks():
+    # blocks whose values lie on the E4M3 grid times 2^s, with the block maximum
+    # exactly 448 * 2^s, come back unchanged
+    rng = np.random.default_rng(6)
+    codes = rng.integers(0, 0x7E, (8, 4, 32))
+    codes[:, :, 0] = 0x7E                                  # 448 in every block
+    sgn = np.where(rng.random((8, 4, 32)) < 0.5, -1.0, 1.0)
+    scale = np.exp2(rng.integers(-20, 20, (8, 4, 1)).astype(float))
+    v = (sgn * mx.e4m3_decode(codes) * scale).reshape(8, 128)
+    assert np.array_equal(mx.qdq(v, axis=1), v)
+
+
+def test_mxfp8_forward_error_matches_format_precision():
+    # E4M3 keeps 3 mantissa bits (about 2.6% RMS relative rounding per
+    # operand); through two quantised GEMMs and a quantised activation the
+    # output error of Gaussian data lands at a few percent, never at zero.
+    T, d, E, k, h = 32, 128, 3, 2, 64
+    rng = np.random.default_rng(7)
+    Xp = rng.standard_normal((T * k, d))
+    W1 = rng.standard_normal((E, d, h)) / np.sqrt(d); W3 = rng.standard_normal((E, d, h)) / np.sqrt(d)
+    W2 = rng.standard_normal((E, h, d)) / np.sqrt(h)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    _, off, _, _ = ol.route_map(idx, E)
+    exact = ol.expert_ffn_forward(Xp, off, W1, W3, W2)
+    q = mx.expert_ffn_forward_mxfp8(Xp, off, W1, W3, W2)
+    rel = np.linalg.norm(q["Yp"] - exact["Yp"]) / np.linalg.norm(exact["Yp"])
+    assert 0.02 < rel < 0.12
+    # the first GEMM alone: two quantised operands, ~3.7% expected
+    h1 = mx.qdq(Xp, axis=1)[off[0]:off[1]] @ mx.qdq(W1[0], axis=0)
+    h1x = Xp[off[0]:off[1]] @ W1[0]
+    rel1 = np.linalg.norm(h1 - h1x) / np.linalg.norm(h1x)
+    assert 0.015 < rel1 < 0.06
