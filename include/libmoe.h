@@ -1,0 +1,210 @@
+/*
+ * libmoe — a GB300-native (sm_103a) single-GPU MoE expert layer behind a C ABI.
+ *
+ * The layer: router top-k -> device-resident route map (counts, offsets,
+ * permutation) -> rowwise dispatch into expert-contiguous rows -> unpadded
+ * grouped SwiGLU GEMM on tcgen05 tensor cores -> routing-weighted combine,
+ * and the backward of every step.
+ *
+ * Sources.  "OLMo-core 3：MoE 训练栈让专家池越大、吞吐不再越慢" (bloombook.cn
+ * tutorial), sections "rowwise EP：用 NVSHMEM 一端直写" (rows written straight
+ * into the destination expert's input buffer by a route-table lookup; combine
+ * brings them back) and "另外两处税：主机同步与 padding" (routing counts, expert
+ * row counts and the per-expert permutation stay on the device, removing two
+ * host syncs; one grouped-GEMM launch over all experts with their exact row
+ * counts, no padding to a common capacity).  The Olmo-core MoE report's
+ * speed-read summary (taotianhua.com), paragraph "GPU-resident metadata
+ * removes recurring host waits", says the same of the report's Sections 8-9.
+ * The pages define neither the router function nor the expert network; the
+ * definitions below (softmax-then-top-k with renormalised gates, ties to the
+ * lower expert id; SwiGLU experts W2(silu(x W1) * (x W3))) are the benchmark
+ * specification's reading.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are DEVICE pointers owned by the caller, except where a
+ *    parameter says "host".  The library allocates no memory, never
+ *    synchronises the host (moe_get_status excepted, on request) and enqueues
+ *    all work on `stream` (NULL = the legacy default stream).
+ *  - bf16 tensors are passed as moe_bf16_t* (uint16_t bit patterns), row-major.
+ *  - Every device pointer must be 16-byte aligned.
+ *  - Host-side argument errors return a negative moe_status_t and launch
+ *    nothing.  A launch failure returns MOE_ERR_CUDA.  Data errors found on the
+ *    device (an expert id outside [0, E), a wait that timed out) are written
+ *    to the status word inside the workspace and leave the outputs
+ *    unspecified; read it with moe_get_status.
+ *  - T = 0 is a valid no-op (weight gradients are then written as zeros).
+ *    Experts that receive no rows are valid.
+ *  - Sizes: 1 <= k <= 8, k <= E <= 1024.  The grouped GEMMs need d and h to be
+ *    multiples of 64 (MOE_ERR_UNSUPPORTED otherwise); the row kernels need d to
+ *    be a multiple of 8.  T * k must fit in int32.
+ *  - Calls are stateless apart from a per-device cache of the SM count and of
+ *    kernel attributes; they are safe to call from several host threads on
+ *    different streams with distinct workspaces.
+ */
+#ifndef LIBMOE_H
+#define LIBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t;               /* bf16 bit pattern */
+typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2,   /* valid but outside what the kernels handle */
+  MOE_ERR_WORKSPACE = -3,     /* workspace null or smaller than the query */
+  MOE_ERR_CUDA = -4           /* a CUDA launch or runtime call failed */
+} moe_status_t;
+
+/* Device-side status codes written into the workspace status word. */
+enum {
+  MOE_DEV_OK = 0,
+  MOE_DEV_BAD_EXPERT_ID = 1,  /* an expert id outside [0, E) was routed */
+  MOE_DEV_WAIT_TIMEOUT = 2    /* a pipeline wait in a GEMM gave up */
+};
+
+/* Human-readable name of a moe_status_t. Never NULL. */
+const char* moe_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int moe_version(void);
+
+/* Number of kernels this library has enqueued since it was loaded (all
+ * threads, all devices).  Host-side counter, for launch accounting. */
+uint64_t moe_launch_count(void);
+
+/* Bytes of workspace needed by moe_expert_offsets, moe_grouped_swiglu_fwd/bwd
+ * and moe_router_logits_bwd for these sizes.  The first 256 bytes hold the
+ * device status word; the rest is route-map and reduction scratch.  The
+ * workspace must be zeroed once (or reset with moe_reset_status) before its
+ * status word is meaningful. */
+size_t moe_workspace_size(int T, int E, int k, int d, int h);
+
+/* Zero the device status word (async on `stream`). */
+int moe_reset_status(void* ws, moe_stream_t stream);
+
+/* Copy the device status word to *host_status (host pointer).  This call
+ * synchronises `stream`; it is the only one that does. */
+int moe_get_status(const void* ws, int32_t* host_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- router */
+
+/* Router logits z[T,E] (fp32) = x[T,d] (bf16) @ W_r[d,E] (fp32) + b[E]
+ * (b may be NULL).  fp32 accumulation. */
+int moe_router_logits(const moe_bf16_t* x, const float* W_r, const float* b,
+                      int T, int d, int E, float* logits, moe_stream_t stream);
+
+/* Top-k of each row of logits[T,E] (fp32): topk_idx[T,k] (int32) lists the k
+ * largest logits in the total order (value descending, expert id ascending;
+ * -0.0 == +0.0), and topk_gate[T,k] (fp32) = softmax over the k selected
+ * logits (the full softmax renormalised over the selection).  NaN logits are
+ * out of contract.  Requires k <= E <= 1024. */
+int moe_router_topk(const float* logits, int T, int E, int k,
+                    int32_t* topk_idx, float* topk_gate, moe_stream_t stream);
+
+/* Gates for externally chosen experts: topk_gate[T,k] = softmax over each
+ * row of sel_logits[T,k] (synthetic uniform routing). */
+int moe_router_gates(const float* sel_logits, int T, int k, float* topk_gate,
+                     moe_stream_t stream);
+
+/* Backward of the renormalised top-k softmax: d_logits[T,E] (fp32, fully
+ * written) is g_j * (dg_j - sum_l g_l dg_l) at column topk_idx[t,j] and zero
+ * in every other column. */
+int moe_router_topk_bwd(const float* topk_gate, const float* d_gate,
+                        const int32_t* topk_idx, int T, int E, int k,
+                        float* d_logits, moe_stream_t stream);
+
+/* Backward of the router logits GEMM: dx[T,d] (bf16, read-modify-write)
+ * += d_logits @ W_r^T; dW_r[d,E] = x^T @ d_logits; db[E] = column sums of
+ * d_logits (db may be NULL).  Deterministic (fixed reduction order; uses the
+ * workspace for split reductions). */
+int moe_router_logits_bwd(const moe_bf16_t* x, const float* W_r,
+                          const float* d_logits, int T, int d, int E,
+                          moe_bf16_t* dx, float* dW_r, float* db,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------- route map */
+
+/* Device-resident route map from topk_idx[T,k] (flattened slot s = t*k + j):
+ *   counts[E]       rows routed to each expert
+ *   offsets[E+1]    exclusive prefix sum of counts (offsets[E] = T*k)
+ *   row_of_slot[R]  row of the expert-sorted buffer that holds slot s:
+ *                   offsets[e] + number of slots s' < s routed to e (stable)
+ *   slot_of_row[R]  inverse permutation
+ * No host synchronisation.  An expert id outside [0, E) sets
+ * MOE_DEV_BAD_EXPERT_ID in the workspace status word. */
+int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E,
+                       int32_t* counts, int32_t* offsets,
+                       int32_t* row_of_slot, int32_t* slot_of_row,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------- dispatch/combine */
+
+/* Rowwise dispatch: xp[row_of_slot[t*k+j], :] = x[t, :] for all t, j.
+ * x[T,d] bf16 -> xp[T*k, d] bf16 (expert-contiguous).  Exact copy. */
+int moe_dispatch_rows(const moe_bf16_t* x, int T, int d, int k,
+                      const int32_t* row_of_slot, moe_bf16_t* xp,
+                      moe_stream_t stream);
+
+/* Combine: out[t,:] = sum_j gate[t,j] * yp[row_of_slot[t*k+j], :] with an
+ * fp32 sum in slot order, rounded once to bf16.  gate == NULL means all ones
+ * (the unpermute-sum of the backward: dX = sum_j dXp[row(t,j)]). */
+int moe_combine(const moe_bf16_t* yp, const int32_t* row_of_slot,
+                const float* gate, int T, int k, int d, moe_bf16_t* out,
+                moe_stream_t stream);
+
+/* Combine backward: dyp[row(t,j), :] = bf16(gate[t,j] * dout[t, :]) and
+ * dgate[t,j] = <dout[t,:], yp[row(t,j),:]> (fp32 accumulation). */
+int moe_combine_bwd(const moe_bf16_t* dout, const moe_bf16_t* yp,
+                    const int32_t* row_of_slot, const float* gate, int T,
+                    int k, int d, moe_bf16_t* dyp, float* dgate,
+                    moe_stream_t stream);
+
+/* ------------------------------------------------------ grouped SwiGLU GEMM */
+
+/* Forward of every expert's SwiGLU FFN on its rows of xp (expert e owns rows
+ * [offsets[e], offsets[e+1]) of the R = T*k rows; offsets is device memory):
+ *   h1 = xp_e @ W1[e],  h3 = xp_e @ W3[e],  a = silu(h1) * h3,  yp_e = a @ W2[e]
+ * xp[R,d], W1/W3[E,d,h], W2[E,h,d], h1/h3/a[R,h], yp[R,d]: bf16; fp32
+ * accumulation in tensor memory; a is computed from the fp32 accumulators.
+ * Two persistent tcgen05 kernels whose tile scheduler reads offsets on the
+ * device; no padding and no host synchronisation. */
+int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets,
+                           int R, int E, int d, int h,
+                           const moe_bf16_t* W1, const moe_bf16_t* W3,
+                           const moe_bf16_t* W2,
+                           moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a,
+                           moe_bf16_t* yp, void* ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/* Backward of moe_grouped_swiglu_fwd for the upstream gradient dyp[R,d]:
+ *   dA  = dyp_e @ W2[e]^T
+ *   dh1 = dA * h3 * silu'(h1)   (silu'(u) = s(u) (1 + u (1 - s(u))), s = sigmoid)
+ *   dh3 = dA * silu(h1)
+ *   dxp = dh1 @ W1[e]^T + dh3 @ W3[e]^T
+ *   dW2[e] = a_e^T @ dyp_e,  dW1[e] = xp_e^T @ dh1_e,  dW3[e] = xp_e^T @ dh3_e
+ * The weight gradients reduce over each expert's own row count (zero rows
+ * give exactly zero).  dh1/dh3[R,h] are caller-provided intermediates (also
+ * outputs).  dW1/dW3[E,d,h], dW2[E,h,d] bf16 from fp32 accumulators, no
+ * split-K, deterministic. */
+int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets,
+                           int R, int E, int d, int h,
+                           const moe_bf16_t* W1, const moe_bf16_t* W3,
+                           const moe_bf16_t* W2,
+                           const moe_bf16_t* h1, const moe_bf16_t* h3,
+                           const moe_bf16_t* a, const moe_bf16_t* dyp,
+                           moe_bf16_t* dh1, moe_bf16_t* dh3, moe_bf16_t* dxp,
+                           moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* LIBMOE_H */

@@ -1,0 +1,95 @@
+"""CPU checks of the C-ABI library: it builds for sm_103a, loads without a GPU,
+exports every entry point include/libmoe.h declares, and rejects bad host
+arguments before touching CUDA.  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from token_dispatch_grouped_router_gb300 import build as B
+from token_dispatch_grouped_router_gb300 import libmoe as LM
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "libmoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return LM.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 17
+    out = subprocess.run(["nm", "-D", "--defined-only", LM.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (moe_[a-z0-9_]+)\b", out))
+    for n in names:
+        assert n in exported, n
+        assert n in LM.SIGNATURES, n
+        assert getattr(lib, n) is not None
+    # and nothing exported that the header does not declare
+    assert exported == set(names)
+
+
+def test_status_strings_and_version(lib):
+    for st in (0, -1, -2, -3, -4):
+        assert lib.moe_status_string(st)
+    assert lib.moe_status_string(123).startswith(b"unknown")
+    assert lib.moe_version() == 100
+
+
+def test_workspace_size_grows_with_the_problem(lib):
+    small = lib.moe_workspace_size(512, 8, 2, 256, 512)
+    big = lib.moe_workspace_size(32768, 128, 4, 2048, 1024)
+    assert 256 <= small < big
+    # route-map scratch: per-chunk histograms + one rank per routed slot
+    R = 32768 * 4
+    assert big >= 256 + (R // 1024) * 128 * 4 + R * 4
+    assert lib.moe_workspace_size(-1, 8, 2, 256, 512) == 0
+
+
+def test_host_argument_checks_return_before_any_cuda_call(lib):
+    NULL = None
+    fake = ctypes.c_void_p(0x1000)   # aligned, never dereferenced: checks fail first
+    # k out of range / k > E
+    assert lib.moe_router_topk(fake, 4, 8, 0, fake, fake, NULL) == -1
+    assert lib.moe_router_topk(fake, 4, 8, 9, fake, fake, NULL) == -1
+    assert lib.moe_router_topk(fake, 4, 2000, 2, fake, fake, NULL) == -1
+    # null or misaligned pointers
+    assert lib.moe_router_topk(NULL, 4, 8, 2, fake, fake, NULL) == -1
+    assert lib.moe_router_topk(ctypes.c_void_p(0x1001), 4, 8, 2, fake, fake, NULL) == -1
+    assert lib.moe_dispatch_rows(fake, 4, 12, 2, fake, fake, NULL) == -1        # d % 8
+    # grouped GEMMs need d, h multiples of 64
+    assert lib.moe_grouped_swiglu_fwd(fake, fake, 8, 4, 96, 128, fake, fake, fake, fake, fake,
+                                      fake, fake, fake, 1 << 20, NULL) == -2
+    # workspace too small / missing
+    assert lib.moe_grouped_swiglu_fwd(fake, fake, 8, 4, 128, 128, fake, fake, fake, fake, fake,
+                                      fake, fake, fake, 16, NULL) == -3
+    assert lib.moe_expert_offsets(fake, 4, 2, 8, fake, fake, fake, fake, NULL, 0, NULL) == -3
+    assert lib.moe_expert_offsets(fake, 1024, 2, 8, fake, fake, fake, fake, fake, 300, NULL) == -3
+    assert lib.moe_get_status(NULL, NULL, NULL) == -3
+    # T = 0 is a no-op that succeeds without launching anything
+    before = lib.moe_launch_count()
+    assert lib.moe_router_topk(NULL, 0, 8, 2, NULL, NULL, NULL) == 0
+    assert lib.moe_combine(NULL, NULL, NULL, 0, 2, 256, NULL, NULL) == 0
+    assert lib.moe_launch_count() == before
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    saved = LM._lib
+    try:
+        LM._lib = None
+        with pytest.raises(RuntimeError, match="not found"):
+            LM.load(str(tmp_path / "missing.so"))
+    finally:
+        LM._lib = saved

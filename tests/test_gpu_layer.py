@@ -1,0 +1,304 @@
+"""GPU parity of the whole layer (forward + backward) against the fp64 oracle.
+
+Small problems are compared tensor by tensor; the full-size workloads are
+compared bit-exactly on the routing metadata and on sampled tokens and
+experts that the oracle recomputes one by one.  Learned routers: both sides
+route on the oracle's fp32 logits, passed to the device top-k through the C
+ABI; the device's own logits GEMM is compared with tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.layer as ol
+from token_dispatch_grouped_router_gb300 import libmoe as L
+from token_dispatch_grouped_router_gb300 import workloads as wl
+from token_dispatch_grouped_router_gb300.layer import MoELayer
+
+from gpu_helpers import assert_close, as_f64, ensure_built, i32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+    L.load()
+
+
+def make_layer(w, inp, backward=True, logits=None):
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=(w.routing == "learned"),
+                     device=DEV, with_backward=backward)
+    layer.load_inputs(inp)
+    if w.routing == "learned":
+        layer.load_logits(logits if logits is not None
+                          else ol.router_logits(inp["x"], inp["W_r"], inp.get("b")))
+    return layer
+
+
+def run(layer, backward=True):
+    L.moe_reset_status(layer.ws)
+    layer.forward()
+    if backward:
+        layer.backward()
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+
+
+def compare_full(layer, w, inp, backward=True):
+    z = None
+    if w.routing == "learned":
+        z = layer.logits.cpu().numpy()
+    ref = ol.layer_forward(inp, w.k, w.E, logits=z)
+    assert np.array_equal(i32(layer.idx), ref["idx"])
+    assert np.array_equal(i32(layer.counts), ref["counts"])
+    assert np.array_equal(i32(layer.offsets), ref["offsets"])
+    assert np.array_equal(i32(layer.row_of_slot), ref["row_of_slot"])
+    assert np.array_equal(i32(layer.slot_of_row), ref["slot_of_row"])
+    assert np.array_equal(as_f64(layer.xp), ref["Xp"])
+    assert_close(layer.gate, ref["g"], "gate", rel_l2=1e-6, max_abs=1e-6)
+    for n, key in (("h1", "H1"), ("h3", "H3"), ("a", "A"), ("yp", "Yp"), ("out", "out")):
+        assert_close(getattr(layer, n), ref[key], n)
+    if not backward:
+        return ref, None
+    refb = ol.layer_backward(inp, ref, w.k, w.E)
+    for n, key in (("dyp", "dYp"), ("dgate", "dg"), ("dh1", "dH1"), ("dh3", "dH3"),
+                   ("dxp", "dXp"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2"),
+                   ("dX", "dX"), ("dlogits", "dz")):
+        assert_close(getattr(layer, n), refb[key], n)
+    if w.routing == "learned":
+        assert_close(layer.dW_r, refb["dW_r"], "dW_r")
+        assert_close(layer.db, refb["db"], "db")
+    # an expert with no rows gets exactly zero weight gradients
+    for e in np.nonzero(ref["counts"] == 0)[0]:
+        for n in ("dW1", "dW3", "dW2"):
+            assert torch.count_nonzero(getattr(layer, n)[e]).item() == 0, (n, e)
+    return ref, refb
+
+
+@pytest.mark.parametrize("T,d,E,k,h,empty", [
+    (300, 128, 6, 2, 192, (3,)),        # ragged rows, h not a multiple of 128
+    (200, 256, 3, 1, 64, ()),           # one 64-wide hidden tile
+    (513, 192, 8, 4, 320, (0, 7)),      # d and h off the 256 grid, empty ends
+    (1000, 512, 16, 4, 256, (5,)),      # several tiles per expert
+    (64, 128, 1, 1, 128, ()),           # a single dense expert
+])
+def test_layer_small_full_compare(T, d, E, k, h, empty):
+    w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
+    inp = wl.generate(w, seed=1)
+    if empty:
+        keep = [e for e in range(E) if e not in empty]
+        rng = np.random.default_rng(2)
+        inp["idx"] = np.stack([rng.permutation(keep)[:k] for _ in range(T)]).astype(np.int32)
+    layer = make_layer(w, inp)
+    run(layer)
+    ref, _ = compare_full(layer, w, inp)
+    for e in empty:
+        assert ref["counts"][e] == 0
+
+
+def test_layer_learned_router_zipf_full_compare():
+    w = wl.small_workload(T=640, d=256, E=32, k=4, h=192, routing="learned", zipf=True)
+    inp = wl.generate(w, seed=0)
+    layer = make_layer(w, inp)
+    run(layer)
+    ref, _ = compare_full(layer, w, inp)
+    assert (ref["counts"] == 0).sum() >= 1 and ref["counts"].max() > 4 * ref["counts"].mean()
+
+
+def test_tiny_workload_forward_full_compare():
+    w = wl.get_workload("tiny_e8")
+    inp = wl.generate(w, seed=0)
+    layer = make_layer(w, inp, backward=False)
+    run(layer, backward=False)
+    compare_full(layer, w, inp, backward=False)
+    # the device's own router GEMM matches the oracle's logits
+    zdev = torch.empty_like(layer.logits)
+    L.moe_router_logits(layer.x, layer.W_r, layer.b, zdev)
+    assert_close(zdev, ol.router_logits(inp["x"], inp["W_r"], None, np.float64), "logits",
+                 rel_l2=1e-5, max_abs=1e-5)
+
+
+def test_graph_capture_proves_no_host_sync_and_replays_bitwise():
+    w = wl.small_workload(T=700, d=256, E=8, k=2, h=128, routing="learned", zipf=True)
+    inp = wl.generate(w, seed=4)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=True, device=DEV)
+    layer.load_inputs(inp)
+    layer.step()                 # eager reference (device router logits included)
+    torch.cuda.synchronize()
+    eager = {n: getattr(layer, n).clone() for n in ("idx", "offsets", "out", "dX", "dW1", "dW2", "dW_r")}
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        # any host synchronisation or device->host copy inside would break capture
+        with torch.cuda.graph(g, stream=s):
+            layer.step()
+    for buf in ("out", "dX", "dW1", "dW2", "dW_r"):
+        getattr(layer, buf).zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for n, v in eager.items():
+        assert torch.equal(getattr(layer, n), v), n
+
+
+def test_deterministic_bitwise():
+    w = wl.small_workload(T=2000, d=256, E=16, k=4, h=256)
+    inp = wl.generate(w, seed=5)
+    layer = make_layer(w, inp)
+    run(layer)
+    first = {n: getattr(layer, n).clone() for n in ("out", "dgate", "dxp", "dW1", "dW3", "dW2", "dX")}
+    run(layer)
+    for n, v in first.items():
+        assert torch.equal(getattr(layer, n), v), n
+
+
+def test_outputs_stay_inside_their_buffers():
+    # every output is a view at the front of a larger buffer whose tail holds a
+    # sentinel; a write past the end of any output would change it
+    w = wl.small_workload(T=333, d=192, E=5, k=2, h=320)
+    inp = wl.generate(w, seed=6)
+    layer = make_layer(w, inp)
+    guards = {}
+    for n in ("xp", "h1", "h3", "a", "yp", "out", "dyp", "dgate", "dh1", "dh3", "dxp", "dW1",
+              "dW3", "dW2", "dX", "dlogits", "row_of_slot", "slot_of_row", "counts", "offsets"):
+        t = getattr(layer, n)
+        big = torch.empty(t.numel() + 4096, dtype=t.dtype, device=DEV)
+        big.view(torch.uint8)[:].fill_(0xA5)
+        view = big[:t.numel()].view(t.shape)
+        view.copy_(t)
+        setattr(layer, n, view)
+        guards[n] = big
+    run(layer)
+    for n, big in guards.items():
+        tail = big[-4096:].view(torch.uint8)
+        assert bool((tail == 0xA5).all()), f"{n} written past its end"
+    compare_full(layer, w, inp)
+
+
+def test_zero_tokens_gives_zero_weight_gradients():
+    w = wl.small_workload(T=0, d=128, E=4, k=2, h=128)
+    layer = MoELayer(0, 128, 4, 2, 128, learned=False, device=DEV)
+    for n in ("W1", "W3", "W2"):
+        getattr(layer, n).normal_()
+    for n in ("dW1", "dW3", "dW2"):
+        getattr(layer, n).fill_(1.0)
+    run(layer)
+    for n in ("dW1", "dW3", "dW2"):
+        assert torch.count_nonzero(getattr(layer, n)).item() == 0
+    assert i32(layer.offsets).sum() == 0
+
+
+def test_argument_errors_on_device_buffers():
+    x = torch.zeros(8, 96, dtype=torch.bfloat16, device=DEV)
+    W = torch.zeros(2, 96, 128, dtype=torch.bfloat16, device=DEV)
+    W2 = torch.zeros(2, 128, 96, dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros(3, dtype=torch.int32, device=DEV)
+    hbuf = torch.zeros(8, 128, dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(L.MoEError) as ei:
+        L.moe_grouped_swiglu_fwd(x, o, W, W, W2, hbuf, hbuf, hbuf, x, ws)
+    assert ei.value.status == -2           # d = 96 is not a multiple of 64
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------- full-size workloads
+
+def _sampled_reference(inp, w, idx, g, ros, toks, hs, experts):
+    """Oracle values for the sampled tokens (forward + backward rows) and for
+    sampled hidden units of the sampled experts' weight gradients."""
+    k = w.k
+    x = ol.decode_bf16(inp["x"]); dY = ol.decode_bf16(inp["dY"])
+    res = {"yp": [], "h1": [], "out": [], "dxp": [], "dgate": [], "dX": [], "rows": []}
+    for t in toks:
+        rows = ros[t * k:(t + 1) * k]
+        out_t = np.zeros(w.d); dX_t = np.zeros(w.d)
+        dg_t = np.zeros(k)
+        for j in range(k):
+            e = int(idx[t, j])
+            f = ol.expert_ffn_forward(x[t:t + 1], [0, 1], inp["W1"][e:e + 1],
+                                      inp["W3"][e:e + 1], inp["W2"][e:e + 1])
+            dyp = g[t, j] * dY[t:t + 1]
+            b = ol.expert_ffn_backward(x[t:t + 1], [0, 1], inp["W1"][e:e + 1],
+                                       inp["W3"][e:e + 1], inp["W2"][e:e + 1],
+                                       f["H1"], f["H3"], f["A"], dyp)
+            res["yp"].append(f["Yp"][0]); res["h1"].append(f["H1"][0]); res["dxp"].append(b["dXp"][0])
+            res["rows"].append(int(rows[j]))
+            out_t += g[t, j] * f["Yp"][0]
+            dX_t += b["dXp"][0]
+            dg_t[j] = float(dY[t] @ f["Yp"][0])
+        res["out"].append(out_t); res["dX"].append(dX_t); res["dgate"].append(dg_t)
+    # weight gradients of sampled experts, restricted to hidden units hs
+    wg = {}
+    c, off, _, sor = ol.route_map(idx, w.E)
+    for e in experts:
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            wg[e] = None
+            continue
+        slots = sor[lo:hi].astype(np.int64)
+        X = x[slots // k]
+        dyp = g[slots // k, slots % k][:, None] * dY[slots // k]
+        W1s = inp["W1"][e][:, hs][None]; W3s = inp["W3"][e][:, hs][None]
+        W2s = inp["W2"][e][hs, :][None]
+        f = ol.expert_ffn_forward(X, [0, hi - lo], W1s, W3s, W2s)
+        b = ol.expert_ffn_backward(X, [0, hi - lo], W1s, W3s, W2s, f["H1"], f["H3"], f["A"], dyp)
+        wg[e] = (b["dW1"][0], b["dW3"][0], b["dW2"][0])
+    return res, wg
+
+
+@pytest.mark.parametrize("key", ["dense_e8", "pool_e128", "skew_e128", "train_e128"])
+def test_full_size_sampled(key):
+    w = wl.get_workload(key)
+    inp = wl.generate(w, seed=0)
+    zref = None
+    if w.routing == "learned":
+        zref = ol.router_logits(inp["x"], inp["W_r"], inp.get("b"))
+    layer = make_layer(w, inp, logits=zref)
+    run(layer)
+    # routing metadata, bit-exact over the whole step
+    if w.routing == "learned":
+        idx = ol.topk(zref, w.k)
+        g = ol.topk_gates(zref, idx)
+    else:
+        idx = inp["idx"]
+        g = ol.softmax_gates(inp["glogit"])
+    c, off, ros, sor = ol.route_map(idx, w.E)
+    assert np.array_equal(i32(layer.idx), idx)
+    assert np.array_equal(i32(layer.counts), c) and np.array_equal(i32(layer.offsets), off)
+    assert np.array_equal(i32(layer.row_of_slot), ros) and np.array_equal(i32(layer.slot_of_row), sor)
+    assert_close(layer.gate, g, "gate", rel_l2=1e-6, max_abs=1e-6)
+    rng = np.random.default_rng(7)
+    toks = np.sort(rng.choice(w.T, 24, replace=False))
+    hs = np.sort(rng.choice(w.h, 16, replace=False))
+    nonempty = np.nonzero(c)[0]
+    experts = sorted({int(nonempty[np.argmax(c[nonempty])]), int(nonempty[np.argmin(c[nonempty])]),
+                      int(rng.choice(nonempty))} | set(int(e) for e in np.nonzero(c == 0)[0][:1]))
+    res, wg = _sampled_reference(inp, w, idx, g, ros, toks, hs, experts)
+    rows = torch.tensor(res["rows"], device=DEV, dtype=torch.long)
+    tk = torch.tensor(toks, device=DEV, dtype=torch.long)
+    # dispatch is an exact copy
+    xp_rows = as_f64(layer.xp[rows])
+    assert np.array_equal(xp_rows, ol.decode_bf16(inp["x"])[np.repeat(toks, w.k)])
+    assert_close(layer.yp[rows], np.array(res["yp"]), "yp")
+    assert_close(layer.h1[rows], np.array(res["h1"]), "h1")
+    assert_close(layer.out[tk], np.array(res["out"]), "out")
+    assert_close(layer.dxp[rows], np.array(res["dxp"]), "dxp")
+    assert_close(layer.dgate[tk], np.array(res["dgate"]), "dgate")
+    if w.routing == "uniform":
+        assert_close(layer.dX[tk], np.array(res["dX"]), "dX")
+    hst = torch.tensor(hs, device=DEV, dtype=torch.long)
+    for e, v in wg.items():
+        if v is None:
+            for n in ("dW1", "dW3", "dW2"):
+                assert torch.count_nonzero(getattr(layer, n)[e]).item() == 0
+            continue
+        assert_close(layer.dW1[e][:, hst], v[0], f"dW1[{e}]")
+        assert_close(layer.dW3[e][:, hst], v[1], f"dW3[{e}]")
+        assert_close(layer.dW2[e][hst, :], v[2], f"dW2[{e}]")
+    if w.routing == "learned":
+        # the device's own router GEMM agrees with the oracle's logits
+        zdev = torch.empty_like(layer.logits)
+        L.moe_router_logits(layer.x, layer.W_r, layer.b, zdev)
+        zd = zdev[tk].cpu().numpy()
+        assert_close(zd, ol.router_logits(ol.decode_bf16(inp["x"])[toks], inp["W_r"], inp["b"],
+                                          np.float64), "logits", rel_l2=1e-5, max_abs=1e-5)

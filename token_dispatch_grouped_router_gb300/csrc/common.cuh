@@ -1,0 +1,102 @@
+// Shared host/device helpers of libmoe: status handling, launch accounting,
+// workspace layout and small device utilities.  sm_103a only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/libmoe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- host side
+
+// Counts every kernel this library enqueues (see moe_launch_count).
+void note_launches(int n);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Current device ordinal.
+int current_device();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define MOE_CHECK_ARG(cond) do { if (!(cond)) return MOE_ERR_INVALID_ARG; } while (0)
+#define MOE_CHECK_PTR(p) do { if ((p) == nullptr || !::moe::aligned16(p)) return MOE_ERR_INVALID_ARG; } while (0)
+#define MOE_LAUNCH_CHECK(n) do { ::moe::note_launches(n); \
+    if (cudaPeekAtLastError() != cudaSuccess) { (void)cudaGetLastError(); return MOE_ERR_CUDA; } } while (0)
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 8;
+
+// Workspace layout (bytes from the start of ws):
+//   [0, 256)   status word (int32) + padding
+//   [256, ..)  scratch shared by the calls that need it; each call uses it
+//              only while its own kernels run, so the regions may overlap:
+//              moe_expert_offsets: per-chunk histograms [chunks][E] int32,
+//                                  then in-chunk stable ranks [R] int32;
+//              moe_router_logits_bwd: dW_r split-K partials [splits][d][E] f32.
+constexpr size_t kStatusBytes = 256;
+constexpr int kRouteChunk = 1024;     // slots per route-map block
+constexpr int kRouterSplits = 16;     // deterministic split-K for dW_r
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct RouteScratch { size_t chunk_counts, local_rank, end; };
+
+inline RouteScratch route_scratch(long long R, int E) {
+  long long chunks = (R + kRouteChunk - 1) / kRouteChunk;
+  RouteScratch L;
+  L.chunk_counts = kStatusBytes;
+  L.local_rank = round_up(L.chunk_counts + (size_t)chunks * E * 4, 256);
+  L.end = round_up(L.local_rank + (size_t)R * 4, 256);
+  return L;
+}
+
+inline size_t router_scratch_end(int E, int d) {
+  return round_up(kStatusBytes + (size_t)kRouterSplits * d * E * 4, 256);
+}
+
+inline size_t workspace_bytes(long long T, int E, int k, int d) {
+  size_t a = route_scratch(T * (long long)k, E).end;
+  size_t b = router_scratch_end(E, d);
+  return a > b ? a : b;
+}
+
+// -------------------------------------------------------------- device side
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16x2 (round to nearest even), low half = a.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace moe

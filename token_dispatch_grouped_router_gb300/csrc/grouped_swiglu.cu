@@ -1,0 +1,675 @@
+// Unpadded grouped SwiGLU GEMMs on tcgen05 tensor cores (forward and backward).
+//
+// "OLMo-core 3：MoE 训练栈让专家池越大、吞吐不再越慢", section "另外两处税：主机同步
+// 与 padding": all small expert GEMMs are merged into one kernel schedule that
+// runs every expert on exactly the row count the device route map gives, with
+// no padding to a common capacity (no wasted FLOPs, no per-expert host
+// launches).  The same page's layer map puts this in a CUTLASS grouped GEMM on
+// B300; nothing here comes from CUTLASS: the kernel is written directly
+// against tcgen05/TMEM/TMA for sm_103a.  The expert network (SwiGLU,
+// W2(silu(x W1) * (x W3))) is the benchmark specification's reading; the
+// pages only say "FFN".  The backward GEMMs are the Dgrad and Wgrad GEMMs
+// named in the tutorial's DeepSeek-V3 paragraph (section "一个低精度格式，同时压三个地方").
+//
+// One persistent kernel template, five modes:
+//   UP : [h1 | h3] = xp_e @ [W1[e] | W3[e]],  epilogue a = silu(h1) * h3
+//   DOWN: yp = a_e @ W2[e]
+//   DA : dA = dyp_e @ W2[e]^T, epilogue dh1 = dA*h3*silu'(h1), dh3 = dA*silu(h1)
+//   DX : dxp = [dh1 | dh3]_e @ [W1[e] | W3[e]]^T   (K = 2h)
+//   WG : dW1[e] = xp_e^T dh1_e, dW3[e] = xp_e^T dh3_e, dW2[e] = a_e^T dyp_e
+//        (the reduction runs over the expert's own rows; K = n_e varies)
+//
+// Tiles are 128 x 256 (BM x BN) with BK = 64; every CTA loops over tiles
+// t = blockIdx.x, blockIdx.x + gridDim.x, ... in expert-major order, so the
+// CTAs working at one time share an expert's weight tile in L2.  The row
+// groups come from `offsets` read on the device: nothing is padded and the
+// host never learns the row counts.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads into a 4-stage shared
+// memory ring; warp 1 allocates 512 TMEM columns (two 128x256 fp32
+// accumulators) and one of its lanes issues tcgen05.mma; warps 2-5 drain a
+// finished accumulator (tcgen05.ld) while the next tile accumulates into the
+// other one.  Every mbarrier wait is bounded: on timeout the kernel records
+// MOE_DEV_WAIT_TIMEOUT, waits (bounded) for its own in-flight copies and
+// MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+enum Mode : int { kUp = 0, kDown = 1, kDA = 2, kDX = 3, kWG = 4 };
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;            // 16 KB
+constexpr int B_STAGE = BN * BK * 2;            // 32 KB
+constexpr int SUB = 64 * 64 * 2;                // one 64x64 bf16 TMA box (8 KB)
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s; a step takes milliseconds
+
+struct GemmArgs {
+  const int32_t* offsets;   // [E+1], device
+  int E, R, d, h;
+  int n_tiles;              // N tiles per expert (row-grouped modes)
+  int kb_total;             // k-blocks per tile (row-grouped modes)
+  int kb_split;             // DX: k-blocks taken from (dh1, W1) before (dh3, W3)
+  uint16_t* out0;
+  uint16_t* out1;
+  uint16_t* out2;
+  const uint16_t* in0;      // DA: h1
+  const uint16_t* in1;      // DA: h3
+  int ldo;                  // row stride (elements) of the row-grouped outputs
+  int* status;
+  int wg_t1, wg_t2;         // WG: tiles per expert of dW1 (= dW3) and of dW2
+  int wg_mt1, wg_mt2;       // WG: M tiles of dW1 (d/128) and dW2 (h/128)
+};
+
+struct Tile {
+  int e, row0, rows, m0, n0, nkb, which, krow0, krows;
+};
+
+struct Shared {
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+};
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Shared* sh, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 127u) == 0) {
+      if (*(volatile int*)&sh->abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *(volatile int*)&sh->abort_flag = 1;
+        set_status(status, MOE_DEV_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// wait used only while draining after an abort: bounded, reports nothing
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int* s_off,
+                                            const int* s_ts) {
+  Tile tl{};
+  if constexpr (MODE == kWG) {
+    const int per = 2 * a.wg_t1 + a.wg_t2;
+    tl.e = t / per;
+    int l = t - tl.e * per;
+    int mt;
+    if (l < a.wg_t1) { tl.which = 0; mt = a.wg_mt1; }
+    else if (l < 2 * a.wg_t1) { tl.which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
+    else { tl.which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
+    tl.m0 = (l % mt) * BM;
+    tl.n0 = (l / mt) * BN;
+    int lo = s_off[tl.e], hi = s_off[tl.e + 1];
+    lo = max(0, min(lo, a.R));
+    hi = max(lo, min(hi, a.R));
+    tl.krow0 = lo;
+    tl.krows = hi - lo;
+    tl.nkb = (tl.krows + BK - 1) / BK;
+  } else {
+    // expert e owns tiles [s_ts[e], s_ts[e+1]): largest e with s_ts[e] <= t
+    int lo = 0, hi = a.E;               // invariant: s_ts[lo] <= t < s_ts[hi]
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (s_ts[mid] <= t) lo = mid; else hi = mid;
+    }
+    tl.e = lo;
+    int seg0 = max(0, min(s_off[lo], a.R));
+    int seg1 = max(seg0, min(s_off[lo + 1], a.R));
+    int ne = seg1 - seg0;
+    int mt = (ne + BM - 1) / BM;
+    int l = t - s_ts[lo];
+    int m_idx = l % mt, n_idx = l / mt;
+    tl.row0 = seg0 + m_idx * BM;
+    tl.rows = min(BM, seg1 - tl.row0);
+    tl.n0 = n_idx * (MODE == kUp ? BN / 2 : BN);
+    tl.nkb = a.kb_total;
+  }
+  return tl;
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa, uint32_t sb,
+                                            uint32_t bar, const CUtensorMap* a0,
+                                            const CUtensorMap* a1, const CUtensorMap* b0,
+                                            const CUtensorMap* b1, const CUtensorMap* b2,
+                                            const GemmArgs& a) {
+  if constexpr (MODE == kUp) {
+    tma_load_2d(sa, a0, bar, kb * BK, tl.row0);
+    tma_load_3d(sb + 0 * SUB, b0, bar, tl.n0, kb * BK, tl.e);
+    tma_load_3d(sb + 1 * SUB, b0, bar, tl.n0 + 64, kb * BK, tl.e);
+    tma_load_3d(sb + 2 * SUB, b1, bar, tl.n0, kb * BK, tl.e);
+    tma_load_3d(sb + 3 * SUB, b1, bar, tl.n0 + 64, kb * BK, tl.e);
+  } else if constexpr (MODE == kDown) {
+    tma_load_2d(sa, a0, bar, kb * BK, tl.row0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_3d(sb + c * SUB, b0, bar, tl.n0 + 64 * c, kb * BK, tl.e);
+  } else if constexpr (MODE == kDA) {
+    tma_load_2d(sa, a0, bar, kb * BK, tl.row0);
+    tma_load_3d(sb, b0, bar, kb * BK, tl.n0, tl.e);
+  } else if constexpr (MODE == kDX) {
+    const bool second = kb >= a.kb_split;
+    const int kk = (second ? kb - a.kb_split : kb) * BK;
+    tma_load_2d(sa, second ? a1 : a0, bar, kk, tl.row0);
+    tma_load_3d(sb, second ? b1 : b0, bar, kk, tl.n0, tl.e);
+  } else {  // kWG
+    const int y = tl.krow0 + kb * BK;
+    const CUtensorMap* am = tl.which == 2 ? a1 : a0;
+    const CUtensorMap* bm = tl.which == 0 ? b0 : (tl.which == 1 ? b1 : b2);
+    tma_load_2d(sa, am, bar, tl.m0, y);
+    tma_load_2d(sa + SUB, am, bar, tl.m0 + 64, y);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * SUB, bm, bar, tl.n0 + 64 * c, y);
+  }
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.f + __expf(-x)); }
+
+__device__ __forceinline__ void store_row32(uint16_t* dst, const float* v) {
+  uint4 o[4];
+  uint32_t* w = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) st_v4(dst + 8 * i, o[i]);
+}
+
+__device__ __forceinline__ void load_row32(const uint16_t* src, float* v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 q = ld_nc_v4(src + 8 * i);
+    v[8 * i + 0] = bf16_lo(q.x); v[8 * i + 1] = bf16_hi(q.x);
+    v[8 * i + 2] = bf16_lo(q.y); v[8 * i + 3] = bf16_hi(q.y);
+    v[8 * i + 4] = bf16_lo(q.z); v[8 * i + 5] = bf16_hi(q.z);
+    v[8 * i + 6] = bf16_lo(q.w); v[8 * i + 7] = bf16_hi(q.w);
+  }
+}
+
+// Epilogue of one tile for the 32 rows of this warp's TMEM lane quarter.
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int lane_q,
+                                              int lane, const GemmArgs& a) {
+  const int r = lane_q * 32 + lane;                 // row inside the tile
+  const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
+  if constexpr (MODE == kWG) {
+    const int M = tl.which == 2 ? a.h : a.d;
+    const int N = tl.which == 2 ? a.d : a.h;
+    uint16_t* out = tl.which == 0 ? a.out0 : (tl.which == 1 ? a.out1 : a.out2);
+    const int grow = tl.m0 + r;
+    const bool rv = grow < M;
+    uint16_t* dst = out + ((size_t)tl.e * M + (rv ? grow : 0)) * N;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      if (tl.nkb > 0) {
+        uint32_t q[32];
+        tmem_ld32(tbase + c * 32, q);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(q[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+      const int col = tl.n0 + c * 32;
+      if (rv && col < N) store_row32(dst + col, v);
+    }
+  } else {
+    const int grow = tl.row0 + r;
+    const bool rv = r < tl.rows;
+    const size_t ro = (size_t)(rv ? grow : 0) * a.ldo;
+    if constexpr (MODE == kUp) {
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t q1[32], q3[32];
+        tmem_ld32(tbase + c * 32, q1);
+        tmem_ld32(tbase + 128 + c * 32, q3);
+        tmem_ld_wait();
+        const int col = tl.n0 + c * 32;
+        if (rv && col < a.h) {
+          float h1[32], h3[32], av[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            h1[i] = __uint_as_float(q1[i]);
+            h3[i] = __uint_as_float(q3[i]);
+            av[i] = silu_f(h1[i]) * h3[i];
+          }
+          store_row32(a.out0 + ro + col, h1);
+          store_row32(a.out1 + ro + col, h3);
+          store_row32(a.out2 + ro + col, av);
+        }
+      }
+    } else if constexpr (MODE == kDA) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t q[32];
+        tmem_ld32(tbase + c * 32, q);
+        tmem_ld_wait();
+        const int col = tl.n0 + c * 32;
+        if (rv && col < a.h) {
+          float h1[32], h3[32], g1[32], g3[32];
+          load_row32(a.in0 + ro + col, h1);
+          load_row32(a.in1 + ro + col, h3);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float da = __uint_as_float(q[i]);
+            const float s = 1.f / (1.f + __expf(-h1[i]));
+            g1[i] = da * h3[i] * s * (1.f + h1[i] * (1.f - s));
+            g3[i] = da * h1[i] * s;
+          }
+          store_row32(a.out0 + ro + col, g1);
+          store_row32(a.out1 + ro + col, g3);
+        }
+      }
+    } else {  // kDown, kDX: plain bf16 store of the accumulator
+      const int N = a.d;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t q[32];
+        tmem_ld32(tbase + c * 32, q);
+        tmem_ld_wait();
+        const int col = tl.n0 + c * 32;
+        if (rv && col < N) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(q[i]);
+          store_row32(a.out0 + ro + col, v);
+        }
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  Shared* sh = reinterpret_cast<Shared*>(sB + STAGES * B_STAGE);
+  int* s_off = reinterpret_cast<int*>(sh + 1);
+  int* s_ts = s_off + (args.E + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- set-up: tile table from the device offsets, barriers, TMEM
+  for (int i = threadIdx.x; i <= args.E; i += kThreads) s_off[i] = __ldg(args.offsets + i);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) { mbar_init(smem_u32(&sh->full[s]), 1); mbar_init(smem_u32(&sh->empty[s]), 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(smem_u32(&sh->tfull[s]), 1); mbar_init(smem_u32(&sh->tempty[s]), 4); }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if constexpr (MODE == kWG) {
+    if (threadIdx.x == 0) sh->total_tiles = args.E * (2 * args.wg_t1 + args.wg_t2);
+  } else {
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < args.E; base += 32) {
+        const int e = base + lane;
+        int cnt = 0;
+        if (e < args.E) {
+          int lo = max(0, min(s_off[e], args.R));
+          int hi = max(lo, min(s_off[e + 1], args.R));
+          cnt = ((hi - lo + BM - 1) / BM) * args.n_tiles;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (e < args.E) s_ts[e] = carry + incl - cnt;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) { s_ts[args.E] = carry; sh->total_tiles = carry; }
+    }
+  }
+  __syncthreads();
+  const int total = sh->total_tiles;
+  if ((int)blockIdx.x >= total) return;      // uniform across the CTA; no TMEM taken yet
+
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmB0);
+    prefetch_tmap(&tmB1); prefetch_tmap(&tmB2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    // the whole warp walks the schedule (converged); lane 0 issues the copies
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, last_par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
+      for (int kb = 0; kb < tl.nkb; ++kb) {
+        if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&sh->full[stage]);
+          mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
+          issue_loads<MODE>(tl, kb, smem_u32(sA + stage * A_STAGE), smem_u32(sB + stage * B_STAGE),
+                            fb, &tmA0, &tmA1, &tmB0, &tmB1, &tmB2, args);
+        }
+        __syncwarp();
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      // let every copy this CTA started land before shared memory goes away
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) drain_wait(smem_u32(&sh->full[s]), (last_par >> s) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    constexpr bool a_mn = (MODE == kWG);
+    constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kWG);
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, a_mn, b_mn);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued_any = false;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
+      if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, sh, args.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t dt = tmem + (uint32_t)(acc * BN);
+      if (tl.nkb == 0) {
+        if (lane == 0) mbar_arrive(smem_u32(&sh->tfull[acc]));
+      } else {
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, sh, args.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sA + stage * A_STAGE);
+          const uint32_t sb = smem_u32(sB + stage * B_STAGE);
+          if constexpr (MODE == kWG) {
+            // last block of a ragged reduction: rows past the expert's end
+            // belong to the next expert (or were zero-filled); clear them
+            const int valid = tl.krows - kb * BK;
+            if (valid < BK) {
+              uint4 z = make_uint4(0, 0, 0, 0);
+              const int nrows = BK - valid;
+              for (int i = lane; i < 6 * nrows * 8; i += 32) {
+                const int sub = i / (nrows * 8);
+                const int rem = i - sub * nrows * 8;
+                const int row = valid + rem / 8, chunk = rem % 8;
+                uint8_t* base = sub < 2 ? (sA + stage * A_STAGE + sub * SUB)
+                                        : (sB + stage * B_STAGE + (sub - 2) * SUB);
+                *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = z;
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              uint64_t ad, bd;
+              if constexpr (a_mn) ad = sdesc_sw128(sa + kk * 2048, SUB, 1024);
+              else ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
+              else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+              mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&sh->empty[stage]));
+          }
+          issued_any = true;
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(smem_u32(&sh->tfull[acc]));
+        __syncwarp();
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (!ok && issued_any && lane == 0) {
+      // wait for the tensor core to finish reading shared memory / writing TMEM
+      mma_commit(smem_u32(&sh->drain));
+      drain_wait(smem_u32(&sh->drain), 0);
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int lane_q = warp & 3;          // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
+      if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, sh, args.status)) break;
+      tc_fence_after();
+      epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * BN), lane_q, lane, args);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      (void)cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] tensor, box [box_outer, box_inner]
+bool map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+           uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over a row-major [outer, mid, inner] tensor, box [1, box_mid, box_inner]
+bool map3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t mid, uint64_t outer,
+           uint32_t box_inner, uint32_t box_mid) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+  cuuint32_t box[3] = {box_inner, box_mid, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t smem_bytes(int E) {
+  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
+}
+
+template <int MODE>
+int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+           const CUtensorMap& b1, const CUtensorMap& b2, const GemmArgs& args, int grid,
+           cudaStream_t s) {
+  const size_t smem = smem_bytes(args.E);
+  auto kern = grouped_gemm_kernel<MODE>;
+  // the attribute is set once per device for the largest size (E = 1024), so
+  // no non-stream CUDA call happens on later (possibly graph-captured) calls
+  static bool attr_set[64] = {false};
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes(kMaxExperts)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    attr_set[dev] = true;
+  }
+  kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, b2, args);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int check_common(const void* ws, size_t ws_bytes, int R, int E, int d, int h) {
+  if (R < 0 || E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 64 != 0 || h % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < kStatusBytes) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int row_grid_upper(int R, int E, int n_tiles) {
+  // tiles <= (ceil(R/BM) + E) * n_tiles; CTAs beyond the real count exit at once
+  long long ub = ((long long)(R + BM - 1) / BM + E) * n_tiles;
+  long long g = sm_count();
+  return (int)(ub < g ? (ub > 0 ? ub : 1) : g);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
+                           const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                           moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a, moe_bf16_t* yp, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  int st = check_common(ws, ws_bytes, R, E, d, h);
+  if (st != MOE_OK) return st;
+  if (R == 0) return MOE_OK;
+  MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3);
+  MOE_CHECK_PTR(W2); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(a); MOE_CHECK_PTR(yp);
+  cudaStream_t s = (cudaStream_t)stream;
+  CUtensorMap mx, mw1, mw3, ma, mw2;
+  if (!map2d(&mx, xp, d, R, 64, BM) || !map3d(&mw1, W1, h, d, E, 64, 64) ||
+      !map3d(&mw3, W3, h, d, E, 64, 64) || !map2d(&ma, a, h, R, 64, BM) ||
+      !map3d(&mw2, W2, d, h, E, 64, 64))
+    return MOE_ERR_CUDA;
+  GemmArgs g{};
+  g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
+  // up-projection + SwiGLU: N tiles of 128 h-columns (x2 for W1 and W3)
+  g.n_tiles = (h + BN / 2 - 1) / (BN / 2);
+  g.kb_total = d / BK;
+  g.out0 = h1; g.out1 = h3; g.out2 = a; g.ldo = h;
+  st = launch<kUp>(mx, mx, mw1, mw3, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
+  if (st != MOE_OK) return st;
+  // down-projection
+  GemmArgs g2 = g;
+  g2.n_tiles = (d + BN - 1) / BN;
+  g2.kb_total = h / BK;
+  g2.out0 = yp; g2.out1 = nullptr; g2.out2 = nullptr; g2.ldo = d;
+  return launch<kDown>(ma, ma, mw2, mw2, mw2, g2, row_grid_upper(R, E, g2.n_tiles), s);
+}
+
+int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
+                           const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                           const moe_bf16_t* h1, const moe_bf16_t* h3, const moe_bf16_t* a,
+                           const moe_bf16_t* dyp, moe_bf16_t* dh1, moe_bf16_t* dh3, moe_bf16_t* dxp,
+                           moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  int st = check_common(ws, ws_bytes, R, E, d, h);
+  if (st != MOE_OK) return st;
+  MOE_CHECK_PTR(dW1); MOE_CHECK_PTR(dW3); MOE_CHECK_PTR(dW2);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (R == 0) {
+    const size_t wb = (size_t)E * d * h * 2;
+    if (cudaMemsetAsync(dW1, 0, wb, s) != cudaSuccess || cudaMemsetAsync(dW3, 0, wb, s) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, wb, s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3); MOE_CHECK_PTR(W2);
+  MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(a); MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dh1);
+  MOE_CHECK_PTR(dh3); MOE_CHECK_PTR(dxp);
+  CUtensorMap m_dyp, m_w2k, m_dh1, m_dh3, m_w1k, m_w3k, m_xpt, m_at, m_dh1t, m_dh3t, m_dypt;
+  // K-major operands (row-grouped dgrad GEMMs)
+  if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, BN) ||
+      !map2d(&m_dh1, dh1, h, R, 64, BM) || !map2d(&m_dh3, dh3, h, R, 64, BM) ||
+      !map3d(&m_w1k, W1, h, d, E, 64, BN) || !map3d(&m_w3k, W3, h, d, E, 64, BN) ||
+      // MN-major operands of the weight-gradient GEMMs (64x64 boxes)
+      !map2d(&m_xpt, xp, d, R, 64, 64) || !map2d(&m_at, a, h, R, 64, 64) ||
+      !map2d(&m_dh1t, dh1, h, R, 64, 64) || !map2d(&m_dh3t, dh3, h, R, 64, 64) ||
+      !map2d(&m_dypt, dyp, d, R, 64, 64))
+    return MOE_ERR_CUDA;
+  GemmArgs g{};
+  g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
+  // dA = dyp @ W2^T with the SwiGLU backward epilogue -> dh1, dh3
+  g.n_tiles = (h + BN - 1) / BN;
+  g.kb_total = d / BK;
+  g.out0 = dh1; g.out1 = dh3; g.in0 = h1; g.in1 = h3; g.ldo = h;
+  st = launch<kDA>(m_dyp, m_dyp, m_w2k, m_w2k, m_w2k, g, row_grid_upper(R, E, g.n_tiles), s);
+  if (st != MOE_OK) return st;
+  // dxp = dh1 @ W1^T + dh3 @ W3^T (one reduction over K = 2h)
+  GemmArgs g2 = g;
+  g2.n_tiles = (d + BN - 1) / BN;
+  g2.kb_total = 2 * (h / BK);
+  g2.kb_split = h / BK;
+  g2.out0 = dxp; g2.out1 = nullptr; g2.in0 = nullptr; g2.in1 = nullptr; g2.ldo = d;
+  st = launch<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, m_w3k, g2, row_grid_upper(R, E, g2.n_tiles), s);
+  if (st != MOE_OK) return st;
+  // weight gradients, reduction over each expert's own rows
+  GemmArgs g3 = g;
+  g3.out0 = dW1; g3.out1 = dW3; g3.out2 = dW2; g3.in0 = nullptr; g3.in1 = nullptr;
+  g3.wg_mt1 = (d + BM - 1) / BM;
+  g3.wg_mt2 = (h + BM - 1) / BM;
+  g3.wg_t1 = g3.wg_mt1 * ((h + BN - 1) / BN);
+  g3.wg_t2 = g3.wg_mt2 * ((d + BN - 1) / BN);
+  long long tiles = (long long)E * (2 * g3.wg_t1 + g3.wg_t2);
+  int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+  return launch<kWG>(m_xpt, m_at, m_dh1t, m_dh3t, m_dypt, g3, grid, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,235 @@
+// Rowwise dispatch and combine (and the combine backward): 16-byte vectorised
+// row copies between token order and the expert-contiguous buffer.
+//
+// "OLMo-core 3：MoE 训练栈让专家池越大、吞吐不再越慢", section "rowwise EP：用
+// NVSHMEM 一端直写": no pack/permute stages; every routed row is written
+// directly into its destination expert buffer by a route-table lookup, and
+// combine brings the expert outputs back (the page's Table 7 puts dispatch at
+// 2.298 ms and combine at 2.423 ms per trace on the multi-GPU stack).  On one
+// GPU the NVSHMEM one-sided put becomes a plain HBM store.
+//
+// One warp per token; each lane moves 16-byte vectors (8 bf16), U of them in
+// flight, so one token row is read once and written k times (dispatch) or k
+// rows are read and one written (combine).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <int U>
+__global__ void __launch_bounds__(kThreads)
+dispatch_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
+                const int32_t* __restrict__ row_of_slot, uint16_t* __restrict__ xp) {
+  const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int nvec = d >> 3;
+  int rows[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
+  const uint16_t* src = x + (size_t)t * d;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    uint4 val[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int v = v0 + 32 * u;
+      if (v < nvec) val[u] = ld_nc_v4(src + (size_t)v * 8);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        uint16_t* dst = xp + (size_t)rows[j] * d;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          int v = v0 + 32 * u;
+          if (v < nvec) st_v4(dst + (size_t)v * 8, val[u]);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float g, uint4 v) {
+  acc[0] = fmaf(g, bf16_lo(v.x), acc[0]); acc[1] = fmaf(g, bf16_hi(v.x), acc[1]);
+  acc[2] = fmaf(g, bf16_lo(v.y), acc[2]); acc[3] = fmaf(g, bf16_hi(v.y), acc[3]);
+  acc[4] = fmaf(g, bf16_lo(v.z), acc[4]); acc[5] = fmaf(g, bf16_hi(v.z), acc[5]);
+  acc[6] = fmaf(g, bf16_lo(v.w), acc[6]); acc[7] = fmaf(g, bf16_hi(v.w), acc[7]);
+}
+
+// out[t] = sum_j g[t,j] * yp[row(t,j)] in slot order, fp32, one rounding.
+template <int U>
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const uint16_t* __restrict__ yp, const int32_t* __restrict__ row_of_slot,
+               const float* __restrict__ gate, int T, int k, int d, uint16_t* __restrict__ out) {
+  const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int nvec = d >> 3;
+  int rows[kMaxTopK];
+  float g[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
+    g[j] = (j < k) ? (gate ? __ldg(gate + (size_t)t * k + j) : 1.f) : 0.f;
+  }
+  uint16_t* dst = out + (size_t)t * d;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const uint16_t* src = yp + (size_t)rows[j] * d;
+        uint4 val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          int v = v0 + 32 * u;
+          if (v < nvec) val[u] = ld_nc_v4(src + (size_t)v * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          int v = v0 + 32 * u;
+          if (v < nvec) fma8(acc[u], g[j], val[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int v = v0 + 32 * u;
+      if (v < nvec) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        st_v4(dst + (size_t)v * 8, o);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
+  acc = fmaf(bf16_lo(a.x), bf16_lo(b.x), acc); acc = fmaf(bf16_hi(a.x), bf16_hi(b.x), acc);
+  acc = fmaf(bf16_lo(a.y), bf16_lo(b.y), acc); acc = fmaf(bf16_hi(a.y), bf16_hi(b.y), acc);
+  acc = fmaf(bf16_lo(a.z), bf16_lo(b.z), acc); acc = fmaf(bf16_hi(a.z), bf16_hi(b.z), acc);
+  acc = fmaf(bf16_lo(a.w), bf16_lo(b.w), acc); acc = fmaf(bf16_hi(a.w), bf16_hi(b.w), acc);
+  return acc;
+}
+
+__device__ __forceinline__ uint4 scale8(uint4 a, float g) {
+  uint4 o;
+  o.x = pack_bf16x2(g * bf16_lo(a.x), g * bf16_hi(a.x));
+  o.y = pack_bf16x2(g * bf16_lo(a.y), g * bf16_hi(a.y));
+  o.z = pack_bf16x2(g * bf16_lo(a.z), g * bf16_hi(a.z));
+  o.w = pack_bf16x2(g * bf16_lo(a.w), g * bf16_hi(a.w));
+  return o;
+}
+
+// dyp[row(t,j)] = g[t,j] * dout[t];  dg[t,j] = <dout[t], yp[row(t,j)]>
+template <int U>
+__global__ void __launch_bounds__(kThreads)
+combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ yp,
+                   const int32_t* __restrict__ row_of_slot, const float* __restrict__ gate,
+                   int T, int k, int d, uint16_t* __restrict__ dyp, float* __restrict__ dgate) {
+  const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int nvec = d >> 3;
+  int rows[kMaxTopK];
+  float g[kMaxTopK], dot[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
+    g[j] = j < k ? __ldg(gate + (size_t)t * k + j) : 0.f;
+    dot[j] = 0.f;
+  }
+  const uint16_t* src = dout + (size_t)t * d;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    uint4 dv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int v = v0 + 32 * u;
+      if (v < nvec) dv[u] = ld_nc_v4(src + (size_t)v * 8);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const uint16_t* yr = yp + (size_t)rows[j] * d;
+        uint16_t* dr = dyp + (size_t)rows[j] * d;
+        uint4 yv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          int v = v0 + 32 * u;
+          if (v < nvec) yv[u] = ld_nc_v4(yr + (size_t)v * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          int v = v0 + 32 * u;
+          if (v < nvec) {
+            dot[j] = dot8(dv[u], yv[u], dot[j]);
+            st_v4(dr + (size_t)v * 8, scale8(dv[u], g[j]));
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      float s = warp_sum(dot[j]);
+      if (lane == 0) dgate[(size_t)t * k + j] = s;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_dispatch_rows(const moe_bf16_t* x, int T, int d, int k, const int32_t* row_of_slot,
+                      moe_bf16_t* xp, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && d % 8 == 0 && k >= 1 && k <= kMaxTopK);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(x); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(xp);
+  dim3 grid((T + kWarps - 1) / kWarps);
+  dispatch_kernel<8><<<grid, kThreads, 0, (cudaStream_t)stream>>>(x, T, d, k, row_of_slot, xp);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_combine(const moe_bf16_t* yp, const int32_t* row_of_slot, const float* gate, int T, int k,
+                int d, moe_bf16_t* out, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && d % 8 == 0 && k >= 1 && k <= kMaxTopK);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(out);
+  if (gate && !aligned16(gate)) return MOE_ERR_INVALID_ARG;
+  dim3 grid((T + kWarps - 1) / kWarps);
+  combine_kernel<4><<<grid, kThreads, 0, (cudaStream_t)stream>>>(yp, row_of_slot, gate, T, k, d, out);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_combine_bwd(const moe_bf16_t* dout, const moe_bf16_t* yp, const int32_t* row_of_slot,
+                    const float* gate, int T, int k, int d, moe_bf16_t* dyp, float* dgate,
+                    moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && d % 8 == 0 && k >= 1 && k <= kMaxTopK);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(dout); MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(gate);
+  MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dgate);
+  dim3 grid((T + kWarps - 1) / kWarps);
+  combine_bwd_kernel<4><<<grid, kThreads, 0, (cudaStream_t)stream>>>(dout, yp, row_of_slot, gate,
+                                                                     T, k, d, dyp, dgate);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+}  // extern "C"

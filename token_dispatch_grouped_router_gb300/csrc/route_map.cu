@@ -1,0 +1,192 @@
+// Device-resident route map: per-expert counts, offsets and the stable
+// slot <-> row permutation, built with no host synchronisation.
+//
+// "OLMo-core 3：MoE 训练栈让专家池越大、吞吐不再越慢", section "另外两处税：主机同步
+// 与 padding": the routing counts, each expert's row count (the grouped GEMM's
+// M dimensions) and the per-expert permutation are all expressed by a route
+// map generated on the device, which removes the two host syncs of the
+// block all-to-all path.
+//
+// Three launches, all integer work, deterministic:
+//  1. route_count: block b owns slots [b*1024, (b+1)*1024).  Each of its 8
+//     warps walks 128 consecutive slots in order, ranking every slot among
+//     the same-expert slots before it (match_any + popc) against a per-warp
+//     shared histogram.  Warp histograms are then scanned per expert, giving
+//     every slot its stable rank inside the block and the block's histogram.
+//  2. route_scan: one block scans the block histograms per expert (column
+//     scan over blocks -> block base per expert, counts[e]) and then scans
+//     counts over experts -> offsets.
+//  3. route_place: row = offsets[e] + block_base[b][e] + rank; writes
+//     row_of_slot[s] and its inverse slot_of_row[row].
+// Slots of one expert therefore land in ascending slot order (stable).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRCThreads = 256;                     // 8 warps
+constexpr int kRCWarps = kRCThreads / 32;
+constexpr int kSlotsPerWarp = kRouteChunk / kRCWarps;   // 128
+constexpr int kIters = kSlotsPerWarp / 32;              // 4
+
+__global__ void __launch_bounds__(kRCThreads)
+route_count_kernel(const int32_t* __restrict__ idx, int R, int E,
+                   int32_t* __restrict__ chunk_counts, int32_t* __restrict__ local_rank,
+                   int* __restrict__ status) {
+  extern __shared__ int32_t hist[];                 // [kRCWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kRCWarps * E; i += kRCThreads) hist[i] = 0;
+  __syncthreads();
+  int32_t* wh = hist + warp * E;
+  const int base = blockIdx.x * kRouteChunk + warp * kSlotsPerWarp;
+  int myE[kIters], myRank[kIters];
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    int s = base + it * 32 + lane;
+    int e = -1;
+    if (s < R) {
+      e = __ldg(idx + s);
+      if (e < 0 || e >= E) { set_status(status, MOE_DEV_BAD_EXPERT_ID); e = -1; }
+    }
+    unsigned peers = __match_any_sync(0xffffffffu, e);
+    int r = -1;
+    if (e >= 0) r = wh[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (peers & lt_mask) == 0) wh[e] += __popc(peers);   // group leader
+    __syncwarp();
+    myE[it] = e;
+    myRank[it] = r;
+  }
+  __syncthreads();
+  // exclusive scan of the warp histograms per expert -> warp bases; totals
+  int32_t* cc = chunk_counts + (size_t)blockIdx.x * E;
+  for (int e = threadIdx.x; e < E; e += kRCThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kRCWarps; ++w) {
+      int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    cc[e] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    int s = base + it * 32 + lane;
+    if (s < R && myE[it] >= 0) local_rank[s] = wh[myE[it]] + myRank[it];
+  }
+}
+
+// Single block of 1024 threads.
+__global__ void __launch_bounds__(1024)
+route_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int32_t tot[kMaxExperts];
+  __shared__ int32_t warp_sums[32];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    int b = 0;
+    for (; b + 4 <= nchunks; b += 4) {
+      int c0 = chunk_counts[(size_t)(b + 0) * E + e];
+      int c1 = chunk_counts[(size_t)(b + 1) * E + e];
+      int c2 = chunk_counts[(size_t)(b + 2) * E + e];
+      int c3 = chunk_counts[(size_t)(b + 3) * E + e];
+      chunk_counts[(size_t)(b + 0) * E + e] = run; run += c0;
+      chunk_counts[(size_t)(b + 1) * E + e] = run; run += c1;
+      chunk_counts[(size_t)(b + 2) * E + e] = run; run += c2;
+      chunk_counts[(size_t)(b + 3) * E + e] = run; run += c3;
+    }
+    for (; b < nchunks; ++b) {
+      int c = chunk_counts[(size_t)b * E + e];
+      chunk_counts[(size_t)b * E + e] = run;
+      run += c;
+    }
+    tot[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of tot[0..E) -> offsets (E <= 1024: one element per thread)
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  int v = t < E ? tot[t] : 0;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int ws = warp_sums[lane];
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_sums[lane] = wi - ws;     // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  int excl = warp_sums[w] + incl - v;
+  if (t < E) offsets[t] = excl;
+  if (t == E - 1) offsets[E] = excl + v;
+}
+
+__global__ void route_place_kernel(const int32_t* __restrict__ idx, int R, int E,
+                                   const int32_t* __restrict__ chunk_base,
+                                   const int32_t* __restrict__ local_rank,
+                                   const int32_t* __restrict__ offsets,
+                                   int32_t* __restrict__ row_of_slot,
+                                   int32_t* __restrict__ slot_of_row) {
+  int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= R) return;
+  int e = __ldg(idx + s);
+  if (e < 0 || e >= E) return;                 // reported by route_count
+  int b = s / kRouteChunk;
+  int row = __ldg(offsets + e) + __ldg(chunk_base + (size_t)b * E + e) + __ldg(local_rank + s);
+  row_of_slot[s] = row;
+  slot_of_row[row] = s;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
+                                  void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= kMaxTopK && E >= 1 && E <= kMaxExperts && k <= E);
+  MOE_CHECK_ARG((long long)T * k <= 0x7fffffffLL);
+  MOE_CHECK_PTR(counts); MOE_CHECK_PTR(offsets);
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  const long long R = (long long)T * k;
+  if (R > 0) { MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(slot_of_row); }
+  RouteScratch L = route_scratch(R, E);
+  if (ws_bytes < L.end) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int nchunks = (int)((R + kRouteChunk - 1) / kRouteChunk);
+  char* wsb = reinterpret_cast<char*>(ws);
+  int32_t* chunk_counts = reinterpret_cast<int32_t*>(wsb + L.chunk_counts);
+  int32_t* local_rank = reinterpret_cast<int32_t*>(wsb + L.local_rank);
+  int* status = reinterpret_cast<int*>(ws);
+  if (R == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  size_t smem = sizeof(int32_t) * kRCWarps * E;
+  route_count_kernel<<<nchunks, kRCThreads, smem, s>>>(topk_idx, (int)R, E, chunk_counts,
+                                                       local_rank, status);
+  route_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, counts, offsets);
+  route_place_kernel<<<(int)((R + 255) / 256), 256, 0, s>>>(topk_idx, (int)R, E, chunk_counts,
+                                                             local_rank, offsets, row_of_slot,
+                                                             slot_of_row);
+  MOE_LAUNCH_CHECK(3);
+  return MOE_OK;
+}

@@ -1,0 +1,343 @@
+// Router: logits GEMM (fp32 on CUDA cores), warp-per-token top-k with shuffle
+// arg-max, renormalised softmax gates, and the backward of both.
+//
+// The pages ("Ai2 Olmo-core 3: The Secret Behind 2.7x MoE Training
+// Throughput", section "The Capacity Tax") only say that a routing function
+// picks a few experts (e.g. 4 of 128) per token.  The function implemented
+// here is the benchmark specification's: softmax over the E logits, top-k,
+// ties to the lower expert id, gates renormalised over the selection.  The
+// router stays in fp32 (the OLMo-core 3 tutorial's DeepSeek-V3 paragraph in
+// section "一个低精度格式，同时压三个地方" keeps gating in high precision).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// ----------------------------------------------------------- SIMT fp32 GEMM
+// out[m][n] = sum_k A(m,k) * B(k,n), 64x64 tiles, BK = 16, 256 threads with a
+// 4x4 register block each.  Used only for the router's small GEMMs (N = E).
+
+enum class Lay { RowMK, ColMK };   // A: RowMK = a[m*ld+k], ColMK = a[k*ld+m]
+enum class LayB { RowKN, ColKN };  // B: RowKN = b[k*ld+n], ColKN = b[n*ld+k]
+enum class Epi { StoreBias, AddBf16, StorePartial };
+
+template <typename TA> __device__ __forceinline__ float ldf(const TA* p);
+template <> __device__ __forceinline__ float ldf<float>(const float* p) { return __ldg(p); }
+template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+constexpr int SB = 64, SK = 16;
+
+template <typename TA, Lay LA, LayB LB, Epi EP>
+__global__ void __launch_bounds__(256)
+simt_gemm_kernel(const TA* __restrict__ A, int lda, const float* __restrict__ B, int ldb,
+                 int M, int N, int K, int k_per_split,
+                 float* __restrict__ outf, __nv_bfloat16* __restrict__ outb, int ldo,
+                 const float* __restrict__ bias) {
+  __shared__ float As[SK][SB + 4];
+  __shared__ float Bs[SK][SB + 4];
+  const int tid = threadIdx.x;
+  const int m0 = blockIdx.x * SB, n0 = blockIdx.y * SB;
+  const int split = blockIdx.z;
+  const int kbeg = split * k_per_split;
+  const int kend = min(K, kbeg + k_per_split);
+  const int tm = (tid / 16) * 4, tn = (tid % 16) * 4;
+  float acc[4][4] = {};
+  for (int k0 = kbeg; k0 < kend; k0 += SK) {
+#pragma unroll
+    for (int i = 0; i < (SK * SB) / 256; ++i) {
+      int e = tid + i * 256;
+      int kk, mm;
+      if (LA == Lay::RowMK) { kk = e % SK; mm = e / SK; } else { mm = e % SB; kk = e / SB; }
+      int gm = m0 + mm, gk = k0 + kk;
+      float v = 0.f;
+      if (gm < M && gk < kend)
+        v = (LA == Lay::RowMK) ? ldf(A + (size_t)gm * lda + gk) : ldf(A + (size_t)gk * lda + gm);
+      As[kk][mm] = v;
+    }
+#pragma unroll
+    for (int i = 0; i < (SK * SB) / 256; ++i) {
+      int e = tid + i * 256;
+      int kk, nn;
+      if (LB == LayB::RowKN) { nn = e % SB; kk = e / SB; } else { kk = e % SK; nn = e / SK; }
+      int gn = n0 + nn, gk = k0 + kk;
+      float v = 0.f;
+      if (gn < N && gk < kend)
+        v = (LB == LayB::RowKN) ? __ldg(B + (size_t)gk * ldb + gn) : __ldg(B + (size_t)gn * ldb + gk);
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = As[kk][tm + i]; b[i] = Bs[kk][tn + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int gm = m0 + tm + i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int gn = n0 + tn + j;
+      if (gn >= N) continue;
+      if (EP == Epi::StoreBias) {
+        outf[(size_t)gm * ldo + gn] = acc[i][j] + (bias ? __ldg(bias + gn) : 0.f);
+      } else if (EP == Epi::AddBf16) {
+        __nv_bfloat16* p = outb + (size_t)gm * ldo + gn;
+        *p = __float2bfloat16_rn(__bfloat162float(*p) + acc[i][j]);
+      } else {
+        outf[((size_t)split * M + gm) * ldo + gn] = acc[i][j];
+      }
+    }
+  }
+}
+
+// dW_r[m][n] = sum over splits of the partials (fixed order: deterministic)
+__global__ void reduce_splits_kernel(const float* __restrict__ part, int splits, int MN,
+                                     float* __restrict__ out) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= MN) return;
+  float s = 0.f;
+  for (int p = 0; p < splits; ++p) s += part[(size_t)p * MN + i];
+  out[i] = s;
+}
+
+// db[e] = sum_t dz[t][e]: one block per expert, fixed-order block reduction
+__global__ void column_sum_kernel(const float* __restrict__ dz, int T, int E, float* __restrict__ db) {
+  __shared__ float red[256];
+  int e = blockIdx.x;
+  float s = 0.f;
+  for (int t = threadIdx.x; t < T; t += 256) s += dz[(size_t)t * E + e];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) db[e] = red[0];
+}
+
+// ----------------------------------------------------------------- top-k
+// One warp per token.  Lane l holds logits l, l+32, ... (VPL per lane).  Each
+// of the k rounds takes every lane's best untaken logit and reduces them with
+// a butterfly arg-max whose order is (value desc, id asc), so every lane ends
+// with the same winner; the owner lane marks it taken.
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  // candidate (v, i) precedes (bv, bi); bi < 0 means "no candidate yet"
+  return i >= 0 && (bi < 0 || v > bv || (v == bv && i < bi));
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256)
+topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+            int32_t* __restrict__ idx_out, float* __restrict__ gate_out) {
+  const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const float* row = logits + (size_t)warp * E;
+  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(row + e) : 0.f;
+  }
+  uint32_t taken = 0;
+  float zsel[kMaxTopK];
+  int isel[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    zsel[j] = 0.f; isel[j] = 0;
+    if (j < k) {
+      float bv = 0.f; int bi = -1;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) { bv = v[i]; bi = e; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      zsel[j] = bv; isel[j] = bi;
+    }
+  }
+  if (lane == 0) {
+    // renormalised softmax over the selection; zsel[0] is the maximum
+    float ex[kMaxTopK], s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) { ex[j] = expf(zsel[j] - zsel[0]); s += ex[j]; }
+    }
+    float inv = 1.f / s;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        idx_out[(size_t)warp * k + j] = isel[j];
+        gate_out[(size_t)warp * k + j] = ex[j] * inv;
+      }
+    }
+  }
+}
+
+__global__ void gates_kernel(const float* __restrict__ sel, int T, int k, float* __restrict__ gate) {
+  int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const float* z = sel + (size_t)t * k;
+  float m = z[0];
+  for (int j = 1; j < k; ++j) m = fmaxf(m, z[j]);
+  float ex[kMaxTopK], s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) { ex[j] = expf(z[j] - m); s += ex[j]; }
+  }
+  float inv = 1.f / s;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) gate[(size_t)t * k + j] = ex[j] * inv;
+}
+
+// dz[t, idx_j] = g_j (dg_j - sum_l g_l dg_l); zero elsewhere.  Warp per token.
+__global__ void __launch_bounds__(256)
+topk_bwd_kernel(const float* __restrict__ gate, const float* __restrict__ dgate,
+                const int32_t* __restrict__ idx, int T, int E, int k, float* __restrict__ dz) {
+  const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  float g[kMaxTopK], dg[kMaxTopK];
+  int id[kMaxTopK];
+  float inner = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    g[j] = 0.f; dg[j] = 0.f; id[j] = -1;
+    if (j < k) {
+      g[j] = __ldg(gate + (size_t)warp * k + j);
+      dg[j] = __ldg(dgate + (size_t)warp * k + j);
+      id[j] = __ldg(idx + (size_t)warp * k + j);
+      inner = fmaf(g[j], dg[j], inner);
+    }
+  }
+  float* row = dz + (size_t)warp * E;
+  for (int e = lane; e < E; e += 32) {
+    float val = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k && id[j] == e) val = g[j] * (dg[j] - inner);
+    row[e] = val;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_router_logits(const moe_bf16_t* x, const float* W_r, const float* b, int T, int d, int E,
+                      float* logits, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && E > 0);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(x); MOE_CHECK_PTR(W_r); MOE_CHECK_PTR(logits);
+  if (b && !aligned16(b)) return MOE_ERR_INVALID_ARG;
+  dim3 grid((T + SB - 1) / SB, (E + SB - 1) / SB, 1);
+  simt_gemm_kernel<__nv_bfloat16, Lay::RowMK, LayB::RowKN, Epi::StoreBias>
+      <<<grid, 256, 0, (cudaStream_t)stream>>>(
+          reinterpret_cast<const __nv_bfloat16*>(x), d, W_r, E, T, E, d, d,
+          logits, nullptr, E, b);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                    float* topk_gate, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && E > 0 && E <= kMaxExperts && k >= 1 && k <= kMaxTopK && k <= E);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(logits); MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(topk_gate);
+  const int threads = 256, warps = threads / 32;
+  dim3 grid((T + warps - 1) / warps);
+  cudaStream_t s = (cudaStream_t)stream;
+  int vpl = (E + 31) / 32;
+  if (vpl <= 1) topk_kernel<1><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 2) topk_kernel<2><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 4) topk_kernel<4><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 8) topk_kernel<8><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 16) topk_kernel<16><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  else topk_kernel<32><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_router_gates(const float* sel_logits, int T, int k, float* topk_gate, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= kMaxTopK);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(sel_logits); MOE_CHECK_PTR(topk_gate);
+  gates_kernel<<<(T + 255) / 256, 256, 0, (cudaStream_t)stream>>>(sel_logits, T, k, topk_gate);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_router_topk_bwd(const float* topk_gate, const float* d_gate, const int32_t* topk_idx,
+                        int T, int E, int k, float* d_logits, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && E > 0 && E <= kMaxExperts && k >= 1 && k <= kMaxTopK && k <= E);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(topk_gate); MOE_CHECK_PTR(d_gate); MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(d_logits);
+  dim3 grid((T + 7) / 8);
+  topk_bwd_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(topk_gate, d_gate, topk_idx, T, E, k, d_logits);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_router_logits_bwd(const moe_bf16_t* x, const float* W_r, const float* d_logits, int T,
+                          int d, int E, moe_bf16_t* dx, float* dW_r, float* db, void* ws,
+                          size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && E > 0 && E <= kMaxExperts);
+  MOE_CHECK_PTR(x); MOE_CHECK_PTR(W_r); MOE_CHECK_PTR(dW_r);
+  if (db && !aligned16(db)) return MOE_ERR_INVALID_ARG;
+  if (T > 0) { MOE_CHECK_PTR(d_logits); MOE_CHECK_PTR(dx); }
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < router_scratch_end(E, d)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) {
+    if (cudaMemsetAsync(dW_r, 0, sizeof(float) * (size_t)d * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (db && cudaMemsetAsync(db, 0, sizeof(float) * (size_t)E, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  // dx += dz @ W_r^T : M = T, N = d, K = E; B(k=e, n) = W_r[n*E + e]
+  {
+    dim3 grid((T + SB - 1) / SB, (d + SB - 1) / SB, 1);
+    simt_gemm_kernel<float, Lay::RowMK, LayB::ColKN, Epi::AddBf16><<<grid, 256, 0, s>>>(
+        d_logits, E, W_r, E, T, d, E, E, nullptr, reinterpret_cast<__nv_bfloat16*>(dx), d, nullptr);
+  }
+  // dW_r = x^T @ dz : M = d, N = E, K = T, split into kRouterSplits partials
+  float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + kStatusBytes);
+  {
+    int kps = (T + kRouterSplits - 1) / kRouterSplits;
+    kps = (kps + SK - 1) / SK * SK;
+    dim3 grid((d + SB - 1) / SB, (E + SB - 1) / SB, kRouterSplits);
+    simt_gemm_kernel<__nv_bfloat16, Lay::ColMK, LayB::RowKN, Epi::StorePartial><<<grid, 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(x), d, d_logits, E, d, E, T, kps, part, nullptr, E,
+        nullptr);
+    int MN = d * E;
+    reduce_splits_kernel<<<(MN + 255) / 256, 256, 0, s>>>(part, kRouterSplits, MN, dW_r);
+  }
+  int n = 3;
+  if (db) { column_sum_kernel<<<E, 256, 0, s>>>(d_logits, T, E, db); ++n; }
+  MOE_LAUNCH_CHECK(n);
+  return MOE_OK;
+}
+
+}  // extern "C"

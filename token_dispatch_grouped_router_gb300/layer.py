@@ -1,0 +1,145 @@
+"""The MoE expert layer as a sequence of libmoe calls on preallocated buffers.
+
+``MoELayer`` owns the device buffers of one layer step (PyTorch supplies the
+memory and the stream) and runs forward and backward purely through the C-ABI
+entry points:
+
+forward : [router_logits ->] router_topk | router_gates -> expert_offsets ->
+          dispatch_rows -> grouped_swiglu_fwd -> combine
+backward: combine_bwd -> grouped_swiglu_bwd -> combine(gates = None) ->
+          router_topk_bwd [-> router_logits_bwd]
+
+Nothing is copied back to the host and nothing waits on the host.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import libmoe as L
+
+
+def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
+    """uint16 bf16 bit patterns (numpy) -> torch.bfloat16 tensor on `device`."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """torch.bfloat16 tensor -> uint16 bit patterns (numpy, host)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class MoELayer:
+    """Buffers and call sequence of one MoE layer step on one GPU."""
+
+    def __init__(self, T: int, d: int, E: int, k: int, h: int, learned: bool,
+                 device="cuda", with_backward: bool = True):
+        self.T, self.d, self.E, self.k, self.h = T, d, E, k, h
+        self.R = T * k
+        self.learned = learned
+        self.with_backward = with_backward
+        dev = torch.device(device)
+        bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+        e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        R = self.R
+        self.x = e(T, d)
+        self.W1 = e(E, d, h); self.W3 = e(E, d, h); self.W2 = e(E, h, d)
+        if learned:
+            self.W_r = e(d, E, dt=f32)
+            self.b: Optional[torch.Tensor] = None
+            self.logits = e(T, E, dt=f32)
+            self.logits_given = False
+        else:
+            self.glogit = e(T, k, dt=f32)
+        self.idx = e(T, k, dt=i32)
+        self.gate = e(T, k, dt=f32)
+        self.counts = e(E, dt=i32)
+        self.offsets = e(E + 1, dt=i32)
+        self.row_of_slot = e(R, dt=i32)
+        self.slot_of_row = e(R, dt=i32)
+        self.xp = e(R, d)
+        self.h1 = e(R, h); self.h3 = e(R, h); self.a = e(R, h)
+        self.yp = e(R, d)
+        self.out = e(T, d)
+        ws_bytes = L.moe_workspace_size(T, E, k, d, h)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        if with_backward:
+            self.dY = e(T, d)
+            self.dyp = e(R, d); self.dgate = e(T, k, dt=f32)
+            self.dh1 = e(R, h); self.dh3 = e(R, h); self.dxp = e(R, d)
+            self.dW1 = e(E, d, h); self.dW3 = e(E, d, h); self.dW2 = e(E, h, d)
+            self.dX = e(T, d)
+            self.dlogits = e(T, E, dt=f32)
+            if learned:
+                self.dW_r = e(d, E, dt=f32)
+                self.db = e(E, dt=f32)
+
+    # ------------------------------------------------------------- inputs
+    def load_inputs(self, inp: Dict[str, np.ndarray]) -> None:
+        """Copy one workload's host inputs (see workloads.generate) to the device."""
+        dev = self.x.device
+        self.x.copy_(bf16_tensor(inp["x"], dev))
+        self.W1.copy_(bf16_tensor(inp["W1"], dev))
+        self.W3.copy_(bf16_tensor(inp["W3"], dev))
+        self.W2.copy_(bf16_tensor(inp["W2"], dev))
+        if self.learned:
+            self.W_r.copy_(torch.from_numpy(inp["W_r"]))
+            if inp.get("b") is not None:
+                self.b = torch.from_numpy(inp["b"]).to(dev)
+        else:
+            self.idx.copy_(torch.from_numpy(inp["idx"]))
+            self.glogit.copy_(torch.from_numpy(inp["glogit"]))
+        if self.with_backward and "dY" in inp:
+            self.dY.copy_(bf16_tensor(inp["dY"], dev))
+
+    def load_logits(self, z: np.ndarray) -> None:
+        """Route on these fp32 logits instead of computing x @ W_r + b (the
+        top-k and everything after it still run on the device)."""
+        self.logits.copy_(torch.from_numpy(np.ascontiguousarray(z, np.float32)))
+        self.logits_given = True
+
+    # ------------------------------------------------------------ forward
+    def route(self) -> None:
+        if self.learned:
+            if not self.logits_given:
+                L.moe_router_logits(self.x, self.W_r, self.b, self.logits)
+            L.moe_router_topk(self.logits, self.k, self.idx, self.gate)
+        else:
+            L.moe_router_gates(self.glogit, self.gate)
+        L.moe_expert_offsets(self.idx, self.E, self.counts, self.offsets, self.row_of_slot,
+                             self.slot_of_row, self.ws)
+
+    def forward(self) -> torch.Tensor:
+        self.route()
+        L.moe_dispatch_rows(self.x, self.row_of_slot, self.k, self.xp)
+        L.moe_grouped_swiglu_fwd(self.xp, self.offsets, self.W1, self.W3, self.W2,
+                                 self.h1, self.h3, self.a, self.yp, self.ws)
+        L.moe_combine(self.yp, self.row_of_slot, self.gate, self.k, self.out)
+        return self.out
+
+    # ----------------------------------------------------------- backward
+    def backward(self) -> None:
+        L.moe_combine_bwd(self.dY, self.yp, self.row_of_slot, self.gate, self.k,
+                          self.dyp, self.dgate)
+        L.moe_grouped_swiglu_bwd(self.xp, self.offsets, self.W1, self.W3, self.W2,
+                                 self.h1, self.h3, self.a, self.dyp, self.dh1, self.dh3,
+                                 self.dxp, self.dW1, self.dW3, self.dW2, self.ws)
+        L.moe_combine(self.dxp, self.row_of_slot, None, self.k, self.dX)
+        L.moe_router_topk_bwd(self.gate, self.dgate, self.idx, self.E, self.dlogits)
+        if self.learned:
+            L.moe_router_logits_bwd(self.x, self.W_r, self.dlogits, self.dX, self.dW_r,
+                                    self.db, self.ws)
+
+    def step(self) -> None:
+        self.forward()
+        if self.with_backward:
+            self.backward()
+
+    def launches_per_step(self) -> int:
+        n = (2 if self.learned and not self.logits_given else 1) + 3 + 1 + 2 + 1   # forward
+        if self.with_backward:
+            n += 1 + 3 + 1 + 1 + (4 if self.learned else 0)
+        return n

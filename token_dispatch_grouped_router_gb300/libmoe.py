@@ -1,0 +1,234 @@
+"""ctypes binding of libmoe: the C-ABI entry points under the same names.
+
+Argument marshalling only: each wrapper checks shapes/dtypes of the torch
+tensors it is given, passes their device pointers and the current CUDA stream
+to the library and raises ``MoEError`` on a non-zero status.  Every step of
+the layer runs in the library's CUDA kernels; there is no fallback.  If the
+library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmoe.so")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+
+# (name, restype, argtypes) exactly as declared in include/libmoe.h
+SIGNATURES = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_version": (_I, []),
+    "moe_launch_count": (ctypes.c_uint64, []),
+    "moe_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "moe_reset_status": (_I, [_P, _P]),
+    "moe_get_status": (_I, [_P, _P, _P]),
+    "moe_router_logits": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_router_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_router_gates": (_I, [_P, _I, _I, _P, _P]),
+    "moe_router_topk_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_router_logits_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_dispatch_rows": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_combine_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_grouped_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _Z, _P]),
+    "moe_grouped_swiglu_bwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P, _P, _P, _P, _Z, _P]),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        msg = load().moe_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{call} failed with status {status}: {msg}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (once) and declare every entry point's signature."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libmoe.so not found at {path}; build it with "
+                "`python -m token_dispatch_grouped_router_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmoe takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ok(name: str, status: int) -> None:
+    if status != 0:
+        raise MoEError(name, status)
+
+
+def _want(t: torch.Tensor, dtype: torch.dtype, shape, name: str) -> None:
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+# ------------------------------------------------------------------ misc
+
+def moe_version() -> int:
+    return load().moe_version()
+
+
+def moe_launch_count() -> int:
+    return int(load().moe_launch_count())
+
+
+def moe_workspace_size(T: int, E: int, k: int, d: int, h: int) -> int:
+    return int(load().moe_workspace_size(T, E, k, d, h))
+
+
+def moe_reset_status(ws: torch.Tensor) -> None:
+    _ok("moe_reset_status", load().moe_reset_status(_ptr(ws), _stream()))
+
+
+def moe_get_status(ws: torch.Tensor) -> int:
+    out = ctypes.c_int32(0)
+    _ok("moe_get_status", load().moe_get_status(_ptr(ws), ctypes.byref(out), _stream()))
+    return int(out.value)
+
+
+# ---------------------------------------------------------------- router
+
+def moe_router_logits(x, W_r, b, logits) -> None:
+    T, d = x.shape
+    E = W_r.shape[1]
+    _want(x, torch.bfloat16, (T, d), "x"); _want(W_r, torch.float32, (d, E), "W_r")
+    _want(logits, torch.float32, (T, E), "logits")
+    if b is not None:
+        _want(b, torch.float32, (E,), "b")
+    _ok("moe_router_logits", load().moe_router_logits(
+        _ptr(x), _ptr(W_r), _ptr(b), T, d, E, _ptr(logits), _stream()))
+
+
+def moe_router_topk(logits, k: int, topk_idx, topk_gate) -> None:
+    T, E = logits.shape
+    _want(logits, torch.float32, (T, E), "logits")
+    _want(topk_idx, torch.int32, (T, k), "topk_idx"); _want(topk_gate, torch.float32, (T, k), "topk_gate")
+    _ok("moe_router_topk", load().moe_router_topk(
+        _ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_gate), _stream()))
+
+
+def moe_router_gates(sel_logits, topk_gate) -> None:
+    T, k = sel_logits.shape
+    _want(sel_logits, torch.float32, (T, k), "sel_logits")
+    _want(topk_gate, torch.float32, (T, k), "topk_gate")
+    _ok("moe_router_gates", load().moe_router_gates(_ptr(sel_logits), T, k, _ptr(topk_gate), _stream()))
+
+
+def moe_router_topk_bwd(topk_gate, d_gate, topk_idx, E: int, d_logits) -> None:
+    T, k = topk_gate.shape
+    _want(d_gate, torch.float32, (T, k), "d_gate"); _want(topk_idx, torch.int32, (T, k), "topk_idx")
+    _want(d_logits, torch.float32, (T, E), "d_logits")
+    _ok("moe_router_topk_bwd", load().moe_router_topk_bwd(
+        _ptr(topk_gate), _ptr(d_gate), _ptr(topk_idx), T, E, k, _ptr(d_logits), _stream()))
+
+
+def moe_router_logits_bwd(x, W_r, d_logits, dx, dW_r, db, ws) -> None:
+    T, d = x.shape
+    E = W_r.shape[1]
+    _want(d_logits, torch.float32, (T, E), "d_logits"); _want(dx, torch.bfloat16, (T, d), "dx")
+    _want(dW_r, torch.float32, (d, E), "dW_r")
+    _ok("moe_router_logits_bwd", load().moe_router_logits_bwd(
+        _ptr(x), _ptr(W_r), _ptr(d_logits), T, d, E, _ptr(dx), _ptr(dW_r), _ptr(db),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+# ------------------------------------------------------------- route map
+
+def moe_expert_offsets(topk_idx, E: int, counts, offsets, row_of_slot, slot_of_row, ws) -> None:
+    T, k = topk_idx.shape
+    _want(topk_idx, torch.int32, (T, k), "topk_idx"); _want(counts, torch.int32, (E,), "counts")
+    _want(offsets, torch.int32, (E + 1,), "offsets")
+    _want(row_of_slot, torch.int32, (T * k,), "row_of_slot")
+    _want(slot_of_row, torch.int32, (T * k,), "slot_of_row")
+    _ok("moe_expert_offsets", load().moe_expert_offsets(
+        _ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(row_of_slot),
+        _ptr(slot_of_row), _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+# ------------------------------------------------------- dispatch/combine
+
+def moe_dispatch_rows(x, row_of_slot, k: int, xp) -> None:
+    T, d = x.shape
+    _want(x, torch.bfloat16, (T, d), "x"); _want(xp, torch.bfloat16, (T * k, d), "xp")
+    _ok("moe_dispatch_rows", load().moe_dispatch_rows(
+        _ptr(x), T, d, k, _ptr(row_of_slot), _ptr(xp), _stream()))
+
+
+def moe_combine(yp, row_of_slot, gate, k: int, out) -> None:
+    T, d = out.shape
+    _want(yp, torch.bfloat16, (T * k, d), "yp"); _want(out, torch.bfloat16, (T, d), "out")
+    if gate is not None:
+        _want(gate, torch.float32, (T, k), "gate")
+    _ok("moe_combine", load().moe_combine(
+        _ptr(yp), _ptr(row_of_slot), _ptr(gate), T, k, d, _ptr(out), _stream()))
+
+
+def moe_combine_bwd(dout, yp, row_of_slot, gate, k: int, dyp, dgate) -> None:
+    T, d = dout.shape
+    _want(yp, torch.bfloat16, (T * k, d), "yp"); _want(dyp, torch.bfloat16, (T * k, d), "dyp")
+    _want(gate, torch.float32, (T, k), "gate"); _want(dgate, torch.float32, (T, k), "dgate")
+    _ok("moe_combine_bwd", load().moe_combine_bwd(
+        _ptr(dout), _ptr(yp), _ptr(row_of_slot), _ptr(gate), T, k, d, _ptr(dyp), _ptr(dgate),
+        _stream()))
+
+
+# ------------------------------------------------------ grouped SwiGLU GEMM
+
+def moe_grouped_swiglu_fwd(xp, offsets, W1, W3, W2, h1, h3, a, yp, ws) -> None:
+    R, d = xp.shape
+    E, _, h = W1.shape
+    _want(W1, torch.bfloat16, (E, d, h), "W1"); _want(W3, torch.bfloat16, (E, d, h), "W3")
+    _want(W2, torch.bfloat16, (E, h, d), "W2"); _want(offsets, torch.int32, (E + 1,), "offsets")
+    for n, t in (("h1", h1), ("h3", h3), ("a", a)):
+        _want(t, torch.bfloat16, (R, h), n)
+    _want(yp, torch.bfloat16, (R, d), "yp")
+    _ok("moe_grouped_swiglu_fwd", load().moe_grouped_swiglu_fwd(
+        _ptr(xp), _ptr(offsets), R, E, d, h, _ptr(W1), _ptr(W3), _ptr(W2), _ptr(h1), _ptr(h3),
+        _ptr(a), _ptr(yp), _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+def moe_grouped_swiglu_bwd(xp, offsets, W1, W3, W2, h1, h3, a, dyp, dh1, dh3, dxp,
+                           dW1, dW3, dW2, ws) -> None:
+    R, d = xp.shape
+    E, _, h = W1.shape
+    for n, t in (("h1", h1), ("h3", h3), ("a", a), ("dh1", dh1), ("dh3", dh3)):
+        _want(t, torch.bfloat16, (R, h), n)
+    _want(dyp, torch.bfloat16, (R, d), "dyp"); _want(dxp, torch.bfloat16, (R, d), "dxp")
+    _want(dW1, torch.bfloat16, (E, d, h), "dW1"); _want(dW3, torch.bfloat16, (E, d, h), "dW3")
+    _want(dW2, torch.bfloat16, (E, h, d), "dW2")
+    _ok("moe_grouped_swiglu_bwd", load().moe_grouped_swiglu_bwd(
+        _ptr(xp), _ptr(offsets), R, E, d, h, _ptr(W1), _ptr(W3), _ptr(W2), _ptr(h1), _ptr(h3),
+        _ptr(a), _ptr(dyp), _ptr(dh1), _ptr(dh3), _ptr(dxp), _ptr(dW1), _ptr(dW3), _ptr(dW2),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream()))
