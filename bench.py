@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Throughput of the single-GPU MoE expert layer, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload KEY] [--impl ours|reference]
+
+One step = one pass of the whole layer over one batch: router gates (or
+router GEMM + top-k), device route map, rowwise dispatch, grouped SwiGLU GEMMs
+(up, down), combine, combine backward, grouped GEMM backward (dact, dx,
+wgrad), unpermute-sum and router backward.  Inputs are seeded synthetic
+tensors resident in HBM.  Between timed steps a 512 MB buffer is written to
+flush the 129 MB L2; every library call of a step is bracketed by CUDA events
+on the launching stream, so the per-kernel times below come from the timed
+steps themselves.
+
+Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs its own
+token batch with its own copy of the experts (replicas, no collective in the
+data path); the step time is the maximum over ranks and `value` counts the
+tokens of all ranks.
+
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only), on token
+samples of the same workload, and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tok/s fwd+bwd at E=8..128, k=4; grouped-GEMM % peak; dispatch GB/s"
+UNIT = "tok/s"
+FLUSH_BYTES = 512 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SOURCES = {
+    "gemm": ["grouped_swiglu.cu", "sm103_ptx.cuh", "common.cuh"],
+    "rows": ["permute.cu", "common.cuh"],
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="dense_e8")
+    ap.add_argument("--compare", default="pool_e128",
+                    help="second workload timed the same way (expert-count flatness); '' to skip")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="total CPU time budget of the --impl reference run")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------- utils
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def sources_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "token_dispatch_grouped_router_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def work_per_launch(w):
+    """Algorithmic FLOPs (GEMMs) or bytes (row kernels) of one launch per label."""
+    R, d, h, T, k = w.R, w.d, w.h, w.T, w.k
+    flops = {"gemm_up": 2.0 * R * d * 2 * h, "gemm_down": 2.0 * R * h * d,
+             "gemm_dact": 2.0 * R * d * h, "gemm_dx": 2.0 * R * 2 * h * d,
+             "gemm_wgrad": 3 * 2.0 * R * d * h}
+    bytes_ = {"dispatch": 2.0 * (T * d + R * d) + 4.0 * R,
+              "combine": 2.0 * (R * d + T * d) + 8.0 * R,
+              "combine_bwd": 2.0 * (T * d + 2 * R * d) + 12.0 * R,
+              "unpermute": 2.0 * (R * d + T * d) + 4.0 * R}
+    return flops, bytes_
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (every 50 ms), each stamped with the
+    host time it was read, so the samples of the timed region can be picked."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_uuid):
+        self.uuid = device_uuid
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+
+    def window(self, t0, t1):
+        """Summary of the samples read during [t0, t1] (a sample is read up to
+        one interval after it was taken); the nearest later sample otherwise."""
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [r for t, r in self.rows if t0 <= t <= t1 + 0.05]
+        how = "inside the timed region"
+        if not inside:
+            after = [r for t, r in self.rows if t > t1]
+            inside = after[:1]
+            how = "first sample after the timed region (region shorter than the interval)"
+        if not inside:
+            return None
+        sm = [num(r[0]) for r in inside if num(r[0]) is not None]
+        reasons = sorted({self.NAMES[i] for r in inside for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][1]),
+                "power_w_max": max((num(r[2]) or 0.0) for r in inside), "reasons": reasons,
+                "samples": len(inside), "which": how, "interval_ms": 50}
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    from token_dispatch_grouped_router_gb300 import libmoe as L
+    from token_dispatch_grouped_router_gb300 import workloads as wl
+    from token_dispatch_grouped_router_gb300.layer import MoELayer, bf16_tensor
+    L.load()
+
+    peaks = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def allmax(v):
+        if not dist:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    def timed(w, inp, K, W, with_e2e, sample_clocks=True):
+        layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=(w.routing == "learned"), device=dev)
+        layer.load_inputs(inp)
+        sampler = ClockSampler(device_uuid(dev)) if (rank == 0 and sample_clocks) else None
+        if sampler:
+            sampler.start()                  # running before the warm-up steps
+        for _ in range(W):
+            layer.step()
+        torch.cuda.synchronize()
+        L.moe_reset_status(layer.ws)
+        # ---------------------------------------------------------- timed region
+        events = []                          # per step: [(label, event), ...]
+
+        def new_mark(lst):
+            def mark(label):
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record()
+                lst.append((label, ev))
+            return mark
+
+        barrier()
+        torch.cuda.synchronize()
+        n0 = L.moe_launch_count()
+        t_wall = time.perf_counter()
+        for _ in range(K):
+            flush.zero_()                    # L2 flush, outside the step's events
+            lst = []
+            layer.step(new_mark(lst))
+            events.append(lst)
+        torch.cuda.synchronize()
+        barrier()
+        t_end = time.perf_counter()
+        wall = t_end - t_wall
+        launches = L.moe_launch_count() - n0
+        clocks = None
+        if sampler:
+            time.sleep(0.15)
+            sampler.stop()
+            clocks = sampler.window(t_wall, t_end)
+        status = L.moe_get_status(layer.ws)
+        if status != 0:
+            raise RuntimeError(f"device status {status} after the timed steps")
+        step_ms, per_label = [], {}
+        for lst in events:
+            step_ms.append(lst[0][1].elapsed_time(lst[-1][1]))
+            for (lab, ev), (_, nxt) in zip(lst[:-1], lst[1:]):
+                per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
+        res = {"ms_per_step": allmax(statistics.mean(step_ms)),
+               "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
+               "launches": launches, "clocks": clocks, "wall_s": wall}
+        if with_e2e:
+            res["e2e"] = e2e(layer, inp, K)
+        del layer
+        torch.cuda.empty_cache()
+        return res
+
+    def e2e(layer, inp, K):
+        """Same step through the public API with host inputs: each step copies
+        its inputs from pinned host memory and reads the outputs back."""
+        T, k = layer.T, layer.k
+        hx = bf16_tensor(inp["x"], "cpu").pin_memory()
+        hdY = bf16_tensor(inp["dY"], "cpu").pin_memory()
+        host_in = [(hx, layer.x), (hdY, layer.dY)]
+        if not layer.learned:
+            host_in += [(torch.from_numpy(inp["idx"]).pin_memory(), layer.idx),
+                        (torch.from_numpy(inp["glogit"]).pin_memory(), layer.glogit)]
+        hout = torch.empty(T, layer.d, dtype=torch.bfloat16).pin_memory()
+        hdx = torch.empty(T, layer.d, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+        d2h = hout.numel() * 2 + hdx.numel() * 2
+        times = []
+        barrier()
+        torch.cuda.synchronize()
+        for _ in range(K):
+            flush.zero_()
+            s = torch.cuda.Event(enable_timing=True); e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            for h, d_ in host_in:
+                d_.copy_(h, non_blocking=True)
+            layer.step()
+            hout.copy_(layer.out, non_blocking=True)
+            hdx.copy_(layer.dX, non_blocking=True)
+            e.record()
+            e.synchronize()
+            times.append(s.elapsed_time(e))
+        barrier()
+        ms = allmax(statistics.mean(times))
+        return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    w = wl.get_workload(args.workload)
+    inp = wl.generate(w, seed=args.seed + rank)
+    main = timed(w, inp, args.steps, args.warmup, with_e2e=True)
+    del inp
+    cmp_res = None
+    if args.compare:
+        w2 = wl.get_workload(args.compare)
+        inp2 = wl.generate(w2, seed=args.seed + rank)
+        cmp_res = timed(w2, inp2, args.steps, args.warmup, with_e2e=False, sample_clocks=False)
+        cmp_res["workload"] = w2.name
+        del inp2
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    ms = main["ms_per_step"]
+    value = world * w.T / (ms / 1e3)
+    km = main["kernels_ms"]
+    flops, bytes_ = work_per_launch(w)
+    # the dominant kernel: the single-kernel call with the largest share of the step
+    single = {k: v for k, v in km.items() if k in flops or k in bytes_}
+    dom = max(single, key=single.get)
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            prof = json.load(f).get(dom)
+        kind = "gemm" if dom in flops else "rows"
+        if prof and prof.get("src_sha") == sources_sha(kind) and prof.get("workload") == w.key:
+            traffic = prof["dram_bytes_per_launch"]
+    except (OSError, ValueError):
+        pass
+    if dom in flops:
+        ach = flops[dom] / (km[dom] / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic,
+                "algorithmic_flops_per_launch": flops[dom],
+                "peak_note": f"{peaks['source']} cuBLAS bf16, sustained"}
+    else:
+        ach = bytes_[dom] / (km[dom] / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": traffic,
+                "algorithmic_bytes_per_launch": bytes_[dom],
+                "peak_note": f"{peaks['source']} copy bandwidth"}
+    gemm_labels = [k for k in flops if k in km]
+    gemm_ms = sum(km[k] for k in gemm_labels)
+    gemm_tflops = sum(flops[k] for k in gemm_labels) / (gemm_ms / 1e3) / 1e12
+    rows = {k: {"ms": km[k], "GB_s": bytes_[k] / (km[k] / 1e3) / 1e9,
+                "frac_hbm": bytes_[k] / (km[k] / 1e3) / 1e9 / peaks["hbm_gbs"]}
+            for k in bytes_ if k in km}
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded normals (x, W, dY), uniform random top-4 routing",
+        "config": {"workload": w.name, "key": w.key, "T": w.T, "d": w.d, "E": w.E, "k": w.k,
+                   "h": w.h, "routing": w.routing, "tokens_per_gpu": w.T,
+                   "l2": "flushed between timed steps (512 MB write)",
+                   "parallelism": f"{world} replica(s), token-sharded, no data-path collective"},
+        "roofline": roof,
+        "gemm": {"tflops": gemm_tflops, "frac_of_peak": gemm_tflops / peaks["bf16_tflops_sustained"],
+                 "ms": gemm_ms},
+        "dispatch_gbs": rows.get("dispatch", {}).get("GB_s"),
+        "row_kernels": rows,
+        "kernels_ms": km,
+        "e2e": main["e2e"],
+        "gpu_launches": main["launches"],
+        "clocks": main["clocks"],
+    }
+    if cmp_res is not None:
+        cv = world * wl.get_workload(args.compare).T / (cmp_res["ms_per_step"] / 1e3)
+        out["compare"] = {"workload": cmp_res["workload"], "value": cv, "unit": UNIT,
+                          "ms_per_step": cmp_res["ms_per_step"], "ratio_to_main": cv / value,
+                          "kernels_ms": cmp_res["kernels_ms"], "gpu_launches": cmp_res["launches"]}
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_seconds)
+    print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def device_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:  # noqa: BLE001
+        return None
+
+
+# ------------------------------------------------------------ oracle timing
+
+def _oracle_step(w, inp, Ts):
+    """fp64 oracle forward + backward on the first Ts tokens of the workload."""
+    import oracle.layer as ol
+    sub = dict(inp)
+    for key in ("x", "dY", "idx", "glogit"):
+        if key in sub:
+            sub[key] = inp[key][:Ts]
+    t0 = time.perf_counter()
+    fwd = ol.layer_forward(sub, w.k, w.E)
+    ol.layer_backward(sub, fwd, w.k, w.E)
+    return time.perf_counter() - t0
+
+
+def _calibrate(w, inp, seconds):
+    t = _oracle_step(w, inp, 256)
+    Ts = int(256 * seconds / max(t, 1e-3))
+    return max(64, min(w.T, Ts))
+
+
+def cpu_baseline(w, seed, seconds):
+    from token_dispatch_grouped_router_gb300 import workloads as wl
+    inp = wl.generate(w, seed=seed)
+    Ts = _calibrate(w, inp, seconds)
+    dt = _oracle_step(w, inp, Ts)
+    return {"value": Ts / dt, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"first {Ts} of {w.T} tokens of {w.key}, full weights, fp64 numpy "
+                      f"forward+backward, one pass"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from token_dispatch_grouped_router_gb300 import workloads as wl
+    w = wl.get_workload(args.workload)
+    inp = wl.generate(w, seed=args.seed)
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)   # a few minutes in total
+    Ts = _calibrate(w, inp, per_step)
+    for _ in range(args.warmup):
+        _oracle_step(w, inp, Ts)
+    times = [_oracle_step(w, inp, Ts) for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    value = Ts / (ms / 1e3)
+    sample = (f"first {Ts} of {w.T} tokens of {w.key} per step, full weights, fp64 numpy "
+              "forward+backward")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic: seeded normals (x, W, dY), uniform random top-4 routing",
+           "config": {"workload": w.name, "key": w.key, "T": w.T, "d": w.d, "E": w.E, "k": w.k,
+                      "h": w.h, "routing": w.routing, "tokens_per_step": Ts},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

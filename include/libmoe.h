@@ -203,6 +203,40 @@ int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets,
                            moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2,
                            void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The phases of the two calls above, one tcgen05 kernel each, for callers
+ * that schedule or time them separately.  Same argument meanings; each phase
+ * needs its inputs from the previous one in stream order:
+ *   fwd_up    h1, h3, a  from xp          (a = silu(h1) * h3)
+ *   fwd_down  yp         from a
+ *   bwd_dact  dh1, dh3   from dyp, h1, h3 (dA = dyp W2^T, SwiGLU backward)
+ *   bwd_dx    dxp        from dh1, dh3
+ *   bwd_wgrad dW1, dW3, dW2 from xp, a, dh1, dh3, dyp (R = 0 writes zeros) */
+int moe_grouped_swiglu_fwd_up(const moe_bf16_t* xp, const int32_t* offsets, int R,
+                              int E, int d, int h, const moe_bf16_t* W1,
+                              const moe_bf16_t* W3, moe_bf16_t* h1, moe_bf16_t* h3,
+                              moe_bf16_t* a, void* ws, size_t ws_bytes,
+                              moe_stream_t stream);
+int moe_grouped_swiglu_fwd_down(const moe_bf16_t* a, const int32_t* offsets, int R,
+                                int E, int d, int h, const moe_bf16_t* W2,
+                                moe_bf16_t* yp, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+int moe_grouped_swiglu_bwd_dact(const int32_t* offsets, int R, int E, int d, int h,
+                                const moe_bf16_t* W2, const moe_bf16_t* h1,
+                                const moe_bf16_t* h3, const moe_bf16_t* dyp,
+                                moe_bf16_t* dh1, moe_bf16_t* dh3, void* ws,
+                                size_t ws_bytes, moe_stream_t stream);
+int moe_grouped_swiglu_bwd_dx(const int32_t* offsets, int R, int E, int d, int h,
+                              const moe_bf16_t* W1, const moe_bf16_t* W3,
+                              const moe_bf16_t* dh1, const moe_bf16_t* dh3,
+                              moe_bf16_t* dxp, void* ws, size_t ws_bytes,
+                              moe_stream_t stream);
+int moe_grouped_swiglu_bwd_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R,
+                                 int E, int d, int h, const moe_bf16_t* a,
+                                 const moe_bf16_t* dyp, const moe_bf16_t* dh1,
+                                 const moe_bf16_t* dh3, moe_bf16_t* dW1,
+                                 moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -302,3 +302,22 @@ def test_full_size_sampled(key):
         zd = zdev[tk].cpu().numpy()
         assert_close(zd, ol.router_logits(ol.decode_bf16(inp["x"])[toks], inp["W_r"], inp["b"],
                                           np.float64), "logits", rel_l2=1e-5, max_abs=1e-5)
+
+
+def test_combined_calls_equal_the_phase_calls():
+    w = wl.small_workload(T=900, d=256, E=12, k=4, h=192)
+    inp = wl.generate(w, seed=8)
+    layer = make_layer(w, inp)
+    run(layer)                     # phase by phase (fwd_up, fwd_down, bwd_dact, bwd_dx, bwd_wgrad)
+    keep = {n: getattr(layer, n).clone() for n in ("h1", "h3", "a", "yp", "dh1", "dh3", "dxp",
+                                                   "dW1", "dW3", "dW2")}
+    for n in keep:
+        getattr(layer, n).zero_()
+    L.moe_grouped_swiglu_fwd(layer.xp, layer.offsets, layer.W1, layer.W3, layer.W2, layer.h1,
+                             layer.h3, layer.a, layer.yp, layer.ws)
+    L.moe_grouped_swiglu_bwd(layer.xp, layer.offsets, layer.W1, layer.W3, layer.W2, layer.h1,
+                             layer.h3, layer.a, layer.dyp, layer.dh1, layer.dh3, layer.dxp,
+                             layer.dW1, layer.dW3, layer.dW2, layer.ws)
+    torch.cuda.synchronize()
+    for n, v in keep.items():
+        assert torch.equal(getattr(layer, n), v), n

@@ -579,49 +579,84 @@ int row_grid_upper(int R, int E, int n_tiles) {
 
 using namespace moe;
 
-extern "C" {
+namespace moe {
+namespace {
 
-int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
-                           const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
-                           moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a, moe_bf16_t* yp, void* ws,
-                           size_t ws_bytes, moe_stream_t stream) {
-  int st = check_common(ws, ws_bytes, R, E, d, h);
-  if (st != MOE_OK) return st;
-  if (R == 0) return MOE_OK;
-  MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3);
-  MOE_CHECK_PTR(W2); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(a); MOE_CHECK_PTR(yp);
-  cudaStream_t s = (cudaStream_t)stream;
-  CUtensorMap mx, mw1, mw3, ma, mw2;
-  if (!map2d(&mx, xp, d, R, 64, BM) || !map3d(&mw1, W1, h, d, E, 64, 64) ||
-      !map3d(&mw3, W3, h, d, E, 64, 64) || !map2d(&ma, a, h, R, 64, BM) ||
-      !map3d(&mw2, W2, d, h, E, 64, 64))
-    return MOE_ERR_CUDA;
+GemmArgs base_args(const int32_t* offsets, int R, int E, int d, int h, void* ws) {
   GemmArgs g{};
   g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
-  // up-projection + SwiGLU: N tiles of 128 h-columns (x2 for W1 and W3)
-  g.n_tiles = (h + BN / 2 - 1) / (BN / 2);
-  g.kb_total = d / BK;
-  g.out0 = h1; g.out1 = h3; g.out2 = a; g.ldo = h;
-  st = launch<kUp>(mx, mx, mw1, mw3, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
-  if (st != MOE_OK) return st;
-  // down-projection
-  GemmArgs g2 = g;
-  g2.n_tiles = (d + BN - 1) / BN;
-  g2.kb_total = h / BK;
-  g2.out0 = yp; g2.out1 = nullptr; g2.out2 = nullptr; g2.ldo = d;
-  return launch<kDown>(ma, ma, mw2, mw2, mw2, g2, row_grid_upper(R, E, g2.n_tiles), s);
+  return g;
 }
 
-int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
-                           const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
-                           const moe_bf16_t* h1, const moe_bf16_t* h3, const moe_bf16_t* a,
-                           const moe_bf16_t* dyp, moe_bf16_t* dh1, moe_bf16_t* dh3, moe_bf16_t* dxp,
-                           moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
-                           size_t ws_bytes, moe_stream_t stream) {
-  int st = check_common(ws, ws_bytes, R, E, d, h);
-  if (st != MOE_OK) return st;
+// [h1 | h3] = xp_e @ [W1[e] | W3[e]], a = silu(h1) * h3
+int run_up(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
+           const moe_bf16_t* W1, const moe_bf16_t* W3, moe_bf16_t* h1, moe_bf16_t* h3,
+           moe_bf16_t* a, void* ws, cudaStream_t s) {
+  MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3);
+  MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(a);
+  CUtensorMap mx, mw1, mw3;
+  if (!map2d(&mx, xp, d, R, 64, BM) || !map3d(&mw1, W1, h, d, E, 64, 64) ||
+      !map3d(&mw3, W3, h, d, E, 64, 64))
+    return MOE_ERR_CUDA;
+  GemmArgs g = base_args(offsets, R, E, d, h, ws);
+  g.n_tiles = (h + BN / 2 - 1) / (BN / 2);      // 128 h-columns of W1 and of W3 per tile
+  g.kb_total = d / BK;
+  g.out0 = h1; g.out1 = h3; g.out2 = a; g.ldo = h;
+  return launch<kUp>(mx, mx, mw1, mw3, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
+}
+
+// yp = a_e @ W2[e]
+int run_down(const moe_bf16_t* a, const int32_t* offsets, int R, int E, int d, int h,
+             const moe_bf16_t* W2, moe_bf16_t* yp, void* ws, cudaStream_t s) {
+  MOE_CHECK_PTR(a); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W2); MOE_CHECK_PTR(yp);
+  CUtensorMap ma, mw2;
+  if (!map2d(&ma, a, h, R, 64, BM) || !map3d(&mw2, W2, d, h, E, 64, 64)) return MOE_ERR_CUDA;
+  GemmArgs g = base_args(offsets, R, E, d, h, ws);
+  g.n_tiles = (d + BN - 1) / BN;
+  g.kb_total = h / BK;
+  g.out0 = yp; g.ldo = d;
+  return launch<kDown>(ma, ma, mw2, mw2, mw2, g, row_grid_upper(R, E, g.n_tiles), s);
+}
+
+// dA = dyp_e @ W2[e]^T with the SwiGLU backward epilogue -> dh1, dh3
+int run_dact(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t* W2,
+             const moe_bf16_t* h1, const moe_bf16_t* h3, const moe_bf16_t* dyp, moe_bf16_t* dh1,
+             moe_bf16_t* dh3, void* ws, cudaStream_t s) {
+  MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W2); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3);
+  MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dh1); MOE_CHECK_PTR(dh3);
+  CUtensorMap m_dyp, m_w2k;
+  if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, BN)) return MOE_ERR_CUDA;
+  GemmArgs g = base_args(offsets, R, E, d, h, ws);
+  g.n_tiles = (h + BN - 1) / BN;
+  g.kb_total = d / BK;
+  g.out0 = dh1; g.out1 = dh3; g.in0 = h1; g.in1 = h3; g.ldo = h;
+  return launch<kDA>(m_dyp, m_dyp, m_w2k, m_w2k, m_w2k, g, row_grid_upper(R, E, g.n_tiles), s);
+}
+
+// dxp = dh1_e @ W1[e]^T + dh3_e @ W3[e]^T (one reduction over K = 2h)
+int run_dx(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t* W1,
+           const moe_bf16_t* W3, const moe_bf16_t* dh1, const moe_bf16_t* dh3, moe_bf16_t* dxp,
+           void* ws, cudaStream_t s) {
+  MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3); MOE_CHECK_PTR(dh1);
+  MOE_CHECK_PTR(dh3); MOE_CHECK_PTR(dxp);
+  CUtensorMap m_dh1, m_dh3, m_w1k, m_w3k;
+  if (!map2d(&m_dh1, dh1, h, R, 64, BM) || !map2d(&m_dh3, dh3, h, R, 64, BM) ||
+      !map3d(&m_w1k, W1, h, d, E, 64, BN) || !map3d(&m_w3k, W3, h, d, E, 64, BN))
+    return MOE_ERR_CUDA;
+  GemmArgs g = base_args(offsets, R, E, d, h, ws);
+  g.n_tiles = (d + BN - 1) / BN;
+  g.kb_total = 2 * (h / BK);
+  g.kb_split = h / BK;
+  g.out0 = dxp; g.ldo = d;
+  return launch<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, m_w3k, g, row_grid_upper(R, E, g.n_tiles), s);
+}
+
+// dW1[e] = xp_e^T dh1_e, dW3[e] = xp_e^T dh3_e, dW2[e] = a_e^T dyp_e (one launch)
+int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
+              const moe_bf16_t* a, const moe_bf16_t* dyp, const moe_bf16_t* dh1,
+              const moe_bf16_t* dh3, moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
+              cudaStream_t s) {
   MOE_CHECK_PTR(dW1); MOE_CHECK_PTR(dW3); MOE_CHECK_PTR(dW2);
-  cudaStream_t s = (cudaStream_t)stream;
   if (R == 0) {
     const size_t wb = (size_t)E * d * h * 2;
     if (cudaMemsetAsync(dW1, 0, wb, s) != cudaSuccess || cudaMemsetAsync(dW3, 0, wb, s) != cudaSuccess ||
@@ -631,45 +666,106 @@ int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets, int R, 
     }
     return MOE_OK;
   }
-  MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3); MOE_CHECK_PTR(W2);
-  MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(a); MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dh1);
-  MOE_CHECK_PTR(dh3); MOE_CHECK_PTR(dxp);
-  CUtensorMap m_dyp, m_w2k, m_dh1, m_dh3, m_w1k, m_w3k, m_xpt, m_at, m_dh1t, m_dh3t, m_dypt;
-  // K-major operands (row-grouped dgrad GEMMs)
-  if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, BN) ||
-      !map2d(&m_dh1, dh1, h, R, 64, BM) || !map2d(&m_dh3, dh3, h, R, 64, BM) ||
-      !map3d(&m_w1k, W1, h, d, E, 64, BN) || !map3d(&m_w3k, W3, h, d, E, 64, BN) ||
-      // MN-major operands of the weight-gradient GEMMs (64x64 boxes)
-      !map2d(&m_xpt, xp, d, R, 64, 64) || !map2d(&m_at, a, h, R, 64, 64) ||
+  MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(a); MOE_CHECK_PTR(dyp);
+  MOE_CHECK_PTR(dh1); MOE_CHECK_PTR(dh3);
+  CUtensorMap m_xpt, m_at, m_dh1t, m_dh3t, m_dypt;
+  // MN-major operands: 64 x 64 boxes along (feature, row)
+  if (!map2d(&m_xpt, xp, d, R, 64, 64) || !map2d(&m_at, a, h, R, 64, 64) ||
       !map2d(&m_dh1t, dh1, h, R, 64, 64) || !map2d(&m_dh3t, dh3, h, R, 64, 64) ||
       !map2d(&m_dypt, dyp, d, R, 64, 64))
     return MOE_ERR_CUDA;
-  GemmArgs g{};
-  g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
-  // dA = dyp @ W2^T with the SwiGLU backward epilogue -> dh1, dh3
-  g.n_tiles = (h + BN - 1) / BN;
-  g.kb_total = d / BK;
-  g.out0 = dh1; g.out1 = dh3; g.in0 = h1; g.in1 = h3; g.ldo = h;
-  st = launch<kDA>(m_dyp, m_dyp, m_w2k, m_w2k, m_w2k, g, row_grid_upper(R, E, g.n_tiles), s);
-  if (st != MOE_OK) return st;
-  // dxp = dh1 @ W1^T + dh3 @ W3^T (one reduction over K = 2h)
-  GemmArgs g2 = g;
-  g2.n_tiles = (d + BN - 1) / BN;
-  g2.kb_total = 2 * (h / BK);
-  g2.kb_split = h / BK;
-  g2.out0 = dxp; g2.out1 = nullptr; g2.in0 = nullptr; g2.in1 = nullptr; g2.ldo = d;
-  st = launch<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, m_w3k, g2, row_grid_upper(R, E, g2.n_tiles), s);
-  if (st != MOE_OK) return st;
-  // weight gradients, reduction over each expert's own rows
-  GemmArgs g3 = g;
-  g3.out0 = dW1; g3.out1 = dW3; g3.out2 = dW2; g3.in0 = nullptr; g3.in1 = nullptr;
-  g3.wg_mt1 = (d + BM - 1) / BM;
-  g3.wg_mt2 = (h + BM - 1) / BM;
-  g3.wg_t1 = g3.wg_mt1 * ((h + BN - 1) / BN);
-  g3.wg_t2 = g3.wg_mt2 * ((d + BN - 1) / BN);
-  long long tiles = (long long)E * (2 * g3.wg_t1 + g3.wg_t2);
+  GemmArgs g = base_args(offsets, R, E, d, h, ws);
+  g.out0 = dW1; g.out1 = dW3; g.out2 = dW2;
+  g.wg_mt1 = (d + BM - 1) / BM;
+  g.wg_mt2 = (h + BM - 1) / BM;
+  g.wg_t1 = g.wg_mt1 * ((h + BN - 1) / BN);
+  g.wg_t2 = g.wg_mt2 * ((d + BN - 1) / BN);
+  long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
   int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  return launch<kWG>(m_xpt, m_at, m_dh1t, m_dh3t, m_dypt, g3, grid, s);
+  return launch<kWG>(m_xpt, m_at, m_dh1t, m_dh3t, m_dypt, g, grid, s);
+}
+
+}  // namespace
+}  // namespace moe
+
+#define MOE_GEMM_PROLOGUE()                                   \
+  int st = check_common(ws, ws_bytes, R, E, d, h);            \
+  if (st != MOE_OK) return st;                                \
+  cudaStream_t s = (cudaStream_t)stream;                      \
+  (void)s
+
+extern "C" {
+
+int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
+                           const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                           moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a, moe_bf16_t* yp, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R == 0) return MOE_OK;
+  MOE_CHECK_PTR(W2); MOE_CHECK_PTR(yp);
+  st = run_up(xp, offsets, R, E, d, h, W1, W3, h1, h3, a, ws, s);
+  if (st != MOE_OK) return st;
+  return run_down(a, offsets, R, E, d, h, W2, yp, ws, s);
+}
+
+int moe_grouped_swiglu_fwd_up(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
+                              int h, const moe_bf16_t* W1, const moe_bf16_t* W3, moe_bf16_t* h1,
+                              moe_bf16_t* h3, moe_bf16_t* a, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R == 0) return MOE_OK;
+  return run_up(xp, offsets, R, E, d, h, W1, W3, h1, h3, a, ws, s);
+}
+
+int moe_grouped_swiglu_fwd_down(const moe_bf16_t* a, const int32_t* offsets, int R, int E, int d,
+                                int h, const moe_bf16_t* W2, moe_bf16_t* yp, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R == 0) return MOE_OK;
+  return run_down(a, offsets, R, E, d, h, W2, yp, ws, s);
+}
+
+int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
+                           const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                           const moe_bf16_t* h1, const moe_bf16_t* h3, const moe_bf16_t* a,
+                           const moe_bf16_t* dyp, moe_bf16_t* dh1, moe_bf16_t* dh3, moe_bf16_t* dxp,
+                           moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R > 0) {
+    st = run_dact(offsets, R, E, d, h, W2, h1, h3, dyp, dh1, dh3, ws, s);
+    if (st != MOE_OK) return st;
+    st = run_dx(offsets, R, E, d, h, W1, W3, dh1, dh3, dxp, ws, s);
+    if (st != MOE_OK) return st;
+  }
+  return run_wgrad(xp, offsets, R, E, d, h, a, dyp, dh1, dh3, dW1, dW3, dW2, ws, s);
+}
+
+int moe_grouped_swiglu_bwd_dact(const int32_t* offsets, int R, int E, int d, int h,
+                                const moe_bf16_t* W2, const moe_bf16_t* h1, const moe_bf16_t* h3,
+                                const moe_bf16_t* dyp, moe_bf16_t* dh1, moe_bf16_t* dh3, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R == 0) return MOE_OK;
+  return run_dact(offsets, R, E, d, h, W2, h1, h3, dyp, dh1, dh3, ws, s);
+}
+
+int moe_grouped_swiglu_bwd_dx(const int32_t* offsets, int R, int E, int d, int h,
+                              const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* dh1,
+                              const moe_bf16_t* dh3, moe_bf16_t* dxp, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R == 0) return MOE_OK;
+  return run_dx(offsets, R, E, d, h, W1, W3, dh1, dh3, dxp, ws, s);
+}
+
+int moe_grouped_swiglu_bwd_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
+                                 int h, const moe_bf16_t* a, const moe_bf16_t* dyp,
+                                 const moe_bf16_t* dh1, const moe_bf16_t* dh3, moe_bf16_t* dW1,
+                                 moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  return run_wgrad(xp, offsets, R, E, d, h, a, dyp, dh1, dh3, dW1, dW3, dW2, ws, s);
 }
 
 }  // extern "C"

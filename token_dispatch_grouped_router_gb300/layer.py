@@ -5,8 +5,8 @@ memory and the stream) and runs forward and backward purely through the C-ABI
 entry points:
 
 forward : [router_logits ->] router_topk | router_gates -> expert_offsets ->
-          dispatch_rows -> grouped_swiglu_fwd -> combine
-backward: combine_bwd -> grouped_swiglu_bwd -> combine(gates = None) ->
+          dispatch_rows -> grouped_swiglu_fwd (up, down) -> combine
+backward: combine_bwd -> grouped_swiglu_bwd (dact, dx, wgrad) -> combine(gates = None) ->
           router_topk_bwd [-> router_logits_bwd]
 
 Nothing is copied back to the host and nothing waits on the host.
@@ -30,6 +30,10 @@ def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """torch.bfloat16 tensor -> uint16 bit patterns (numpy, host)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _nomark(label: str) -> None:
+    return None
 
 
 class MoELayer:
@@ -102,41 +106,67 @@ class MoELayer:
         self.logits_given = True
 
     # ------------------------------------------------------------ forward
-    def route(self) -> None:
+    # `mark(label)` (optional) is called before each library call and with
+    # "end" after the last one; the benchmark records CUDA events there.
+    def route(self, mark=None) -> None:
+        mark = mark or _nomark
         if self.learned:
             if not self.logits_given:
+                mark("router_logits")
                 L.moe_router_logits(self.x, self.W_r, self.b, self.logits)
+            mark("router_topk")
             L.moe_router_topk(self.logits, self.k, self.idx, self.gate)
         else:
+            mark("router_gates")
             L.moe_router_gates(self.glogit, self.gate)
+        mark("expert_offsets")
         L.moe_expert_offsets(self.idx, self.E, self.counts, self.offsets, self.row_of_slot,
                              self.slot_of_row, self.ws)
 
-    def forward(self) -> torch.Tensor:
-        self.route()
+    def forward(self, mark=None) -> torch.Tensor:
+        mark = mark or _nomark
+        self.route(mark)
+        mark("dispatch")
         L.moe_dispatch_rows(self.x, self.row_of_slot, self.k, self.xp)
-        L.moe_grouped_swiglu_fwd(self.xp, self.offsets, self.W1, self.W3, self.W2,
-                                 self.h1, self.h3, self.a, self.yp, self.ws)
+        mark("gemm_up")
+        L.moe_grouped_swiglu_fwd_up(self.xp, self.offsets, self.W1, self.W3, self.h1, self.h3,
+                                    self.a, self.ws)
+        mark("gemm_down")
+        L.moe_grouped_swiglu_fwd_down(self.a, self.offsets, self.W2, self.yp, self.ws)
+        mark("combine")
         L.moe_combine(self.yp, self.row_of_slot, self.gate, self.k, self.out)
         return self.out
 
     # ----------------------------------------------------------- backward
-    def backward(self) -> None:
+    def backward(self, mark=None) -> None:
+        mark = mark or _nomark
+        mark("combine_bwd")
         L.moe_combine_bwd(self.dY, self.yp, self.row_of_slot, self.gate, self.k,
                           self.dyp, self.dgate)
-        L.moe_grouped_swiglu_bwd(self.xp, self.offsets, self.W1, self.W3, self.W2,
-                                 self.h1, self.h3, self.a, self.dyp, self.dh1, self.dh3,
-                                 self.dxp, self.dW1, self.dW3, self.dW2, self.ws)
+        mark("gemm_dact")
+        L.moe_grouped_swiglu_bwd_dact(self.offsets, self.W2, self.h1, self.h3, self.dyp,
+                                      self.dh1, self.dh3, self.ws)
+        mark("gemm_dx")
+        L.moe_grouped_swiglu_bwd_dx(self.offsets, self.W1, self.W3, self.dh1, self.dh3,
+                                    self.dxp, self.ws)
+        mark("gemm_wgrad")
+        L.moe_grouped_swiglu_bwd_wgrad(self.xp, self.offsets, self.a, self.dyp, self.dh1,
+                                       self.dh3, self.dW1, self.dW3, self.dW2, self.ws)
+        mark("unpermute")
         L.moe_combine(self.dxp, self.row_of_slot, None, self.k, self.dX)
+        mark("router_bwd")
         L.moe_router_topk_bwd(self.gate, self.dgate, self.idx, self.E, self.dlogits)
         if self.learned:
+            mark("router_logits_bwd")
             L.moe_router_logits_bwd(self.x, self.W_r, self.dlogits, self.dX, self.dW_r,
                                     self.db, self.ws)
 
-    def step(self) -> None:
-        self.forward()
+    def step(self, mark=None) -> None:
+        self.forward(mark)
         if self.with_backward:
-            self.backward()
+            self.backward(mark)
+        if mark is not None:
+            mark("end")
 
     def launches_per_step(self) -> int:
         n = (2 if self.learned and not self.logits_given else 1) + 3 + 1 + 2 + 1   # forward

@@ -41,6 +41,12 @@ SIGNATURES = {
                                     _Z, _P]),
     "moe_grouped_swiglu_bwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_grouped_swiglu_fwd_up": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_grouped_swiglu_fwd_down": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    "moe_grouped_swiglu_bwd_dact": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_grouped_swiglu_bwd_dx": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_grouped_swiglu_bwd_wgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                          _P, _Z, _P]),
 }
 
 _lib = None
@@ -232,3 +238,59 @@ def moe_grouped_swiglu_bwd(xp, offsets, W1, W3, W2, h1, h3, a, dyp, dh1, dh3, dx
         _ptr(xp), _ptr(offsets), R, E, d, h, _ptr(W1), _ptr(W3), _ptr(W2), _ptr(h1), _ptr(h3),
         _ptr(a), _ptr(dyp), _ptr(dh1), _ptr(dh3), _ptr(dxp), _ptr(dW1), _ptr(dW3), _ptr(dW2),
         _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+def _wsb(ws):
+    return ws.numel() * ws.element_size()
+
+
+def moe_grouped_swiglu_fwd_up(xp, offsets, W1, W3, h1, h3, a, ws) -> None:
+    R, d = xp.shape
+    E, _, h = W1.shape
+    for n, t in (("h1", h1), ("h3", h3), ("a", a)):
+        _want(t, torch.bfloat16, (R, h), n)
+    _want(W3, torch.bfloat16, (E, d, h), "W3")
+    _ok("moe_grouped_swiglu_fwd_up", load().moe_grouped_swiglu_fwd_up(
+        _ptr(xp), _ptr(offsets), R, E, d, h, _ptr(W1), _ptr(W3), _ptr(h1), _ptr(h3), _ptr(a),
+        _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_grouped_swiglu_fwd_down(a, offsets, W2, yp, ws) -> None:
+    R, h = a.shape
+    E, _, d = W2.shape
+    _want(W2, torch.bfloat16, (E, h, d), "W2"); _want(yp, torch.bfloat16, (R, d), "yp")
+    _ok("moe_grouped_swiglu_fwd_down", load().moe_grouped_swiglu_fwd_down(
+        _ptr(a), _ptr(offsets), R, E, d, h, _ptr(W2), _ptr(yp), _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_grouped_swiglu_bwd_dact(offsets, W2, h1, h3, dyp, dh1, dh3, ws) -> None:
+    R, d = dyp.shape
+    E, h, _ = W2.shape
+    for n, t in (("h1", h1), ("h3", h3), ("dh1", dh1), ("dh3", dh3)):
+        _want(t, torch.bfloat16, (R, h), n)
+    _ok("moe_grouped_swiglu_bwd_dact", load().moe_grouped_swiglu_bwd_dact(
+        _ptr(offsets), R, E, d, h, _ptr(W2), _ptr(h1), _ptr(h3), _ptr(dyp), _ptr(dh1),
+        _ptr(dh3), _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_grouped_swiglu_bwd_dx(offsets, W1, W3, dh1, dh3, dxp, ws) -> None:
+    R, d = dxp.shape
+    E, _, h = W1.shape
+    _want(dh1, torch.bfloat16, (R, h), "dh1"); _want(dh3, torch.bfloat16, (R, h), "dh3")
+    _want(W3, torch.bfloat16, (E, d, h), "W3")
+    _ok("moe_grouped_swiglu_bwd_dx", load().moe_grouped_swiglu_bwd_dx(
+        _ptr(offsets), R, E, d, h, _ptr(W1), _ptr(W3), _ptr(dh1), _ptr(dh3), _ptr(dxp),
+        _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_grouped_swiglu_bwd_wgrad(xp, offsets, a, dyp, dh1, dh3, dW1, dW3, dW2, ws) -> None:
+    R, d = xp.shape
+    E, _, h = dW1.shape
+    for n, t in (("a", a), ("dh1", dh1), ("dh3", dh3)):
+        _want(t, torch.bfloat16, (R, h), n)
+    _want(dyp, torch.bfloat16, (R, d), "dyp")
+    _want(dW1, torch.bfloat16, (E, d, h), "dW1"); _want(dW3, torch.bfloat16, (E, d, h), "dW3")
+    _want(dW2, torch.bfloat16, (E, h, d), "dW2")
+    _ok("moe_grouped_swiglu_bwd_wgrad", load().moe_grouped_swiglu_bwd_wgrad(
+        _ptr(xp), _ptr(offsets), R, E, d, h, _ptr(a), _ptr(dyp), _ptr(dh1), _ptr(dh3),
+        _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(ws), ws.numel() * ws.element_size(), _stream()))
