@@ -144,6 +144,32 @@ int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E,
                        int32_t* row_of_slot, int32_t* slot_of_row,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Allocation-free moe_expert_offsets (no counterpart on the pages).
+ *
+ * For callers that cannot allocate device memory: code running inside a CUDA
+ * stream capture (cudaMalloc/cudaFree are illegal there and synchronise the
+ * device), engines that give a plugin only the tensors from their own
+ * pre-planned arena, and real-time loops that must not block on an allocator.
+ * Same outputs as moe_expert_offsets, but the route-map scratch lives in a
+ * static device array inside libmoe (2 MiB + 256 B, held on every GPU that
+ * loads the library until the process exits) instead of a workspace.
+ *  - Limit: T * k <= 262144; larger sizes return MOE_ERR_UNSUPPORTED and
+ *    launch nothing.
+ *  - status: optional device int32 (4-byte aligned) that receives
+ *    MOE_DEV_BAD_EXPERT_ID like the workspace status word; NULL discards it.
+ *    Clear it yourself before the call if you read it.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the one array and no call clears it (every entry a call
+ *    reads is written earlier in that call): calls that can overlap on the
+ *    GPU (different streams, or concurrent host threads) race and must be
+ *    serialised by the caller.
+ *  - No cudaMalloc/cudaFree or allocating library call is made. */
+int moe_expert_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E,
+                               int32_t* counts, int32_t* offsets,
+                               int32_t* row_of_slot, int32_t* slot_of_row,
+                               int32_t* status, moe_stream_t stream);
+
 /* ------------------------------------------------------- dispatch/combine */
 
 /* Rowwise dispatch: xp[row_of_slot[t*k+j], :] = x[t, :] for all t, j.

@@ -190,3 +190,89 @@ extern "C" int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E, 
   MOE_LAUNCH_CHECK(3);
   return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of moe_expert_offsets.
+//
+// For callers that cannot allocate device memory: code that runs while a
+// stream is being captured into a CUDA graph (cudaMalloc/cudaFree are not
+// allowed there and synchronise the device), engines that hand a plugin only
+// the tensors they own from a pre-planned arena, and real-time loops that must
+// never block on the allocator.  The route-map scratch (per-chunk expert
+// histograms and in-chunk ranks) lives in this file-scope device array
+// instead of a caller workspace.  Every GPU that loads the library keeps the
+// array (2 MiB + 256 B) until the process exits.
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxSlots = 262144;                                // T * k
+constexpr int kNoAllocChunkInts = (kNoAllocMaxSlots / kRouteChunk) * kMaxExperts;
+constexpr int kNoAllocDummyInts = 64;                                   // status sink
+
+static __device__ __align__(256) int32_t
+    g_route_scratch[kNoAllocDummyInts + kNoAllocChunkInts + kNoAllocMaxSlots];
+
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_base[64] = {nullptr};
+
+// Device address of g_route_scratch on the current device (looked up once per
+// device; the host-side symbol itself is not a device address).
+int32_t* noalloc_scratch(int dev) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_base[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_base[dev] = static_cast<int32_t*>(p);
+  }
+  return g_noalloc_base[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_expert_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E,
+                                          int32_t* counts, int32_t* offsets,
+                                          int32_t* row_of_slot, int32_t* slot_of_row,
+                                          int32_t* status, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= kMaxTopK && E >= 1 && E <= kMaxExperts && k <= E);
+  MOE_CHECK_ARG((long long)T * k <= 0x7fffffffLL);
+  MOE_CHECK_PTR(counts); MOE_CHECK_PTR(offsets);
+  if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+  const long long R = (long long)T * k;
+  if (R > kNoAllocMaxSlots) return MOE_ERR_UNSUPPORTED;     // beyond the static scratch
+  if (R > 0) { MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(slot_of_row); }
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  int32_t* base = noalloc_scratch(dev);
+  if (base == nullptr) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (R == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  // every scratch entry the kernels read is written earlier in the same call
+  // (histograms for all chunks x E, ranks for every valid slot), so nothing
+  // has to be cleared between calls
+  int32_t* st = status ? status : base;                     // NULL: errors go to a sink
+  int32_t* chunk_counts = base + kNoAllocDummyInts;
+  int32_t* local_rank = chunk_counts + kNoAllocChunkInts;
+  const int nchunks = (int)((R + kRouteChunk - 1) / kRouteChunk);
+  size_t smem = sizeof(int32_t) * kRCWarps * E;
+  route_count_kernel<<<nchunks, kRCThreads, smem, s>>>(topk_idx, (int)R, E, chunk_counts,
+                                                       local_rank, st);
+  route_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, counts, offsets);
+  route_place_kernel<<<(int)((R + 255) / 256), 256, 0, s>>>(topk_idx, (int)R, E, chunk_counts,
+                                                             local_rank, offsets, row_of_slot,
+                                                             slot_of_row);
+  MOE_LAUNCH_CHECK(3);
+  return MOE_OK;
+}

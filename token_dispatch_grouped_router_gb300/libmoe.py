@@ -34,6 +34,7 @@ SIGNATURES = {
     "moe_router_topk_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_router_logits_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_rows": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
@@ -181,6 +182,20 @@ def moe_expert_offsets(topk_idx, E: int, counts, offsets, row_of_slot, slot_of_r
     _ok("moe_expert_offsets", load().moe_expert_offsets(
         _ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(row_of_slot),
         _ptr(slot_of_row), _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+def moe_expert_offsets_noalloc(topk_idx, E: int, counts, offsets, row_of_slot, slot_of_row,
+                               status=None) -> None:
+    """moe_expert_offsets without a workspace (static device scratch inside
+    the library; T*k <= 262144; see include/libmoe.h)."""
+    T, k = topk_idx.shape
+    _want(topk_idx, torch.int32, (T, k), "topk_idx"); _want(counts, torch.int32, (E,), "counts")
+    _want(offsets, torch.int32, (E + 1,), "offsets")
+    _want(row_of_slot, torch.int32, (T * k,), "row_of_slot")
+    _want(slot_of_row, torch.int32, (T * k,), "slot_of_row")
+    _ok("moe_expert_offsets_noalloc", load().moe_expert_offsets_noalloc(
+        _ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(row_of_slot),
+        _ptr(slot_of_row), _ptr(status), _stream()))
 
 
 # ------------------------------------------------------- dispatch/combine
