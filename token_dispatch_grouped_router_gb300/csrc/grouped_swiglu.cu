@@ -48,8 +48,14 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;            // 16 KB
 constexpr int B_STAGE = BN * BK * 2;            // 32 KB
 constexpr int SUB = 64 * 64 * 2;                // one 64x64 bf16 TMA box (8 KB)
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                    // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue
 constexpr int kTmemCols = 512;
+// per-epilogue-warp staging buffer: a 32-row x 32-column bf16 chunk with an
+// 80-byte row pitch, so both the row-per-thread side and the coalesced side
+// of the transpose are free of bank conflicts
+constexpr int kStagePitch = 80;
+constexpr int kStageBytes = 32 * kStagePitch;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s; a step takes milliseconds
 
 struct GemmArgs {
@@ -181,43 +187,87 @@ __device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa,
   }
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.f + __expf(-x)); }
+// sigmoid through the identity sigmoid(x) = (1 + tanh(x / 2)) / 2 on the
+// hardware tanh approximation (one MUFU op instead of an exp and a divide);
+// its error is far below the bf16 rounding of the stored results
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
+__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
 
-__device__ __forceinline__ void store_row32(uint16_t* dst, const float* v) {
-  uint4 o[4];
+__device__ __forceinline__ void pack_row32(const float* v, uint4 (&o)[4]) {
   uint32_t* w = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
   for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) st_v4(dst + 8 * i, o[i]);
 }
 
-__device__ __forceinline__ void load_row32(const uint16_t* src, float* v) {
+// The warp's 32 rows (one per lane, 32 values each) -> global memory at
+// g[row * ld + 0..31] for rows < nrows, through the staging buffer so that each
+// store instruction writes 8 rows x 64 contiguous bytes.
+__device__ __forceinline__ void store_chunk(uint8_t* stg, const float* v, int lane, uint16_t* g,
+                                            size_t ld, int nrows) {
+  uint4 o[4];
+  pack_row32(v, o);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 q = ld_nc_v4(src + 8 * i);
-    v[8 * i + 0] = bf16_lo(q.x); v[8 * i + 1] = bf16_hi(q.x);
-    v[8 * i + 2] = bf16_lo(q.y); v[8 * i + 3] = bf16_hi(q.y);
-    v[8 * i + 4] = bf16_lo(q.z); v[8 * i + 5] = bf16_hi(q.z);
-    v[8 * i + 6] = bf16_lo(q.w); v[8 * i + 7] = bf16_hi(q.w);
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stg + lane * kStagePitch + 16 * i) = o[i];
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int p = it * 32 + lane, row = p >> 2, c = p & 3;
+    if (row < nrows)
+      st_v4(g + (size_t)row * ld + 8 * c, *reinterpret_cast<const uint4*>(stg + row * kStagePitch + 16 * c));
+  }
+  __syncwarp();
+}
+
+// Coalesced load of a 32-row x 32-column bf16 chunk (8 rows x 64 bytes per
+// instruction); piece it*32+lane holds row (it*32+lane)/4, 16-byte column (..)%4.
+__device__ __forceinline__ void load_chunk(uint4 (&q)[4], const uint16_t* g, size_t ld, int lane,
+                                           int nrows) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int p = it * 32 + lane, row = p >> 2, c = p & 3;
+    q[it] = row < nrows ? ld_nc_v4(g + (size_t)row * ld + 8 * c) : make_uint4(0, 0, 0, 0);
   }
 }
 
-// Epilogue of one tile for the 32 rows of this warp's TMEM lane quarter.
+// Pieces from load_chunk -> this lane's own row (32 bf16 values, packed in pairs).
+__device__ __forceinline__ void chunk_to_row(const uint4 (&q)[4], uint8_t* stg, int lane,
+                                             uint32_t (&w)[16]) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int p = it * 32 + lane, row = p >> 2, c = p & 3;
+    *reinterpret_cast<uint4*>(stg + row * kStagePitch + 16 * c) = q[it];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 t = *reinterpret_cast<const uint4*>(stg + lane * kStagePitch + 16 * i);
+    w[4 * i + 0] = t.x; w[4 * i + 1] = t.y; w[4 * i + 2] = t.z; w[4 * i + 3] = t.w;
+  }
+  __syncwarp();
+}
+
+// Epilogue of one tile for the 32 rows of this warp's TMEM lane quarter and
+// the half `half` of the tile's columns (two warps share a lane quarter).
+// Accumulator rows arrive one per lane (tcgen05.ld 32x32b); global traffic is
+// coalesced through the warp's staging buffer `stg`.
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int lane_q,
-                                              int lane, const GemmArgs& a) {
-  const int r = lane_q * 32 + lane;                 // row inside the tile
+__device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int lane_q, int half,
+                                              int lane, uint8_t* stg, const GemmArgs& a) {
   const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
   if constexpr (MODE == kWG) {
     const int M = tl.which == 2 ? a.h : a.d;
     const int N = tl.which == 2 ? a.d : a.h;
     uint16_t* out = tl.which == 0 ? a.out0 : (tl.which == 1 ? a.out1 : a.out2);
-    const int grow = tl.m0 + r;
-    const bool rv = grow < M;
-    uint16_t* dst = out + ((size_t)tl.e * M + (rv ? grow : 0)) * N;
+    const int r0 = tl.m0 + lane_q * 32;               // first row of this warp's slice
+    const int nrows = min(32, M - r0);
+    uint16_t* g = out + ((size_t)tl.e * M + (nrows > 0 ? r0 : 0)) * N;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * 4; c < half * 4 + 4; ++c) {
       float v[32];
       if (tl.nkb > 0) {
         uint32_t q[32];
@@ -230,21 +280,20 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
       const int col = tl.n0 + c * 32;
-      if (rv && col < N) store_row32(dst + col, v);
+      if (col < N) store_chunk(stg, v, lane, g + col, N, nrows);
     }
   } else {
-    const int grow = tl.row0 + r;
-    const bool rv = r < tl.rows;
-    const size_t ro = (size_t)(rv ? grow : 0) * a.ldo;
+    const int nrows = min(32, tl.rows - lane_q * 32);  // rows of this slice in the segment
+    const size_t r0 = (size_t)tl.row0 + (nrows > 0 ? lane_q * 32 : 0);
     if constexpr (MODE == kUp) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = half * 2; c < half * 2 + 2; ++c) {
         uint32_t q1[32], q3[32];
         tmem_ld32(tbase + c * 32, q1);
         tmem_ld32(tbase + 128 + c * 32, q3);
         tmem_ld_wait();
         const int col = tl.n0 + c * 32;
-        if (rv && col < a.h) {
+        if (col < a.h) {
           float h1[32], h3[32], av[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -252,46 +301,65 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
             h3[i] = __uint_as_float(q3[i]);
             av[i] = silu_f(h1[i]) * h3[i];
           }
-          store_row32(a.out0 + ro + col, h1);
-          store_row32(a.out1 + ro + col, h3);
-          store_row32(a.out2 + ro + col, av);
+          store_chunk(stg, h1, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
+          store_chunk(stg, h3, lane, a.out1 + r0 * a.ldo + col, a.ldo, nrows);
+          store_chunk(stg, av, lane, a.out2 + r0 * a.ldo + col, a.ldo, nrows);
         }
       }
     } else if constexpr (MODE == kDA) {
+      // the h1/h3 chunk loads of chunk c+1 are in flight while chunk c is computed
+      const int c0 = half * 4;
+      uint4 p1[4], p3[4];
+      {
+        const int col = tl.n0 + c0 * 32;
+        load_chunk(p1, a.in0 + r0 * a.ldo + col, a.ldo, lane, col < a.h ? nrows : 0);
+        load_chunk(p3, a.in1 + r0 * a.ldo + col, a.ldo, lane, col < a.h ? nrows : 0);
+      }
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = c0; c < c0 + 4; ++c) {
         uint32_t q[32];
         tmem_ld32(tbase + c * 32, q);
-        tmem_ld_wait();
         const int col = tl.n0 + c * 32;
-        if (rv && col < a.h) {
-          float h1[32], h3[32], g1[32], g3[32];
-          load_row32(a.in0 + ro + col, h1);
-          load_row32(a.in1 + ro + col, h3);
+        uint32_t w1[16], w3[16];                 // h1, h3 of this row, bf16 pairs
+        if (col < a.h) {
+          chunk_to_row(p1, stg, lane, w1);
+          chunk_to_row(p3, stg, lane, w3);
+        }
+        if (c + 1 < c0 + 4) {                  // prefetch buffers are free again
+          const int ncol = col + 32;
+          load_chunk(p1, a.in0 + r0 * a.ldo + ncol, a.ldo, lane, ncol < a.h ? nrows : 0);
+          load_chunk(p3, a.in1 + r0 * a.ldo + ncol, a.ldo, lane, ncol < a.h ? nrows : 0);
+        }
+        tmem_ld_wait();
+        if (col < a.h) {
+          float g1[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
+            const float h1 = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+            const float h3 = (i & 1) ? bf16_hi(w3[i >> 1]) : bf16_lo(w3[i >> 1]);
             const float da = __uint_as_float(q[i]);
-            const float s = 1.f / (1.f + __expf(-h1[i]));
-            g1[i] = da * h3[i] * s * (1.f + h1[i] * (1.f - s));
-            g3[i] = da * h1[i] * s;
+            const float sg = sigmoid_f(h1);
+            g1[i] = da * h3 * sg * (1.f + h1 * (1.f - sg));
+            q[i] = __float_as_uint(da * h1 * sg);                    // dh3 in place
           }
-          store_row32(a.out0 + ro + col, g1);
-          store_row32(a.out1 + ro + col, g3);
+          store_chunk(stg, g1, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
+          store_chunk(stg, reinterpret_cast<const float*>(q), lane, a.out1 + r0 * a.ldo + col,
+                      a.ldo, nrows);
         }
       }
     } else {  // kDown, kDX: plain bf16 store of the accumulator
       const int N = a.d;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * 4; c < half * 4 + 4; ++c) {
         uint32_t q[32];
         tmem_ld32(tbase + c * 32, q);
         tmem_ld_wait();
         const int col = tl.n0 + c * 32;
-        if (rv && col < N) {
+        if (col < N) {
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(q[i]);
-          store_row32(a.out0 + ro + col, v);
+          store_chunk(stg, v, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
         }
       }
     }
@@ -307,7 +375,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  Shared* sh = reinterpret_cast<Shared*>(sB + STAGES * B_STAGE);
+  uint8_t* sStage = sB + STAGES * B_STAGE;                   // kEpiWarps x kStageBytes
+  Shared* sh = reinterpret_cast<Shared*>(sStage + kEpiWarps * kStageBytes);
   int* s_off = reinterpret_cast<int*>(sh + 1);
   int* s_ts = s_off + (args.E + 1);
 
@@ -318,7 +387,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) { mbar_init(smem_u32(&sh->full[s]), 1); mbar_init(smem_u32(&sh->empty[s]), 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(smem_u32(&sh->tfull[s]), 1); mbar_init(smem_u32(&sh->tempty[s]), 4); }
+    for (int s = 0; s < 2; ++s) { mbar_init(smem_u32(&sh->tfull[s]), 1); mbar_init(smem_u32(&sh->tempty[s]), kEpiWarps); }
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
     fence_mbar_init();
@@ -415,28 +484,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
           tc_fence_after();
           const uint32_t sa = smem_u32(sA + stage * A_STAGE);
           const uint32_t sb = smem_u32(sB + stage * B_STAGE);
+          int nkk = BK / 16;
           if constexpr (MODE == kWG) {
             // last block of a ragged reduction: rows past the expert's end
-            // belong to the next expert (or were zero-filled); clear them
+            // belong to the next expert (or were zero-filled).  Skip the
+            // 16-row groups that hold none of this expert's rows and clear the
+            // foreign rows of the one partial group in both operands.
             const int valid = tl.krows - kb * BK;
             if (valid < BK) {
-              uint4 z = make_uint4(0, 0, 0, 0);
-              const int nrows = BK - valid;
-              for (int i = lane; i < 6 * nrows * 8; i += 32) {
-                const int sub = i / (nrows * 8);
-                const int rem = i - sub * nrows * 8;
-                const int row = valid + rem / 8, chunk = rem % 8;
-                uint8_t* base = sub < 2 ? (sA + stage * A_STAGE + sub * SUB)
-                                        : (sB + stage * B_STAGE + (sub - 2) * SUB);
-                *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = z;
+              nkk = (valid + 15) >> 4;
+              const int zlo = valid, zhi = nkk * 16;
+              if (zhi > zlo) {
+                // lane -> (row offset lane/8, 16-byte chunk lane%8) of each
+                // 128-byte row, rows zlo.. in steps of 4, all six 64x64 sub-tiles
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                const int chunk = lane & 7;
+#pragma unroll
+                for (int sub = 0; sub < 6; ++sub) {
+                  uint8_t* base = sub < 2 ? (sA + stage * A_STAGE + sub * SUB)
+                                          : (sB + stage * B_STAGE + (sub - 2) * SUB);
+                  for (int row = zlo + (lane >> 3); row < zhi; row += 4)
+                    *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = z;
+                }
+                fence_proxy_async_smem();
               }
-              fence_proxy_async_smem();
             }
             __syncwarp();
           }
           if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
+            for (int kk = 0; kk < nkk; ++kk) {
               uint64_t ad, bd;
               if constexpr (a_mn) ad = sdesc_sw128(sa + kk * 2048, SUB, 1024);
               else ad = sdesc_sw128(sa + kk * 32, 16, 1024);
@@ -464,13 +540,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   } else {
     // --------------------------------------------------------------- epilogue
     const int lane_q = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;     // which half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, sh, args.status)) break;
       tc_fence_after();
-      epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * BN), lane_q, lane, args);
+      epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * BN), lane_q, half, lane,
+                          sStage + (warp - 2) * kStageBytes, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
@@ -532,7 +610,8 @@ bool map3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t mid, uint64
 }
 
 constexpr size_t smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
+  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)kEpiWarps * kStageBytes +
+         sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
 }
 
 template <int MODE>
