@@ -263,6 +263,50 @@ int moe_grouped_swiglu_bwd_wgrad(const moe_bf16_t* xp, const int32_t* offsets, i
                                  moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
                                  size_t ws_bytes, moe_stream_t stream);
 
+/* ----------------------------------------------------------------- MXFP8 */
+/* MXFP8 = E4M3 codes (uint8) with one E8M0 scale byte (2^(byte-127)) per 32
+ * consecutive elements along a GEMM's reduction dimension ("OLMo-core 3：MoE
+ * 训练栈让专家池越大、吞吐不再越慢", section "一个低精度格式，同时压三个地方").  Scale
+ * rule: e = smallest integer with max|block| <= 448 * 2^e (clamped to
+ * [-127, 127], -127 for an all-zero block); codes = RNE_E4M3(v * 2^-e).  The
+ * page's list of scale steps is garbled; this is the reading that its
+ * surviving sentence (divide by 448, power of two, block max just fits)
+ * supports.  Scale tables are row-major bytes, 4-byte aligned. */
+
+/* src[rows][K] (bf16) -> q[rows][K] codes and scale[rows][K/32].  K % 32 == 0. */
+int moe_mxfp8_quantize_rows(const moe_bf16_t* src, int rows, int K, uint8_t* q,
+                            uint8_t* scale, moe_stream_t stream);
+
+/* Expert weights W[E][K][N] (bf16, K = reduction dim) -> K-major codes
+ * wq[E][N][K] and scales ws[E][N][K/32] (the transposed layout the
+ * block-scaled GEMM reads).  K % 32 == 0, N % 128 == 0.  Call once per
+ * optimizer step for W1, W3 (K = d, N = h) and W2 (K = h, N = d). */
+int moe_mxfp8_quantize_weights(const moe_bf16_t* W, int E, int K, int N,
+                               uint8_t* wq, uint8_t* ws, moe_stream_t stream);
+
+/* Rowwise dispatch of quantised rows: each token row is quantised once along d
+ * and written to its k expert rows: xq[R][d] codes, xs[R][d/32] scales; the
+ * bf16 row also goes to xp[R][d] when xp != NULL (the backward stays bf16).
+ * d % 32 == 0. */
+int moe_dispatch_rows_mxfp8(const moe_bf16_t* x, int T, int d, int k,
+                            const int32_t* row_of_slot, uint8_t* xq, uint8_t* xs,
+                            moe_bf16_t* xp, moe_stream_t stream);
+
+/* Forward of the grouped SwiGLU FFN with MXFP8 GEMM operands and fp32
+ * accumulation (block-scaled tcgen05 MMA): h1 = Xq_e W1q[e], h3 = Xq_e W3q[e],
+ * a = silu(h1) * h3 (bf16 h1, h3, a for the bf16 backward), a quantised along
+ * h into aq[R][h] / as[R][h/32], yp = Aq_e W2q[e] (bf16).  Weights come from
+ * moe_mxfp8_quantize_weights (w1q/w3q [E][h][d], w2q [E][d][h]).  d and h
+ * must be multiples of 128. */
+int moe_grouped_swiglu_fwd_mxfp8(const uint8_t* xq, const uint8_t* xs,
+                                 const int32_t* offsets, int R, int E, int d, int h,
+                                 const uint8_t* w1q, const uint8_t* w1s,
+                                 const uint8_t* w3q, const uint8_t* w3s,
+                                 const uint8_t* w2q, const uint8_t* w2s,
+                                 moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a,
+                                 uint8_t* aq, uint8_t* as, moe_bf16_t* yp,
+                                 void* ws, size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -138,7 +138,7 @@ def expert_ffn_forward_mxfp8(Xp, offsets, W1, W3, W2) -> Dict[str, np.ndarray]:
     R = Xq.shape[0]
     h = np.asarray(W1).shape[2]
     Yp = np.zeros((R, np.asarray(W2).shape[2]))
-    A = np.zeros((R, h))
+    A = np.zeros((R, h)); H1 = np.zeros((R, h)); H3 = np.zeros((R, h))
     for e in range(E):
         lo, hi = off[e], off[e + 1]
         if hi == lo:
@@ -146,8 +146,8 @@ def expert_ffn_forward_mxfp8(Xp, offsets, W1, W3, W2) -> Dict[str, np.ndarray]:
         w1 = qdq(W1[e], axis=0)
         w3 = qdq(W3[e], axis=0)
         w2 = qdq(W2[e], axis=0)
-        H1 = Xq[lo:hi] @ w1
-        H3 = Xq[lo:hi] @ w3
-        A[lo:hi] = silu(H1) * H3
+        H1[lo:hi] = Xq[lo:hi] @ w1
+        H3[lo:hi] = Xq[lo:hi] @ w3
+        A[lo:hi] = silu(H1[lo:hi]) * H3[lo:hi]
         Yp[lo:hi] = qdq(A[lo:hi], axis=1) @ w2
-    return {"A": A, "Yp": Yp}
+    return {"H1": H1, "H3": H3, "A": A, "Yp": Yp}

@@ -1,0 +1,209 @@
+"""GPU parity of the MXFP8 path against the fp64 oracle.
+
+Quantised codes and scales are compared bit-exactly (the inputs are bf16, so
+the scaled value v * 2^-e is exact on both sides and RNE to E4M3 is one
+function).  The block-scaled forward is compared with the oracle's
+quantise -> dequantise -> exact-arithmetic mode within relative L2 4e-2; the
+quantised activation A is computed on the device from fp32 accumulators, so
+its codes are compared through their dequantised values."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.layer as ol
+import oracle.mxfp8 as om
+from token_dispatch_grouped_router_gb300 import libmoe as L
+from token_dispatch_grouped_router_gb300 import workloads as wl
+from token_dispatch_grouped_router_gb300.layer import bf16_tensor
+
+from gpu_helpers import assert_close, as_f64, ensure_built
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+MX_REL_L2 = 4e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+    L.load()
+
+
+def u8(t):
+    return t.detach().cpu().numpy()
+
+
+def _edge_values(rng, rows, K):
+    v = rng.standard_normal((rows, K)).astype(np.float32)
+    v[0] = 0.0                                              # all-zero block row
+    v[1, :32] = np.float32(448.0) * np.float32(2.0) ** rng.integers(-20, 20)   # exact fits
+    v[2] *= np.float32(1e-30)                               # tiny magnitudes
+    v[3, ::2] = -0.0                                        # signed zeros
+    v[4] *= np.float32(1e30)                                # huge magnitudes
+    return wl.bf16_bits(v)
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (37, 96), (513, 2048)])
+def test_quantize_rows_bit_exact(rows, K):
+    rng = np.random.default_rng(rows + K)
+    x = _edge_values(rng, max(rows, 5), K)[:rows]
+    q = torch.empty(rows, K, dtype=torch.uint8, device=DEV)
+    s = torch.empty(rows, K // 32, dtype=torch.uint8, device=DEV)
+    L.moe_mxfp8_quantize_rows(bf16_tensor(x, DEV), q, s)
+    qr, sr = om.quantize_blocks(x, axis=1)
+    assert np.array_equal(u8(s), sr)
+    assert np.array_equal(u8(q), qr)
+
+
+@pytest.mark.parametrize("E,K,N", [(2, 64, 128), (3, 256, 384), (8, 2048, 1024)])
+def test_quantize_weights_bit_exact(E, K, N):
+    rng = np.random.default_rng(E * K)
+    W = wl.bf16_bits(rng.standard_normal((E, K, N)).astype(np.float32) / np.sqrt(K))
+    wq = torch.empty(E, N, K, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(E, N, K // 32, dtype=torch.uint8, device=DEV)
+    L.moe_mxfp8_quantize_weights(bf16_tensor(W, DEV), wq, ws)
+    gq, gs = u8(wq), u8(ws)
+    for e in range(E):
+        qr, sr = om.quantize_blocks(W[e], axis=0)           # blocks along K for every column
+        assert np.array_equal(gs[e], sr.T), e
+        assert np.array_equal(gq[e], qr.T), e
+
+
+@pytest.mark.parametrize("T,d,k", [(5, 32, 1), (300, 2048, 4), (77, 96, 2)])
+def test_dispatch_mxfp8_bit_exact(T, d, k):
+    E = 8
+    rng = np.random.default_rng(T + d)
+    x = _edge_values(rng, T, d) if T >= 5 else wl.bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    _, _, ros, _ = ol.route_map(idx, E)
+    xq = torch.empty(T * k, d, dtype=torch.uint8, device=DEV)
+    xs = torch.empty(T * k, d // 32, dtype=torch.uint8, device=DEV)
+    xp = torch.empty(T * k, d, dtype=torch.bfloat16, device=DEV)
+    L.moe_dispatch_rows_mxfp8(bf16_tensor(x, DEV), torch.from_numpy(ros).to(DEV), k, xq, xs, xp)
+    qr, sr = om.quantize_blocks(x, axis=1)
+    slots = np.arange(T * k)
+    assert np.array_equal(u8(xq)[ros[slots]], qr[slots // k])
+    assert np.array_equal(u8(xs)[ros[slots]], sr[slots // k])
+    assert np.array_equal(as_f64(xp), ol.dispatch(x, ros, k))
+
+
+def _mx_layer(w, inp):
+    """Device MXFP8 forward of workload w: weight quantisation, route map,
+    quantising dispatch, block-scaled grouped GEMMs."""
+    T, d, E, k, h = w.T, w.d, w.E, w.k, w.h
+    R = T * k
+    dev = DEV
+    t = {}
+    for n in ("W1", "W3", "W2"):
+        t[n] = bf16_tensor(inp[n], dev)
+    u = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)  # noqa: E731
+    b = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    t["w1q"], t["w1s"] = u(E, h, d), u(E, h, d // 32)
+    t["w3q"], t["w3s"] = u(E, h, d), u(E, h, d // 32)
+    t["w2q"], t["w2s"] = u(E, d, h), u(E, d, h // 32)
+    L.moe_mxfp8_quantize_weights(t["W1"], t["w1q"], t["w1s"])
+    L.moe_mxfp8_quantize_weights(t["W3"], t["w3q"], t["w3s"])
+    L.moe_mxfp8_quantize_weights(t["W2"], t["w2q"], t["w2s"])
+    idx = torch.from_numpy(np.ascontiguousarray(inp["idx"])).to(dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ros = torch.empty(R, dtype=torch.int32, device=dev)
+    sor = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = torch.zeros(L.moe_workspace_size(T, E, k, d, h), dtype=torch.uint8, device=dev)
+    L.moe_expert_offsets(idx, E, counts, offs, ros, sor, ws)
+    t["xq"], t["xs"], t["xp"] = u(R, d), u(R, d // 32), b(R, d)
+    L.moe_dispatch_rows_mxfp8(bf16_tensor(inp["x"], dev), ros, k, t["xq"], t["xs"], t["xp"])
+    t["h1"], t["h3"], t["a"], t["yp"] = b(R, h), b(R, h), b(R, h), b(R, d)
+    t["aq"], t["as"] = u(R, h), u(R, h // 32)
+    L.moe_reset_status(ws)
+    L.moe_grouped_swiglu_fwd_mxfp8(t["xq"], t["xs"], offs, t["w1q"], t["w1s"], t["w3q"], t["w3s"],
+                                   t["w2q"], t["w2s"], t["h1"], t["h3"], t["a"], t["aq"], t["as"],
+                                   t["yp"], ws)
+    torch.cuda.synchronize()
+    assert L.moe_get_status(ws) == 0
+    t["offsets"] = offs
+    t["ros"] = ros
+    return t
+
+
+@pytest.mark.parametrize("T,d,E,k,h,empty", [
+    (300, 256, 6, 2, 384, (2,)),       # ragged rows, three 128-column blocks of h
+    (1000, 512, 16, 4, 256, (0, 15)),
+    (64, 128, 1, 1, 128, ()),
+])
+def test_grouped_forward_mxfp8_small(T, d, E, k, h, empty):
+    w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
+    inp = wl.generate(w, seed=2, with_backward=False)
+    if empty:
+        keep = [e for e in range(E) if e not in empty]
+        rng = np.random.default_rng(3)
+        inp["idx"] = np.stack([rng.permutation(keep)[:k] for _ in range(T)]).astype(np.int32)
+    t = _mx_layer(w, inp)
+    c, off, ros, _ = ol.route_map(inp["idx"], E)
+    Xp = ol.dispatch(inp["x"], ros, k)
+    ref = om.expert_ffn_forward_mxfp8(Xp, off, inp["W1"], inp["W3"], inp["W2"])
+    assert_close(t["h1"], ref["H1"], "h1")
+    assert_close(t["h3"], ref["H3"], "h3")
+    assert_close(t["a"], ref["A"], "a")
+    # device-quantised a, dequantised, against the exact a it came from
+    aq_dq = om.dequantize_blocks(u8(t["aq"]), u8(t["as"]), axis=1)
+    assert_close(aq_dq, ref["A"], "a quantised", rel_l2=MX_REL_L2, max_abs=0.1)
+    assert_close(t["yp"], ref["Yp"], "yp", rel_l2=MX_REL_L2, max_abs=0.1)
+    exact = ol.expert_ffn_forward(Xp, off, inp["W1"], inp["W3"], inp["W2"])["Yp"]
+    rel = np.linalg.norm(as_f64(t["yp"]) - exact) / np.linalg.norm(exact)
+    assert rel < 0.12                       # E4M3 precision against the unquantised layer
+    for e in empty:
+        assert c[e] == 0
+
+
+def test_full_size_mxfp8_sampled():
+    w = wl.get_workload("train_e128")
+    inp = wl.generate(w, seed=0, with_backward=False)
+    t = _mx_layer(w, inp)
+    k = w.k
+    c, off, ros, sor = ol.route_map(inp["idx"], w.E)
+    assert np.array_equal(t["offsets"].cpu().numpy(), off)
+    rng = np.random.default_rng(11)
+    toks = np.sort(rng.choice(w.T, 12, replace=False))
+    rows, yref, href = [], [], []
+    x = inp["x"]
+    for tk in toks:
+        for j in range(k):
+            e = int(inp["idx"][tk, j])
+            Xq = om.qdq(ol.decode_bf16(x[tk:tk + 1]), axis=1)
+            w1 = om.qdq(inp["W1"][e], axis=0); w3 = om.qdq(inp["W3"][e], axis=0)
+            w2 = om.qdq(inp["W2"][e], axis=0)
+            H1 = Xq @ w1
+            A = ol.silu(H1) * (Xq @ w3)
+            yref.append((om.qdq(A, axis=1) @ w2)[0]); href.append(H1[0])
+            rows.append(int(ros[tk * k + j]))
+    rt = torch.tensor(rows, device=DEV, dtype=torch.long)
+    assert_close(t["h1"][rt], np.array(href), "h1")
+    assert_close(t["yp"][rt], np.array(yref), "yp", rel_l2=MX_REL_L2, max_abs=0.1)
+
+
+def test_layer_step_mxfp8_forward_bf16_backward():
+    # the layer's MXFP8 step: forward through the block-scaled GEMMs, backward
+    # in bf16 from the forward's stored activations; the oracle composes its
+    # quantise->dequantise forward with the analytic backward at those values
+    from token_dispatch_grouped_router_gb300.layer import MoELayer
+    w = wl.small_workload(T=500, d=256, E=8, k=2, h=256)
+    inp = wl.generate(w, seed=5)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=False, device=DEV)
+    layer.load_inputs(inp)
+    layer.enable_mxfp8()
+    L.moe_reset_status(layer.ws)
+    layer.step_mxfp8()
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    k, E = w.k, w.E
+    g = ol.softmax_gates(inp["glogit"])
+    _, off, ros, _ = ol.route_map(inp["idx"], E)
+    Xp = ol.dispatch(inp["x"], ros, k)
+    f = om.expert_ffn_forward_mxfp8(Xp, off, inp["W1"], inp["W3"], inp["W2"])
+    assert_close(layer.out, ol.combine(f["Yp"], ros, g, k), "out", rel_l2=MX_REL_L2, max_abs=0.1)
+    dYp, dg = ol.combine_backward(inp["dY"], f["Yp"], ros, g, k)
+    b = ol.expert_ffn_backward(Xp, off, inp["W1"], inp["W3"], inp["W2"], f["H1"], f["H3"], f["A"], dYp)
+    for n, key in (("dxp", "dXp"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2")):
+        assert_close(getattr(layer, n), b[key], n, rel_l2=MX_REL_L2, max_abs=0.1)
+    assert_close(layer.dgate, dg, "dgate", rel_l2=MX_REL_L2, max_abs=0.1)

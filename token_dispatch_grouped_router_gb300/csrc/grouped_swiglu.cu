@@ -32,15 +32,13 @@
 // other one.  Every mbarrier wait is bounded: on timeout the kernel records
 // MOE_DEV_WAIT_TIMEOUT, waits (bounded) for its own in-flight copies and
 // MMAs, frees TMEM and returns.
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
-#include "sm103_ptx.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace {
 
 using namespace ptx;
+using namespace gemm;
 
 enum Mode : int { kUp = 0, kDown = 1, kDA = 2, kDX = 3, kWG = 4 };
 
@@ -48,16 +46,7 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;            // 16 KB
 constexpr int B_STAGE = BN * BK * 2;            // 32 KB
 constexpr int SUB = 64 * 64 * 2;                // one 64x64 bf16 TMA box (8 KB)
-constexpr int kEpiWarps = 8;                    // two per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue
 constexpr int kTmemCols = 512;
-// per-epilogue-warp staging buffer: a 32-row x 32-column bf16 chunk with an
-// 80-byte row pitch, so both the row-per-thread side and the coalesced side
-// of the transpose are free of bank conflicts
-constexpr int kStagePitch = 80;
-constexpr int kStageBytes = 32 * kStagePitch;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s; a step takes milliseconds
-
 struct GemmArgs {
   const int32_t* offsets;   // [E+1], device
   int E, R, d, h;
@@ -79,36 +68,7 @@ struct Tile {
   int e, row0, rows, m0, n0, nkb, which, krow0, krows;
 };
 
-struct Shared {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  int total_tiles;
-};
-
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, Shared* sh, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 127u) == 0) {
-      if (*(volatile int*)&sh->abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *(volatile int*)&sh->abort_flag = 1;
-        set_status(status, MOE_DEV_WAIT_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// wait used only while draining after an abort: bounded, reports nothing
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return;
-  }
-}
+using Shared = PipeShared<STAGES>;
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int* s_off,
@@ -131,22 +91,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int*
     tl.krows = hi - lo;
     tl.nkb = (tl.krows + BK - 1) / BK;
   } else {
-    // expert e owns tiles [s_ts[e], s_ts[e+1]): largest e with s_ts[e] <= t
-    int lo = 0, hi = a.E;               // invariant: s_ts[lo] <= t < s_ts[hi]
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (s_ts[mid] <= t) lo = mid; else hi = mid;
-    }
-    tl.e = lo;
-    int seg0 = max(0, min(s_off[lo], a.R));
-    int seg1 = max(seg0, min(s_off[lo + 1], a.R));
-    int ne = seg1 - seg0;
-    int mt = (ne + BM - 1) / BM;
-    int l = t - s_ts[lo];
-    int m_idx = l % mt, n_idx = l / mt;
-    tl.row0 = seg0 + m_idx * BM;
-    tl.rows = min(BM, seg1 - tl.row0);
-    tl.n0 = n_idx * (MODE == kUp ? BN / 2 : BN);
+    const RowTile r = decode_row_tile(t, a.E, a.R, s_off, s_ts);
+    tl.e = r.e;
+    tl.row0 = r.row0;
+    tl.rows = r.rows;
+    tl.n0 = r.n_idx * (MODE == kUp ? BN / 2 : BN);
     tl.nkb = a.kb_total;
   }
   return tl;
@@ -185,70 +134,6 @@ __device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa,
 #pragma unroll
     for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * SUB, bm, bar, tl.n0 + 64 * c, y);
   }
-}
-
-// sigmoid through the identity sigmoid(x) = (1 + tanh(x / 2)) / 2 on the
-// hardware tanh approximation (one MUFU op instead of an exp and a divide);
-// its error is far below the bf16 rounding of the stored results
-__device__ __forceinline__ float tanh_hw(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float sigmoid_f(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
-__device__ __forceinline__ float silu_f(float x) { return x * sigmoid_f(x); }
-
-__device__ __forceinline__ void pack_row32(const float* v, uint4 (&o)[4]) {
-  uint32_t* w = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-}
-
-// The warp's 32 rows (one per lane, 32 values each) -> global memory at
-// g[row * ld + 0..31] for rows < nrows, through the staging buffer so that each
-// store instruction writes 8 rows x 64 contiguous bytes.
-__device__ __forceinline__ void store_chunk(uint8_t* stg, const float* v, int lane, uint16_t* g,
-                                            size_t ld, int nrows) {
-  uint4 o[4];
-  pack_row32(v, o);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stg + lane * kStagePitch + 16 * i) = o[i];
-  __syncwarp();
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int p = it * 32 + lane, row = p >> 2, c = p & 3;
-    if (row < nrows)
-      st_v4(g + (size_t)row * ld + 8 * c, *reinterpret_cast<const uint4*>(stg + row * kStagePitch + 16 * c));
-  }
-  __syncwarp();
-}
-
-// Coalesced load of a 32-row x 32-column bf16 chunk (8 rows x 64 bytes per
-// instruction); piece it*32+lane holds row (it*32+lane)/4, 16-byte column (..)%4.
-__device__ __forceinline__ void load_chunk(uint4 (&q)[4], const uint16_t* g, size_t ld, int lane,
-                                           int nrows) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int p = it * 32 + lane, row = p >> 2, c = p & 3;
-    q[it] = row < nrows ? ld_nc_v4(g + (size_t)row * ld + 8 * c) : make_uint4(0, 0, 0, 0);
-  }
-}
-
-// Pieces from load_chunk -> this lane's own row (32 bf16 values, packed in pairs).
-__device__ __forceinline__ void chunk_to_row(const uint4 (&q)[4], uint8_t* stg, int lane,
-                                             uint32_t (&w)[16]) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int p = it * 32 + lane, row = p >> 2, c = p & 3;
-    *reinterpret_cast<uint4*>(stg + row * kStagePitch + 16 * c) = q[it];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 t = *reinterpret_cast<const uint4*>(stg + lane * kStagePitch + 16 * i);
-    w[4 * i + 0] = t.x; w[4 * i + 1] = t.y; w[4 * i + 2] = t.z; w[4 * i + 3] = t.w;
-  }
-  __syncwarp();
 }
 
 // Epilogue of one tile for the 32 rows of this warp's TMEM lane quarter and
@@ -397,25 +282,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     if (threadIdx.x == 0) sh->total_tiles = args.E * (2 * args.wg_t1 + args.wg_t2);
   } else {
     if (warp == 0) {
-      int carry = 0;
-      for (int base = 0; base < args.E; base += 32) {
-        const int e = base + lane;
-        int cnt = 0;
-        if (e < args.E) {
-          int lo = max(0, min(s_off[e], args.R));
-          int hi = max(lo, min(s_off[e + 1], args.R));
-          cnt = ((hi - lo + BM - 1) / BM) * args.n_tiles;
-        }
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        if (e < args.E) s_ts[e] = carry + incl - cnt;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) { s_ts[args.E] = carry; sh->total_tiles = carry; }
+      const int n = build_row_tile_table(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
+      if (lane == 0) sh->total_tiles = n;
     }
   }
   __syncthreads();
@@ -444,7 +312,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
       for (int kb = 0; kb < tl.nkb; ++kb) {
-        if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, sh, args.status)) { ok = false; break; }
+        if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t fb = smem_u32(&sh->full[stage]);
           mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
@@ -473,14 +341,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     bool ok = true, issued_any = false;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
-      if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, sh, args.status)) { ok = false; break; }
+      if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t dt = tmem + (uint32_t)(acc * BN);
       if (tl.nkb == 0) {
         if (lane == 0) mbar_arrive(smem_u32(&sh->tfull[acc]));
       } else {
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, sh, args.status)) { ok = false; break; }
+          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(sA + stage * A_STAGE);
           const uint32_t sb = smem_u32(sB + stage * B_STAGE);
@@ -545,7 +413,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
-      if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, sh, args.status)) break;
+      if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
       epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * BN), lane_q, half, lane,
                           sStage + (warp - 2) * kStageBytes, args);
@@ -566,49 +434,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    else
-      (void)cudaGetLastError();
-  }
-  return fn;
-}
-
-// 2-D bf16 map over a row-major [outer, inner] tensor, box [box_outer, box_inner]
-bool map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-           uint32_t box_outer) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D bf16 map over a row-major [outer, mid, inner] tensor, box [1, box_mid, box_inner]
-bool map3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t mid, uint64_t outer,
-           uint32_t box_inner, uint32_t box_mid) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {inner, mid, outer};
-  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
-  cuuint32_t box[3] = {box_inner, box_mid, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr size_t smem_bytes(int E) {
   return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)kEpiWarps * kStageBytes +
          sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
@@ -620,19 +445,9 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
            cudaStream_t s) {
   const size_t smem = smem_bytes(args.E);
   auto kern = grouped_gemm_kernel<MODE>;
-  // the attribute is set once per device for the largest size (E = 1024), so
-  // no non-stream CUDA call happens on later (possibly graph-captured) calls
-  static bool attr_set[64] = {false};
-  const int dev = current_device();
-  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes(kMaxExperts)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
-    attr_set[dev] = true;
-  }
+  static bool attr_done[64] = {false};
+  // set once per device for the largest size (E = 1024)
+  if (ensure_smem_attr(kern, smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
   kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, b2, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
@@ -644,13 +459,6 @@ int check_common(const void* ws, size_t ws_bytes, int R, int E, int d, int h) {
   if (ws == nullptr || ws_bytes < kStatusBytes) return MOE_ERR_WORKSPACE;
   if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
-}
-
-int row_grid_upper(int R, int E, int n_tiles) {
-  // tiles <= (ceil(R/BM) + E) * n_tiles; CTAs beyond the real count exit at once
-  long long ub = ((long long)(R + BM - 1) / BM + E) * n_tiles;
-  long long g = sm_count();
-  return (int)(ub < g ? (ub > 0 ? ub : 1) : g);
 }
 
 }  // namespace

@@ -161,6 +161,51 @@ class MoELayer:
             L.moe_router_logits_bwd(self.x, self.W_r, self.dlogits, self.dX, self.dW_r,
                                     self.db, self.ws)
 
+    # ------------------------------------------------------------- MXFP8
+    def enable_mxfp8(self) -> None:
+        """Allocate the MXFP8 buffers: K-major E4M3 weight copies with their
+        E8M0 scales, quantised expert rows and quantised activations."""
+        E, d, h, R = self.E, self.d, self.h, self.R
+        dev = self.x.device
+        u = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)  # noqa: E731
+        self.w1q, self.w1s = u(E, h, d), u(E, h, d // 32)
+        self.w3q, self.w3s = u(E, h, d), u(E, h, d // 32)
+        self.w2q, self.w2s = u(E, d, h), u(E, d, h // 32)
+        self.xq, self.xs = u(R, d), u(R, d // 32)
+        self.aq, self.as_ = u(R, h), u(R, h // 32)
+
+    def quantize_weights(self, mark=None) -> None:
+        """Re-make the MXFP8 weight copies (once per optimizer step)."""
+        mark = mark or _nomark
+        mark("mx_quantize_weights")
+        L.moe_mxfp8_quantize_weights(self.W1, self.w1q, self.w1s)
+        L.moe_mxfp8_quantize_weights(self.W3, self.w3q, self.w3s)
+        L.moe_mxfp8_quantize_weights(self.W2, self.w2q, self.w2s)
+
+    def forward_mxfp8(self, mark=None) -> torch.Tensor:
+        """Forward with MXFP8 GEMM operands; h1, h3, a and xp are also kept in
+        bf16 so that the backward (bf16) can follow unchanged."""
+        mark = mark or _nomark
+        self.route(mark)
+        mark("dispatch_mxfp8")
+        L.moe_dispatch_rows_mxfp8(self.x, self.row_of_slot, self.k, self.xq, self.xs, self.xp)
+        mark("gemm_fwd_mxfp8")
+        L.moe_grouped_swiglu_fwd_mxfp8(self.xq, self.xs, self.offsets, self.w1q, self.w1s,
+                                       self.w3q, self.w3s, self.w2q, self.w2s, self.h1, self.h3,
+                                       self.a, self.aq, self.as_, self.yp, self.ws)
+        mark("combine")
+        L.moe_combine(self.yp, self.row_of_slot, self.gate, self.k, self.out)
+        return self.out
+
+    def step_mxfp8(self, mark=None, requantize: bool = True) -> None:
+        if requantize:
+            self.quantize_weights(mark)
+        self.forward_mxfp8(mark)
+        if self.with_backward:
+            self.backward(mark)
+        if mark is not None:
+            mark("end")
+
     def step(self, mark=None) -> None:
         self.forward(mark)
         if self.with_backward:

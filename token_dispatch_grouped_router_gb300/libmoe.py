@@ -42,6 +42,11 @@ SIGNATURES = {
                                     _Z, _P]),
     "moe_grouped_swiglu_bwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
+    "moe_mxfp8_quantize_weights": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_dispatch_rows_mxfp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                          _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_grouped_swiglu_fwd_up": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_grouped_swiglu_fwd_down": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_grouped_swiglu_bwd_dact": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
@@ -309,3 +314,51 @@ def moe_grouped_swiglu_bwd_wgrad(xp, offsets, a, dyp, dh1, dh3, dW1, dW3, dW2, w
     _ok("moe_grouped_swiglu_bwd_wgrad", load().moe_grouped_swiglu_bwd_wgrad(
         _ptr(xp), _ptr(offsets), R, E, d, h, _ptr(a), _ptr(dyp), _ptr(dh1), _ptr(dh3),
         _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+# ------------------------------------------------------------------ MXFP8
+
+def moe_mxfp8_quantize_rows(src, q, scale) -> None:
+    rows, K = src.shape
+    _want(src, torch.bfloat16, (rows, K), "src"); _want(q, torch.uint8, (rows, K), "q")
+    _want(scale, torch.uint8, (rows, K // 32), "scale")
+    _ok("moe_mxfp8_quantize_rows", load().moe_mxfp8_quantize_rows(
+        _ptr(src), rows, K, _ptr(q), _ptr(scale), _stream()))
+
+
+def moe_mxfp8_quantize_weights(W, wq, ws) -> None:
+    E, K, N = W.shape
+    _want(W, torch.bfloat16, (E, K, N), "W"); _want(wq, torch.uint8, (E, N, K), "wq")
+    _want(ws, torch.uint8, (E, N, K // 32), "ws")
+    _ok("moe_mxfp8_quantize_weights", load().moe_mxfp8_quantize_weights(
+        _ptr(W), E, K, N, _ptr(wq), _ptr(ws), _stream()))
+
+
+def moe_dispatch_rows_mxfp8(x, row_of_slot, k: int, xq, xs, xp=None) -> None:
+    T, d = x.shape
+    _want(x, torch.bfloat16, (T, d), "x"); _want(xq, torch.uint8, (T * k, d), "xq")
+    _want(xs, torch.uint8, (T * k, d // 32), "xs")
+    if xp is not None:
+        _want(xp, torch.bfloat16, (T * k, d), "xp")
+    _ok("moe_dispatch_rows_mxfp8", load().moe_dispatch_rows_mxfp8(
+        _ptr(x), T, d, k, _ptr(row_of_slot), _ptr(xq), _ptr(xs), _ptr(xp), _stream()))
+
+
+def moe_grouped_swiglu_fwd_mxfp8(xq, xs, offsets, w1q, w1s, w3q, w3s, w2q, w2s,
+                                 h1, h3, a, aq, as_, yp, ws) -> None:
+    R, d = xq.shape
+    E, h, _ = w1q.shape
+    _want(xs, torch.uint8, (R, d // 32), "xs")
+    for n, t in (("w1q", w1q), ("w3q", w3q)):
+        _want(t, torch.uint8, (E, h, d), n)
+    for n, t in (("w1s", w1s), ("w3s", w3s)):
+        _want(t, torch.uint8, (E, h, d // 32), n)
+    _want(w2q, torch.uint8, (E, d, h), "w2q"); _want(w2s, torch.uint8, (E, d, h // 32), "w2s")
+    for n, t in (("h1", h1), ("h3", h3), ("a", a)):
+        _want(t, torch.bfloat16, (R, h), n)
+    _want(aq, torch.uint8, (R, h), "aq"); _want(as_, torch.uint8, (R, h // 32), "as")
+    _want(yp, torch.bfloat16, (R, d), "yp")
+    _ok("moe_grouped_swiglu_fwd_mxfp8", load().moe_grouped_swiglu_fwd_mxfp8(
+        _ptr(xq), _ptr(xs), _ptr(offsets), R, E, d, h, _ptr(w1q), _ptr(w1s), _ptr(w3q),
+        _ptr(w3s), _ptr(w2q), _ptr(w2s), _ptr(h1), _ptr(h3), _ptr(a), _ptr(aq), _ptr(as_),
+        _ptr(yp), _ptr(ws), _wsb(ws), _stream()))
