@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--workload", default="dense_e8")
     ap.add_argument("--compare", default="pool_e128",
                     help="second workload timed the same way (expert-count flatness); '' to skip")
+    ap.add_argument("--mxfp8-workload", default="train_e128",
+                    help="workload of the BF16 vs MXFP8-forward comparison; '' to skip")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -221,14 +223,23 @@ def run_ours(args):
         if dist:
             dist.barrier()
 
-    def timed(w, inp, K, W, with_e2e, sample_clocks=True):
+    def make_layer(w, inp, mxfp8=False):
         layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=(w.routing == "learned"), device=dev)
         layer.load_inputs(inp)
+        if mxfp8:
+            layer.enable_mxfp8()
+            layer.quantize_weights()
+        return layer
+
+    def timed_layer(layer, K, W, step=None, sample_clocks=False):
+        """W warm-up steps, then K timed steps with an L2 flush between them
+        and a CUDA event before every library call of every timed step."""
+        step = step or layer.step
         sampler = ClockSampler(device_uuid(dev)) if (rank == 0 and sample_clocks) else None
         if sampler:
             sampler.start()                  # running before the warm-up steps
         for _ in range(W):
-            layer.step()
+            step()
         torch.cuda.synchronize()
         L.moe_reset_status(layer.ws)
         # ---------------------------------------------------------- timed region
@@ -248,7 +259,7 @@ def run_ours(args):
         for _ in range(K):
             flush.zero_()                    # L2 flush, outside the step's events
             lst = []
-            layer.step(new_mark(lst))
+            step(new_mark(lst))
             events.append(lst)
         torch.cuda.synchronize()
         barrier()
@@ -268,9 +279,13 @@ def run_ours(args):
             step_ms.append(lst[0][1].elapsed_time(lst[-1][1]))
             for (lab, ev), (_, nxt) in zip(lst[:-1], lst[1:]):
                 per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
-        res = {"ms_per_step": allmax(statistics.mean(step_ms)),
-               "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
-               "launches": launches, "clocks": clocks, "wall_s": wall}
+        return {"ms_per_step": allmax(statistics.mean(step_ms)),
+                "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
+                "launches": launches, "clocks": clocks, "wall_s": wall}
+
+    def timed(w, inp, K, W, with_e2e, sample_clocks=True):
+        layer = make_layer(w, inp)
+        res = timed_layer(layer, K, W, sample_clocks=sample_clocks)
         if with_e2e:
             res["e2e"] = e2e(layer, inp, K)
         del layer
@@ -322,6 +337,21 @@ def run_ours(args):
         cmp_res = timed(w2, inp2, args.steps, args.warmup, with_e2e=False, sample_clocks=False)
         cmp_res["workload"] = w2.name
         del inp2
+
+    mx_res = None
+    if args.mxfp8_workload:
+        w3 = wl.get_workload(args.mxfp8_workload)
+        inp3 = wl.generate(w3, seed=args.seed + rank)
+        layer = make_layer(w3, inp3, mxfp8=True)
+        del inp3
+        bf = timed_layer(layer, args.steps, args.warmup)
+        mx = timed_layer(layer, args.steps, args.warmup,
+                         step=lambda mark=None: layer.step_mxfp8(mark, requantize=True))
+        mxc = timed_layer(layer, args.steps, args.warmup,
+                          step=lambda mark=None: layer.step_mxfp8(mark, requantize=False))
+        del layer
+        torch.cuda.empty_cache()
+        mx_res = (w3, bf, mx, mxc)
 
     if rank != 0:
         if dist:
@@ -388,6 +418,28 @@ def run_ours(args):
         out["compare"] = {"workload": cmp_res["workload"], "value": cv, "unit": UNIT,
                           "ms_per_step": cmp_res["ms_per_step"], "ratio_to_main": cv / value,
                           "kernels_ms": cmp_res["kernels_ms"], "gpu_launches": cmp_res["launches"]}
+    if mx_res is not None:
+        w3, bf, mx, mxc = mx_res
+        fl, _ = work_per_launch(w3)
+        fwd_flops = fl["gemm_up"] + fl["gemm_down"]
+        bf_fwd = bf["kernels_ms"]["gemm_up"] + bf["kernels_ms"]["gemm_down"]
+        mx_fwd = mx["kernels_ms"]["gemm_fwd_mxfp8"]
+        out["mxfp8"] = {
+            "workload": w3.name,
+            "bf16": {"value": world * w3.T / (bf["ms_per_step"] / 1e3), "ms_per_step": bf["ms_per_step"],
+                     "fwd_gemm_ms": bf_fwd, "fwd_gemm_tflops": fwd_flops / (bf_fwd / 1e3) / 1e12},
+            "mxfp8_fwd": {"value": world * w3.T / (mx["ms_per_step"] / 1e3), "ms_per_step": mx["ms_per_step"],
+                          "fwd_gemm_ms": mx_fwd, "fwd_gemm_tflops": fwd_flops / (mx_fwd / 1e3) / 1e12,
+                          "weight_quantize_ms": mx["kernels_ms"].get("mx_quantize_weights")},
+            "mxfp8_fwd_cached_weights": {
+                "value": world * w3.T / (mxc["ms_per_step"] / 1e3), "ms_per_step": mxc["ms_per_step"],
+                "note": "weights re-quantised once per optimizer step, outside the step"},
+            "step_speedup": bf["ms_per_step"] / mx["ms_per_step"],
+            "step_speedup_cached_weights": bf["ms_per_step"] / mxc["ms_per_step"],
+            "fwd_gemm_speedup": bf_fwd / mx_fwd,
+            "unit": UNIT, "units_note": "fp8 GEMM TFLOP/s compare to a 2x higher tensor peak than bf16",
+            "kernels_ms_mxfp8": mx["kernels_ms"],
+        }
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, args.seed, args.cpu_seconds)
     print(json.dumps(out), flush=True)
