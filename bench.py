@@ -75,6 +75,23 @@ def dist_env():
     return world, rank, local
 
 
+def allmax(v: float, device=None) -> float:
+    """Maximum of v over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens per second: every rank processes its own batch, the
+    step takes the slowest rank's time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -212,13 +229,6 @@ def run_ours(args):
     peaks = measured_peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def allmax(v):
-        if not dist:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     def barrier():
         if dist:
             dist.barrier()
@@ -279,7 +289,7 @@ def run_ours(args):
             step_ms.append(lst[0][1].elapsed_time(lst[-1][1]))
             for (lab, ev), (_, nxt) in zip(lst[:-1], lst[1:]):
                 per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
-        return {"ms_per_step": allmax(statistics.mean(step_ms)),
+        return {"ms_per_step": allmax(statistics.mean(step_ms), dev),
                 "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
                 "launches": launches, "clocks": clocks, "wall_s": wall}
 
@@ -322,18 +332,18 @@ def run_ours(args):
             e.synchronize()
             times.append(s.elapsed_time(e))
         barrier()
-        ms = allmax(statistics.mean(times))
-        return {"value": world * T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+        ms = allmax(statistics.mean(times), dev)
+        return {"value": throughput(T, world, ms), "unit": UNIT, "ms_per_step": ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     w = wl.get_workload(args.workload)
-    inp = wl.generate(w, seed=args.seed + rank)
+    inp = wl.generate(w, seed=args.seed + rank, with_backward=True)
     main = timed(w, inp, args.steps, args.warmup, with_e2e=True)
     del inp
     cmp_res = None
     if args.compare:
         w2 = wl.get_workload(args.compare)
-        inp2 = wl.generate(w2, seed=args.seed + rank)
+        inp2 = wl.generate(w2, seed=args.seed + rank, with_backward=True)
         cmp_res = timed(w2, inp2, args.steps, args.warmup, with_e2e=False, sample_clocks=False)
         cmp_res["workload"] = w2.name
         del inp2
@@ -341,7 +351,7 @@ def run_ours(args):
     mx_res = None
     if args.mxfp8_workload:
         w3 = wl.get_workload(args.mxfp8_workload)
-        inp3 = wl.generate(w3, seed=args.seed + rank)
+        inp3 = wl.generate(w3, seed=args.seed + rank, with_backward=True)
         layer = make_layer(w3, inp3, mxfp8=True)
         del inp3
         bf = timed_layer(layer, args.steps, args.warmup)
@@ -359,7 +369,7 @@ def run_ours(args):
         return
 
     ms = main["ms_per_step"]
-    value = world * w.T / (ms / 1e3)
+    value = throughput(w.T, world, ms)
     km = main["kernels_ms"]
     flops, bytes_ = work_per_launch(w)
     # the dominant kernel: the single-kernel call with the largest share of the step
@@ -479,7 +489,7 @@ def _calibrate(w, inp, seconds):
 
 def cpu_baseline(w, seed, seconds):
     from token_dispatch_grouped_router_gb300 import workloads as wl
-    inp = wl.generate(w, seed=seed)
+    inp = wl.generate(w, seed=seed, with_backward=True)
     Ts = _calibrate(w, inp, seconds)
     dt = _oracle_step(w, inp, Ts)
     return {"value": Ts / dt, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
@@ -494,7 +504,7 @@ def run_reference(args):
         return
     from token_dispatch_grouped_router_gb300 import workloads as wl
     w = wl.get_workload(args.workload)
-    inp = wl.generate(w, seed=args.seed)
+    inp = wl.generate(w, seed=args.seed, with_backward=True)
     per_step = args.ref_seconds / max(1, args.steps + args.warmup)   # a few minutes in total
     Ts = _calibrate(w, inp, per_step)
     for _ in range(args.warmup):
