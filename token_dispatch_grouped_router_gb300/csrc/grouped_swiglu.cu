@@ -47,6 +47,9 @@ constexpr int A_STAGE = BM * BK * 2;            // 16 KB
 constexpr int B_STAGE = BN * BK * 2;            // 32 KB
 constexpr int SUB = 64 * 64 * 2;                // one 64x64 bf16 TMA box (8 KB)
 constexpr int kTmemCols = 512;
+// warps: 0 TMA producer, 1 MMA issuer, 2-9 epilogue, 10 ragged-tail fixup (wgrad)
+constexpr int kFixWarp = 2 + kEpiWarps;
+constexpr int kThreadsBF = 32 * (kFixWarp + 1);
 struct GemmArgs {
   const int32_t* offsets;   // [E+1], device
   int E, R, d, h;
@@ -99,6 +102,19 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int*
     tl.nkb = a.kb_total;
   }
   return tl;
+}
+
+// wgrad only: the last k-block of an expert whose row count is not a multiple
+// of 64 holds rows of the next expert.  MMAs run over ceil(valid/16) 16-row
+// groups; rows [zlo, zhi) of the last group must be cleared first.  Returns
+// the number of MMAs for this k-block.
+__device__ __forceinline__ int wg_tail(const Tile& tl, int kb, int& zlo, int& zhi) {
+  const int valid = tl.krows - kb * BK;
+  if (valid >= BK) { zlo = zhi = 0; return BK / 16; }
+  const int nkk = (valid + 15) >> 4;
+  zlo = valid;
+  zhi = nkk * 16;
+  return nkk;
 }
 
 template <int MODE>
@@ -252,7 +268,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsBF, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
@@ -268,10 +284,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- set-up: tile table from the device offsets, barriers, TMEM
-  for (int i = threadIdx.x; i <= args.E; i += kThreads) s_off[i] = __ldg(args.offsets + i);
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) { mbar_init(smem_u32(&sh->full[s]), 1); mbar_init(smem_u32(&sh->empty[s]), 1); }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+      mbar_init(smem_u32(&sh->fixed[s]), 1);
+    }
     for (int s = 0; s < 2; ++s) { mbar_init(smem_u32(&sh->tfull[s]), 1); mbar_init(smem_u32(&sh->tempty[s]), kEpiWarps); }
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
@@ -337,7 +357,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kWG);
     constexpr uint32_t idesc = idesc_bf16(BM, BN, a_mn, b_mn);
     int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0;
+    uint32_t phase = 0, acc_phase = 0, fix_par = 0;
     bool ok = true, issued_any = false;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
@@ -348,37 +368,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         if (lane == 0) mbar_arrive(smem_u32(&sh->tfull[acc]));
       } else {
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+          int nkk = BK / 16, zlo = 0, zhi = 0;
+          if constexpr (MODE == kWG) nkk = wg_tail(tl, kb, zlo, zhi);
+          if (zhi > zlo) {
+            // the fixup warp clears the foreign rows of this stage, then releases it
+            if (!bounded_wait(smem_u32(&sh->fixed[stage]), (fix_par >> stage) & 1u, &sh->abort_flag,
+                              args.status)) { ok = false; break; }
+            fix_par ^= 1u << stage;
+          } else if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sa = smem_u32(sA + stage * A_STAGE);
           const uint32_t sb = smem_u32(sB + stage * B_STAGE);
-          int nkk = BK / 16;
-          if constexpr (MODE == kWG) {
-            // last block of a ragged reduction: rows past the expert's end
-            // belong to the next expert (or were zero-filled).  Skip the
-            // 16-row groups that hold none of this expert's rows and clear the
-            // foreign rows of the one partial group in both operands.
-            const int valid = tl.krows - kb * BK;
-            if (valid < BK) {
-              nkk = (valid + 15) >> 4;
-              const int zlo = valid, zhi = nkk * 16;
-              if (zhi > zlo) {
-                // lane -> (row offset lane/8, 16-byte chunk lane%8) of each
-                // 128-byte row, rows zlo.. in steps of 4, all six 64x64 sub-tiles
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                const int chunk = lane & 7;
-#pragma unroll
-                for (int sub = 0; sub < 6; ++sub) {
-                  uint8_t* base = sub < 2 ? (sA + stage * A_STAGE + sub * SUB)
-                                          : (sB + stage * B_STAGE + (sub - 2) * SUB);
-                  for (int row = zlo + (lane >> 3); row < zhi; row += 4)
-                    *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = z;
-                }
-                fence_proxy_async_smem();
-              }
-            }
-            __syncwarp();
-          }
           if (lane == 0) {
             for (int kk = 0; kk < nkk; ++kk) {
               uint64_t ad, bd;
@@ -405,7 +408,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
       mma_commit(smem_u32(&sh->drain));
       drain_wait(smem_u32(&sh->drain), 0);
     }
-  } else {
+  } else if (warp < kFixWarp) {
     // --------------------------------------------------------------- epilogue
     const int lane_q = warp & 3;          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;     // which half of the tile's columns
@@ -421,6 +424,43 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  } else if constexpr (MODE == kWG) {
+    // ------------------------------------------------------- ragged-tail fixup
+    // Walks the same k-block sequence as the MMA issuer, waiting for each
+    // stage's data.  For the last block of an expert whose rows end inside a
+    // 16-row group, it zeroes the foreign rows [zlo, zhi) of all six 64x64
+    // sub-tiles (a whole 128-byte row each, so the swizzle does not matter),
+    // publishes the writes to the async proxy and releases the stage.
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
+      bool ok = true;
+      for (int kb = 0; kb < tl.nkb; ++kb) {
+        int zlo, zhi;
+        wg_tail(tl, kb, zlo, zhi);
+        // observe every stage's data in order, so this warp is never more than
+        // one phase ahead on a barrier (a parity wait could otherwise see an
+        // older phase of the same parity as complete)
+        if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+        if (zhi > zlo) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          const int chunk = lane & 7;
+#pragma unroll
+          for (int sub = 0; sub < 6; ++sub) {
+            uint8_t* base = sub < 2 ? (sA + stage * A_STAGE + sub * SUB)
+                                    : (sB + stage * B_STAGE + (sub - 2) * SUB);
+            for (int row = zlo + (lane >> 3); row < zhi; row += 4)
+              *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = z;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh->fixed[stage]));
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
     }
   }
 
@@ -448,7 +488,7 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
   static bool attr_done[64] = {false};
   // set once per device for the largest size (E = 1024)
   if (ensure_smem_attr(kern, smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, b2, args);
+  kern<<<grid, kThreadsBF, smem, s>>>(a0, a1, b0, b1, b2, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
