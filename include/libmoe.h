@@ -81,7 +81,8 @@ uint64_t moe_launch_count(void);
 
 /* Bytes of workspace needed by moe_expert_offsets, moe_grouped_swiglu_fwd/bwd
  * and moe_router_logits_bwd for these sizes.  The first 256 bytes hold the
- * device status word; the rest is route-map and reduction scratch.  The
+ * device status word; the rest is route-map and reduction scratch and the
+ * weight-gradient phase's per-expert TMA descriptors.  The
  * workspace must be zeroed once (or reset with moe_reset_status) before its
  * status word is meaningful. */
 size_t moe_workspace_size(int T, int E, int k, int d, int h);
@@ -218,7 +219,11 @@ int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets,
  * The weight gradients reduce over each expert's own row count (zero rows
  * give exactly zero).  dh1/dh3[R,h] are caller-provided intermediates (also
  * outputs).  dW1/dW3[E,d,h], dW2[E,h,d] bf16 from fp32 accumulators, no
- * split-K, deterministic. */
+ * split-K, deterministic.  The weight-gradient phase keeps five TMA
+ * descriptors per expert in ws (bytes [256, 256 + 640 E)), written on the
+ * device from offsets: for R > 0 ws must be 128-byte aligned
+ * (MOE_ERR_INVALID_ARG) and ws_bytes >= moe_workspace_size(...)
+ * (MOE_ERR_WORKSPACE). */
 int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets,
                            int R, int E, int d, int h,
                            const moe_bf16_t* W1, const moe_bf16_t* W3,

@@ -93,3 +93,17 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             LM.load(str(tmp_path / "missing.so"))
     finally:
         LM._lib = saved
+
+
+def test_wgrad_workspace_holds_the_per_expert_descriptors(lib):
+    # five 128-byte TMA descriptors per expert after the 256-byte status word
+    for E in (1, 8, 128, 1024):
+        assert lib.moe_workspace_size(16, E, 1, 64, 64) >= 256 + 640 * E
+    fake = ctypes.c_void_p(0x1000)
+    args = lambda ws, n: (fake, fake, 64, 128, 128, 128, fake, fake, fake, fake, fake, fake,
+                          fake, ws, n, None)
+    need = lib.moe_workspace_size(16, 128, 4, 128, 128)
+    # too small for 128 experts' descriptors (but larger than the status word)
+    assert lib.moe_grouped_swiglu_bwd_wgrad(*args(fake, 256 + 640 * 127)) == -3
+    # descriptors must sit on 128-byte boundaries
+    assert lib.moe_grouped_swiglu_bwd_wgrad(*args(ctypes.c_void_p(0x1010), need)) == -1

@@ -38,7 +38,9 @@ constexpr int kMaxTopK = 8;
 //              only while its own kernels run, so the regions may overlap:
 //              moe_expert_offsets: per-chunk histograms [chunks][E] int32,
 //                                  then in-chunk stable ranks [R] int32;
-//              moe_router_logits_bwd: dW_r split-K partials [splits][d][E] f32.
+//              moe_router_logits_bwd: dW_r split-K partials [splits][d][E] f32;
+//              moe_grouped_swiglu_bwd(_wgrad): per-expert TMA descriptors
+//                                  [E][5] x 128 B (needs a 128-byte aligned ws).
 constexpr size_t kStatusBytes = 256;
 constexpr int kRouteChunk = 1024;     // slots per route-map block
 constexpr int kRouterSplits = 16;     // deterministic split-K for dW_r
@@ -60,10 +62,15 @@ inline size_t router_scratch_end(int E, int d) {
   return round_up(kStatusBytes + (size_t)kRouterSplits * d * E * 4, 256);
 }
 
+constexpr int kWgradMaps = 5;          // xp, a, dh1, dh3, dyp
+inline size_t wgrad_maps_end(int E) { return kStatusBytes + (size_t)E * kWgradMaps * 128; }
+
 inline size_t workspace_bytes(long long T, int E, int k, int d) {
   size_t a = route_scratch(T * (long long)k, E).end;
   size_t b = router_scratch_end(E, d);
-  return a > b ? a : b;
+  size_t c = wgrad_maps_end(E);
+  a = a > b ? a : b;
+  return a > c ? a : c;
 }
 
 // -------------------------------------------------------------- device side

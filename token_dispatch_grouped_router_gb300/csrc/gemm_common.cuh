@@ -28,7 +28,6 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s; a step takes millisec
 template <int STAGES>
 struct PipeShared {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
-  uint64_t fixed[STAGES];     // stage data repaired by a helper warp (optional use)
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;

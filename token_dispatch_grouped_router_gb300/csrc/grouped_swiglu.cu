@@ -47,9 +47,6 @@ constexpr int A_STAGE = BM * BK * 2;            // 16 KB
 constexpr int B_STAGE = BN * BK * 2;            // 32 KB
 constexpr int SUB = 64 * 64 * 2;                // one 64x64 bf16 TMA box (8 KB)
 constexpr int kTmemCols = 512;
-// warps: 0 TMA producer, 1 MMA issuer, 2-9 epilogue, 10 ragged-tail fixup (wgrad)
-constexpr int kFixWarp = 2 + kEpiWarps;
-constexpr int kThreadsBF = 32 * (kFixWarp + 1);
 struct GemmArgs {
   const int32_t* offsets;   // [E+1], device
   int E, R, d, h;
@@ -65,6 +62,8 @@ struct GemmArgs {
   int* status;
   int wg_t1, wg_t2;         // WG: tiles per expert of dW1 (= dW3) and of dW2
   int wg_mt1, wg_mt2;       // WG: M tiles of dW1 (d/128) and dW2 (h/128)
+  const CUtensorMap* wg_maps;  // WG: [E][5] descriptors of xp, a, dh1, dh3, dyp
+                               //     whose row extent ends at the expert's last row
 };
 
 struct Tile {
@@ -104,17 +103,12 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int*
   return tl;
 }
 
-// wgrad only: the last k-block of an expert whose row count is not a multiple
-// of 64 holds rows of the next expert.  MMAs run over ceil(valid/16) 16-row
-// groups; rows [zlo, zhi) of the last group must be cleared first.  Returns
-// the number of MMAs for this k-block.
-__device__ __forceinline__ int wg_tail(const Tile& tl, int kb, int& zlo, int& zhi) {
+// wgrad only: MMAs for k-block kb of an expert, one per 16-row group that
+// holds any of its rows.  The expert's own descriptors end at its last row,
+// so TMA fills the rest of the last block with zeros.
+__device__ __forceinline__ int wg_groups(const Tile& tl, int kb) {
   const int valid = tl.krows - kb * BK;
-  if (valid >= BK) { zlo = zhi = 0; return BK / 16; }
-  const int nkk = (valid + 15) >> 4;
-  zlo = valid;
-  zhi = nkk * 16;
-  return nkk;
+  return valid >= BK ? BK / 16 : (valid + 15) >> 4;
 }
 
 template <int MODE>
@@ -141,10 +135,11 @@ __device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa,
     const int kk = (second ? kb - a.kb_split : kb) * BK;
     tma_load_2d(sa, second ? a1 : a0, bar, kk, tl.row0);
     tma_load_3d(sb, second ? b1 : b0, bar, kk, tl.n0, tl.e);
-  } else {  // kWG
+  } else {  // kWG: the expert's own descriptors (rows past its end read as 0)
     const int y = tl.krow0 + kb * BK;
-    const CUtensorMap* am = tl.which == 2 ? a1 : a0;
-    const CUtensorMap* bm = tl.which == 0 ? b0 : (tl.which == 1 ? b1 : b2);
+    const CUtensorMap* em = a.wg_maps + (size_t)tl.e * kWgradMaps;
+    const CUtensorMap* am = em + (tl.which == 2 ? 1 : 0);
+    const CUtensorMap* bm = em + 2 + tl.which;
     tma_load_2d(sa, am, bar, tl.m0, y);
     tma_load_2d(sa + SUB, am, bar, tl.m0 + 64, y);
 #pragma unroll
@@ -268,7 +263,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreadsBF, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
@@ -290,7 +285,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&sh->full[s]), 1);
       mbar_init(smem_u32(&sh->empty[s]), 1);
-      mbar_init(smem_u32(&sh->fixed[s]), 1);
     }
     for (int s = 0; s < 2; ++s) { mbar_init(smem_u32(&sh->tfull[s]), 1); mbar_init(smem_u32(&sh->tempty[s]), kEpiWarps); }
     mbar_init(smem_u32(&sh->drain), 1);
@@ -331,6 +325,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
+      if constexpr (MODE == kWG) {
+        // the descriptors were written by an earlier kernel through the
+        // generic proxy; make them visible to the tensormap proxy
+        if (lane == 0 && tl.nkb > 0) {
+          const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
+          tensormap_acquire(em + (tl.which == 2 ? 1 : 0));
+          tensormap_acquire(em + 2 + tl.which);
+        }
+      }
       for (int kb = 0; kb < tl.nkb; ++kb) {
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
@@ -357,7 +360,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kWG);
     constexpr uint32_t idesc = idesc_bf16(BM, BN, a_mn, b_mn);
     int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0, fix_par = 0;
+    uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
@@ -368,14 +371,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         if (lane == 0) mbar_arrive(smem_u32(&sh->tfull[acc]));
       } else {
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          int nkk = BK / 16, zlo = 0, zhi = 0;
-          if constexpr (MODE == kWG) nkk = wg_tail(tl, kb, zlo, zhi);
-          if (zhi > zlo) {
-            // the fixup warp clears the foreign rows of this stage, then releases it
-            if (!bounded_wait(smem_u32(&sh->fixed[stage]), (fix_par >> stage) & 1u, &sh->abort_flag,
-                              args.status)) { ok = false; break; }
-            fix_par ^= 1u << stage;
-          } else if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) {
+          int nkk = BK / 16;
+          if constexpr (MODE == kWG) nkk = wg_groups(tl, kb);
+          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) {
             ok = false;
             break;
           }
@@ -408,7 +406,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
       mma_commit(smem_u32(&sh->drain));
       drain_wait(smem_u32(&sh->drain), 0);
     }
-  } else if (warp < kFixWarp) {
+  } else {
     // --------------------------------------------------------------- epilogue
     const int lane_q = warp & 3;          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;     // which half of the tile's columns
@@ -425,43 +423,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
-  } else if constexpr (MODE == kWG) {
-    // ------------------------------------------------------- ragged-tail fixup
-    // Walks the same k-block sequence as the MMA issuer, waiting for each
-    // stage's data.  For the last block of an expert whose rows end inside a
-    // 16-row group, it zeroes the foreign rows [zlo, zhi) of all six 64x64
-    // sub-tiles (a whole 128-byte row each, so the swizzle does not matter),
-    // publishes the writes to the async proxy and releases the stage.
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
-      bool ok = true;
-      for (int kb = 0; kb < tl.nkb; ++kb) {
-        int zlo, zhi;
-        wg_tail(tl, kb, zlo, zhi);
-        // observe every stage's data in order, so this warp is never more than
-        // one phase ahead on a barrier (a parity wait could otherwise see an
-        // older phase of the same parity as complete)
-        if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
-        if (zhi > zlo) {
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          const int chunk = lane & 7;
-#pragma unroll
-          for (int sub = 0; sub < 6; ++sub) {
-            uint8_t* base = sub < 2 ? (sA + stage * A_STAGE + sub * SUB)
-                                    : (sB + stage * B_STAGE + (sub - 2) * SUB);
-            for (int row = zlo + (lane >> 3); row < zhi; row += 4)
-              *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = z;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sh->fixed[stage]));
-        }
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-      }
-      if (!ok) break;
-    }
   }
 
   tc_fence_before();
@@ -470,6 +431,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// wgrad descriptors: expert e gets copies of the five operand descriptors
+// (xp, a, dh1, dh3, dyp) whose row extent is the expert's end row, so a tile
+// that starts inside the expert reads zeros past its last row.  Thread i
+// writes descriptor i of the [E][5] table.
+struct WgradTemplates { CUtensorMap m[kWgradMaps]; };
+
+__global__ void __launch_bounds__(128)
+wgrad_maps_kernel(const __grid_constant__ WgradTemplates tp, const int32_t* __restrict__ offsets,
+                  int E, int R, CUtensorMap* __restrict__ maps) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= E * kWgradMaps) return;
+  const int e = i / kWgradMaps, op = i - e * kWgradMaps;
+  const int lo = max(0, min(__ldg(offsets + e), R));
+  const int hi = max(lo, min(__ldg(offsets + e + 1), R));
+  const uint4* src = reinterpret_cast<const uint4*>(&tp.m[op]);
+  uint4* dst = reinterpret_cast<uint4*>(maps + i);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dst[j] = src[j];
+  // an empty expert's descriptor is never used; keep its extent legal
+  tensormap_set_dim<1>(maps + i, max(hi, 1));
+  tensormap_release();
 }
 
 // ------------------------------------------------------------------ host side
@@ -488,7 +472,7 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
   static bool attr_done[64] = {false};
   // set once per device for the largest size (E = 1024)
   if (ensure_smem_attr(kern, smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  kern<<<grid, kThreadsBF, smem, s>>>(a0, a1, b0, b1, b2, args);
+  kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, b2, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -582,8 +566,12 @@ int run_dx(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t*
 int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, int h,
               const moe_bf16_t* a, const moe_bf16_t* dyp, const moe_bf16_t* dh1,
               const moe_bf16_t* dh3, moe_bf16_t* dW1, moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
-              cudaStream_t s) {
+              size_t ws_bytes, cudaStream_t s) {
   MOE_CHECK_PTR(dW1); MOE_CHECK_PTR(dW3); MOE_CHECK_PTR(dW2);
+  if (R > 0) {
+    if (ws_bytes < wgrad_maps_end(E)) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 127) != 0) return MOE_ERR_INVALID_ARG;
+  }
   if (R == 0) {
     const size_t wb = (size_t)E * d * h * 2;
     if (cudaMemsetAsync(dW1, 0, wb, s) != cudaSuccess || cudaMemsetAsync(dW3, 0, wb, s) != cudaSuccess ||
@@ -595,13 +583,17 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   }
   MOE_CHECK_PTR(xp); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(a); MOE_CHECK_PTR(dyp);
   MOE_CHECK_PTR(dh1); MOE_CHECK_PTR(dh3);
-  CUtensorMap m_xpt, m_at, m_dh1t, m_dh3t, m_dypt;
+  WgradTemplates tp;
   // MN-major operands: 64 x 64 boxes along (feature, row)
-  if (!map2d(&m_xpt, xp, d, R, 64, 64) || !map2d(&m_at, a, h, R, 64, 64) ||
-      !map2d(&m_dh1t, dh1, h, R, 64, 64) || !map2d(&m_dh3t, dh3, h, R, 64, 64) ||
-      !map2d(&m_dypt, dyp, d, R, 64, 64))
+  if (!map2d(&tp.m[0], xp, d, R, 64, 64) || !map2d(&tp.m[1], a, h, R, 64, 64) ||
+      !map2d(&tp.m[2], dh1, h, R, 64, 64) || !map2d(&tp.m[3], dh3, h, R, 64, 64) ||
+      !map2d(&tp.m[4], dyp, d, R, 64, 64))
     return MOE_ERR_CUDA;
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  wgrad_maps_kernel<<<(E * kWgradMaps + 127) / 128, 128, 0, s>>>(tp, offsets, E, R, maps);
+  MOE_LAUNCH_CHECK(1);
   GemmArgs g = base_args(offsets, R, E, d, h, ws);
+  g.wg_maps = maps;
   g.out0 = dW1; g.out1 = dW3; g.out2 = dW2;
   g.wg_mt1 = (d + BM - 1) / BM;
   g.wg_mt2 = (h + BM - 1) / BM;
@@ -609,7 +601,7 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   g.wg_t2 = g.wg_mt2 * ((d + BN - 1) / BN);
   long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
   int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  return launch<kWG>(m_xpt, m_at, m_dh1t, m_dh3t, m_dypt, g, grid, s);
+  return launch<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], tp.m[4], g, grid, s);
 }
 
 }  // namespace
@@ -665,7 +657,7 @@ int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets, int R, 
     st = run_dx(offsets, R, E, d, h, W1, W3, dh1, dh3, dxp, ws, s);
     if (st != MOE_OK) return st;
   }
-  return run_wgrad(xp, offsets, R, E, d, h, a, dyp, dh1, dh3, dW1, dW3, dW2, ws, s);
+  return run_wgrad(xp, offsets, R, E, d, h, a, dyp, dh1, dh3, dW1, dW3, dW2, ws, ws_bytes, s);
 }
 
 int moe_grouped_swiglu_bwd_dact(const int32_t* offsets, int R, int E, int d, int h,
@@ -692,7 +684,7 @@ int moe_grouped_swiglu_bwd_wgrad(const moe_bf16_t* xp, const int32_t* offsets, i
                                  moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws, size_t ws_bytes,
                                  moe_stream_t stream) {
   MOE_GEMM_PROLOGUE();
-  return run_wgrad(xp, offsets, R, E, d, h, a, dyp, dh1, dh3, dW1, dW3, dW2, ws, s);
+  return run_wgrad(xp, offsets, R, E, d, h, a, dyp, dh1, dh3, dW1, dW3, dW2, ws, ws_bytes, s);
 }
 
 }  // extern "C"

@@ -67,6 +67,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// TMA descriptors kept in global memory and edited on the device: replace
+// the extent of dimension `dim` of the descriptor at `map` (generic proxy),
+// publish such edits (release), and make them visible to the tensormap proxy
+// of a later reader (acquire on the 128-byte object).
+template <int DIM>
+__device__ __forceinline__ void tensormap_set_dim(CUtensorMap* map, int extent) {
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], %1, %2;"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "n"(DIM), "r"(extent) : "memory");
+}
+__device__ __forceinline__ void tensormap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;"
+               ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 // make generic-proxy shared-memory writes visible to the async proxy
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
