@@ -35,12 +35,22 @@ struct PipeShared {
 
 // Wait for the phase `parity` of an mbarrier; give up after kWaitLimitNs (or
 // when another warp of the CTA has given up), recording MOE_DEV_WAIT_TIMEOUT.
+// KIND 0: try_wait (the thread may be suspended until the phase completes);
+// 1: the same with cluster-scope acquire; 2: polling with test_wait.
+enum WaitKind : int { kWaitTry = 0, kWaitTryCluster = 1, kWaitPoll = 2 };
+template <int KIND = kWaitTry>
+__device__ __forceinline__ bool probe_phase(uint32_t bar, uint32_t parity) {
+  if constexpr (KIND == kWaitTryCluster) return mbar_try_wait_cluster(bar, parity);
+  else if constexpr (KIND == kWaitPoll) return mbar_test_wait(bar, parity);
+  else return mbar_try_wait(bar, parity);
+}
+template <int KIND = kWaitTry>
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, int* abort_flag,
                                              int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (probe_phase<KIND>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe_phase<KIND>(bar, parity)) return true;
     if ((n & 127u) == 0) {
       if (*(volatile int*)abort_flag) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {

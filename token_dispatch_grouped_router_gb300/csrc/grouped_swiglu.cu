@@ -433,6 +433,193 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   }
 }
 
+// ------------------------------------------------- wgrad on CTA pairs
+// The weight gradients as 256 x 256 output tiles, each computed by a pair of
+// CTAs (a 2-CTA cluster) with tcgen05 MMAs of M = 256, N = 256: CTA r of the
+// pair loads rows [m0 + 128r, +128) of A and columns [n0 + 128r, +128) of B
+// for every 64-row k-block, so a CTA stages 32 KB per k-block for a 128 x 256
+// share of the output (48 KB on a single CTA).  Both CTAs' copies complete on
+// the even CTA's `full` barrier; that CTA issues the MMAs and commits them to
+// the `empty` and `tfull` barriers of both CTAs.
+constexpr int P_STAGES = 6;
+constexpr int P_HALF = 128 * BK * 2;                  // 16 KB: 128 features x 64 rows
+constexpr int P_TILE = 256;
+using PairShared = PipeShared<P_STAGES>;
+
+__device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const int* s_off) {
+  Tile tl{};
+  const int per = 2 * a.wg_t1 + a.wg_t2;
+  tl.e = t / per;
+  int l = t - tl.e * per;
+  int mt;
+  if (l < a.wg_t1) { tl.which = 0; mt = a.wg_mt1; }
+  else if (l < 2 * a.wg_t1) { tl.which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
+  else { tl.which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
+  tl.m0 = (l % mt) * P_TILE;
+  tl.n0 = (l / mt) * P_TILE;
+  int lo = s_off[tl.e], hi = s_off[tl.e + 1];
+  lo = max(0, min(lo, a.R));
+  hi = max(lo, min(hi, a.R));
+  tl.krow0 = lo;
+  tl.krows = hi - lo;
+  tl.nkb = (tl.krows + BK - 1) / BK;
+  return tl;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * P_HALF;
+  uint8_t* sStage = sB + P_STAGES * P_HALF;
+  PairShared* sh = reinterpret_cast<PairShared*>(sStage + kEpiWarps * kStageBytes);
+  int* s_off = reinterpret_cast<int*>(sh + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sh->tfull[s]), 1);
+      mbar_init(smem_u32(&sh->tempty[s]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort_flag = 0;
+    fence_mbar_init();
+  }
+  const int total = args.E * (2 * args.wg_t1 + args.wg_t2);
+  // both CTAs' barriers exist before either CTA signals the other's
+  cluster_sync();
+  if (pair >= total) return;                 // uniform across the pair; no TMEM taken
+
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sh->tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, last_par = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      const Tile tl = decode_pair_tile(t, args, s_off);
+      const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
+      const CUtensorMap* am = em + (tl.which == 2 ? 1 : 0);
+      const CUtensorMap* bm = em + 2 + tl.which;
+      if (lane == 0 && tl.nkb > 0) { tensormap_acquire(am); tensormap_acquire(bm); }
+      const int ma = tl.m0 + 128 * (int)rank, nb = tl.n0 + 128 * (int)rank;
+      for (int kb = 0; kb < tl.nkb; ++kb) {
+        if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t fb_local = smem_u32(&sh->full[stage]);
+          const uint32_t fb = mapa_shared(fb_local, 0);
+          if (leader) mbar_arrive_expect_tx(fb_local, 4 * P_HALF);   // both CTAs' copies
+          const int y = tl.krow0 + kb * BK;
+          const uint32_t sa = smem_u32(sA + stage * P_HALF), sb = smem_u32(sB + stage * P_HALF);
+          tma_load_2d_pair(sa, am, fb, ma, y);
+          tma_load_2d_pair(sa + SUB, am, fb, ma + 64, y);
+          tma_load_2d_pair(sb, bm, fb, nb, y);
+          tma_load_2d_pair(sb + SUB, bm, fb, nb + 64, y);
+        }
+        __syncwarp();
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && leader && lane == 0) {
+      // the even CTA's full barriers count both CTAs' copies
+      for (int s = 0; s < P_STAGES; ++s)
+        if (issued & (1u << s)) drain_wait(smem_u32(&sh->full[s]), (last_par >> s) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------- MMA issuer (even CTA of the pair)
+    if (leader) {
+      constexpr uint32_t idesc = idesc_bf16(P_TILE, P_TILE, true, true);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, issued_any = false;
+      for (int t = pair; t < total && ok; t += npairs) {
+        const Tile tl = decode_pair_tile(t, args, s_off);
+        if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tf = smem_u32(&sh->tfull[acc]);
+        if (tl.nkb == 0) {
+          if (lane == 0) { mbar_arrive_cluster(mapa_shared(tf, 0)); mbar_arrive_cluster(mapa_shared(tf, 1)); }
+        } else {
+          const uint32_t dt = tmem + (uint32_t)(acc * P_TILE);
+          for (int kb = 0; kb < tl.nkb; ++kb) {
+            const int nkk = wg_groups(tl, kb);
+            if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t sa = smem_u32(sA + stage * P_HALF), sb = smem_u32(sB + stage * P_HALF);
+              for (int kk = 0; kk < nkk; ++kk)
+                mma_f16_pair(dt, sdesc_sw128(sa + kk * 2048, SUB, 1024),
+                             sdesc_sw128(sb + kk * 2048, SUB, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              const uint32_t eb = smem_u32(&sh->empty[stage]);
+              mma_commit_pair(mapa_shared(eb, 0));
+              mma_commit_pair(mapa_shared(eb, 1));
+            }
+            issued_any = true;
+            __syncwarp();
+            if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          if (lane == 0) { mma_commit_pair(mapa_shared(tf, 0)); mma_commit_pair(mapa_shared(tf, 1)); }
+          __syncwarp();
+        }
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok && issued_any && lane == 0) {
+        mma_commit_pair(mapa_shared(smem_u32(&sh->drain), 0));
+        drain_wait(smem_u32(&sh->drain), 0);
+      }
+    }
+    // the odd CTA's MMA warp only holds its half of the TMEM allocation
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int lane_q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < total; t += npairs) {
+      Tile tl = decode_pair_tile(t, args, s_off);
+      tl.m0 += 128 * (int)rank;                 // this CTA's rows of the output tile
+      if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
+      tc_fence_after();
+      epilogue_tile<kWG>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
+                         sStage + (warp - 2) * kStageBytes, args);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tempty[acc]), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  // no CTA leaves (or frees TMEM) while its peer may still signal it
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // wgrad descriptors: expert e gets copies of the five operand descriptors
 // (xp, a, dh1, dh3, dyp) whose row extent is the expert's end row, so a tile
 // that starts inside the expert reads zeros past its last row.  Thread i
@@ -473,6 +660,63 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
   // set once per device for the largest size (E = 1024)
   if (ensure_smem_attr(kern, smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
   kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, b2, args);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+constexpr size_t pair_smem_bytes(int E) {
+  return 1024 + (size_t)P_STAGES * 2 * P_HALF + (size_t)kEpiWarps * kStageBytes + sizeof(PairShared) +
+         (size_t)(E + 1) * 4;
+}
+
+// 2-CTA clusters of wgrad_pair_kernel that fit on the device at once
+// (queried once per device, outside any stream capture that follows)
+int pair_cluster_limit(cudaStream_t s) {
+  static int limit[64] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return -1;
+  if (limit[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * sm_count());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pair_smem_bytes(kMaxExperts);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, wgrad_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return -1;
+    }
+    limit[dev] = n;
+  }
+  return limit[dev];
+}
+
+int launch_wgrad_pair(const GemmArgs& g, long long tiles, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  if (ensure_smem_attr(wgrad_pair_kernel, pair_smem_bytes(kMaxExperts), attr_done) != MOE_OK)
+    return MOE_ERR_CUDA;
+  const int limit = pair_cluster_limit(s);
+  if (limit <= 0) return MOE_ERR_CUDA;
+  const int npairs = (int)(tiles < limit ? tiles : limit);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * npairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pair_smem_bytes(g.E);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, wgrad_pair_kernel, g) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -595,13 +839,13 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   GemmArgs g = base_args(offsets, R, E, d, h, ws);
   g.wg_maps = maps;
   g.out0 = dW1; g.out1 = dW3; g.out2 = dW2;
-  g.wg_mt1 = (d + BM - 1) / BM;
-  g.wg_mt2 = (h + BM - 1) / BM;
-  g.wg_t1 = g.wg_mt1 * ((h + BN - 1) / BN);
-  g.wg_t2 = g.wg_mt2 * ((d + BN - 1) / BN);
-  long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
-  int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  return launch<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], tp.m[4], g, grid, s);
+  // 256 x 256 output tiles, one per CTA pair
+  g.wg_mt1 = (d + P_TILE - 1) / P_TILE;
+  g.wg_mt2 = (h + P_TILE - 1) / P_TILE;
+  g.wg_t1 = g.wg_mt1 * ((h + P_TILE - 1) / P_TILE);
+  g.wg_t2 = g.wg_mt2 * ((d + P_TILE - 1) / P_TILE);
+  const long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
+  return launch_wgrad_pair(g, tiles, s);
 }
 
 }  // namespace
