@@ -82,6 +82,11 @@ def compare_full(layer, w, inp, backward=True):
     (513, 192, 8, 4, 320, (0, 7)),      # d and h off the 256 grid, empty ends
     (1000, 512, 16, 4, 256, (5,)),      # several tiles per expert
     (64, 128, 1, 1, 128, ()),           # a single dense expert
+    # >= 512 rows per expert on average: the UP, DOWN and DX GEMMs run on
+    # CTA pairs with 256-row tiles
+    (2700, 192, 4, 2, 320, (2,)),       # pair tiles, ragged tails, one empty expert
+    (2100, 256, 2, 1, 128, ()),         # pair tiles, one 128-wide hidden tile
+    (1100, 128, 1, 1, 64, ()),          # last tile's odd CTA holds no rows
 ])
 def test_layer_small_full_compare(T, d, E, k, h, empty):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
@@ -141,8 +146,9 @@ def test_graph_capture_proves_no_host_sync_and_replays_bitwise():
         assert torch.equal(getattr(layer, n), v), n
 
 
-def test_deterministic_bitwise():
-    w = wl.small_workload(T=2000, d=256, E=16, k=4, h=256)
+@pytest.mark.parametrize("T,E", [(2000, 16), (2048, 4)])   # single-CTA / CTA-pair row GEMMs
+def test_deterministic_bitwise(T, E):
+    w = wl.small_workload(T=T, d=256, E=E, k=4, h=256)
     inp = wl.generate(w, seed=5)
     layer = make_layer(w, inp)
     run(layer)
@@ -152,10 +158,11 @@ def test_deterministic_bitwise():
         assert torch.equal(getattr(layer, n), v), n
 
 
-def test_outputs_stay_inside_their_buffers():
+@pytest.mark.parametrize("T,E", [(333, 5), (1400, 2)])    # single-CTA / CTA-pair row GEMMs
+def test_outputs_stay_inside_their_buffers(T, E):
     # every output is a view at the front of a larger buffer whose tail holds a
     # sentinel; a write past the end of any output would change it
-    w = wl.small_workload(T=333, d=192, E=5, k=2, h=320)
+    w = wl.small_workload(T=T, d=192, E=E, k=2, h=320)
     inp = wl.generate(w, seed=6)
     layer = make_layer(w, inp)
     guards = {}

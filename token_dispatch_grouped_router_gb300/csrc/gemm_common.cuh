@@ -153,10 +153,11 @@ __device__ __forceinline__ void chunk_to_row(const uint4 (&q)[4], uint8_t* stg, 
 }
 
 // ------------------------------------------------- row-grouped tile table
-// Expert e owns ceil(n_e / 128) row blocks x n_tiles column blocks; the
+// Expert e owns ceil(n_e / TM) row blocks x n_tiles column blocks; the
 // tiles are numbered expert-major.  Warp 0 writes the expert offsets (clamped
 // to [0, R]) into s_off[0..E] and the first tile of every expert into
 // s_ts[0..E] (s_ts[E] = number of tiles).  s_off must already hold offsets.
+template <int TM = 128>
 __device__ __forceinline__ int build_row_tile_table(const int* s_off, int* s_ts, int E, int R,
                                                     int n_tiles, int lane) {
   int carry = 0;
@@ -166,7 +167,7 @@ __device__ __forceinline__ int build_row_tile_table(const int* s_off, int* s_ts,
     if (e < E) {
       const int lo = max(0, min(s_off[e], R));
       const int hi = max(lo, min(s_off[e + 1], R));
-      cnt = ((hi - lo + 127) / 128) * n_tiles;
+      cnt = ((hi - lo + TM - 1) / TM) * n_tiles;
     }
     int incl = cnt;
 #pragma unroll
@@ -185,8 +186,9 @@ struct RowTile {
   int e, row0, rows, n_idx;
 };
 
-// Tile t -> expert, first row, valid rows (<= 128) and column-block index;
+// Tile t -> expert, first row, valid rows (<= TM) and column-block index;
 // within an expert the row block varies fastest.
+template <int TM = 128>
 __device__ __forceinline__ RowTile decode_row_tile(int t, int E, int R, const int* s_off,
                                                    const int* s_ts) {
   int lo = 0, hi = E;                 // invariant: s_ts[lo] <= t < s_ts[hi]
@@ -198,12 +200,12 @@ __device__ __forceinline__ RowTile decode_row_tile(int t, int E, int R, const in
   r.e = lo;
   const int seg0 = max(0, min(s_off[lo], R));
   const int seg1 = max(seg0, min(s_off[lo + 1], R));
-  const int mt = (seg1 - seg0 + 127) / 128;
+  const int mt = (seg1 - seg0 + TM - 1) / TM;
   const int l = t - s_ts[lo];
   const int m_idx = l % mt;
   r.n_idx = l / mt;
-  r.row0 = seg0 + m_idx * 128;
-  r.rows = min(128, seg1 - r.row0);
+  r.row0 = seg0 + m_idx * TM;
+  r.rows = min(TM, seg1 - r.row0);
   return r;
 }
 
@@ -257,8 +259,11 @@ inline bool map3d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t mid,
 // Persistent grid for a row-grouped GEMM: at most one CTA per SM; the real
 // tile count is only known on the device (<= (ceil(R/128) + E) * n_tiles) and
 // CTAs without a tile exit at once.
+inline long long row_tiles_upper(int R, int E, int n_tiles, int tm = 128) {
+  return ((long long)(R + tm - 1) / tm + E) * n_tiles;
+}
 inline int row_grid_upper(int R, int E, int n_tiles) {
-  long long ub = ((long long)(R + 127) / 128 + E) * n_tiles;
+  long long ub = row_tiles_upper(R, E, n_tiles);
   long long g = sm_count();
   return (int)(ub < g ? (ub > 0 ? ub : 1) : g);
 }

@@ -433,40 +433,96 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   }
 }
 
-// ------------------------------------------------- wgrad on CTA pairs
-// The weight gradients as 256 x 256 output tiles, each computed by a pair of
-// CTAs (a 2-CTA cluster) with tcgen05 MMAs of M = 256, N = 256: CTA r of the
-// pair loads rows [m0 + 128r, +128) of A and columns [n0 + 128r, +128) of B
-// for every 64-row k-block, so a CTA stages 32 KB per k-block for a 128 x 256
-// share of the output (48 KB on a single CTA).  Both CTAs' copies complete on
-// the even CTA's `full` barrier; that CTA issues the MMAs and commits them to
-// the `empty` and `tfull` barriers of both CTAs.
+// ------------------------------------------------------------ CTA pairs
+// The same GEMMs on pairs of CTAs (2-CTA clusters) with tcgen05 MMAs of
+// M = 256, N = 256: CTA r of a pair stages rows [128r, 128r + 128) of the
+// tile's A operand and columns [128r, 128r + 128) of its B operand for every
+// 64-deep k-block, i.e. 32 KB per k-block for a 128 x 256 share of the output
+// (48 KB on a single CTA).  Both CTAs' copies complete on the even CTA's
+// `full` barrier; that CTA issues the MMAs and commits them to the `empty`
+// and `tfull` barriers of both CTAs; every epilogue warp of the pair releases
+// an accumulator on the even CTA's `tempty` barrier.
+//   UP, DOWN, DX:      256-row tiles of an expert's rows; UP splits B into
+//                      W1 columns (even CTA) and W3 columns (odd CTA), so the
+//                      accumulator keeps the single-CTA column layout.  (The
+//                      DA epilogue, which reads h1 and h3 for every output,
+//                      bounds that GEMM already on a single CTA; it stays there.)
+//   WG:                256 x 256 tiles of dW over the expert's rows.
 constexpr int P_STAGES = 6;
-constexpr int P_HALF = 128 * BK * 2;                  // 16 KB: 128 features x 64 rows
+constexpr int P_HALF = 128 * BK * 2;                  // 16 KB: 128 rows x 64 deep
 constexpr int P_TILE = 256;
 using PairShared = PipeShared<P_STAGES>;
 
-__device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const int* s_off) {
+template <int MODE>
+__device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const int* s_off,
+                                                 const int* s_ts) {
   Tile tl{};
-  const int per = 2 * a.wg_t1 + a.wg_t2;
-  tl.e = t / per;
-  int l = t - tl.e * per;
-  int mt;
-  if (l < a.wg_t1) { tl.which = 0; mt = a.wg_mt1; }
-  else if (l < 2 * a.wg_t1) { tl.which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
-  else { tl.which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
-  tl.m0 = (l % mt) * P_TILE;
-  tl.n0 = (l / mt) * P_TILE;
-  int lo = s_off[tl.e], hi = s_off[tl.e + 1];
-  lo = max(0, min(lo, a.R));
-  hi = max(lo, min(hi, a.R));
-  tl.krow0 = lo;
-  tl.krows = hi - lo;
-  tl.nkb = (tl.krows + BK - 1) / BK;
+  if constexpr (MODE == kWG) {
+    const int per = 2 * a.wg_t1 + a.wg_t2;
+    tl.e = t / per;
+    int l = t - tl.e * per;
+    int mt;
+    if (l < a.wg_t1) { tl.which = 0; mt = a.wg_mt1; }
+    else if (l < 2 * a.wg_t1) { tl.which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
+    else { tl.which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
+    tl.m0 = (l % mt) * P_TILE;
+    tl.n0 = (l / mt) * P_TILE;
+    int lo = s_off[tl.e], hi = s_off[tl.e + 1];
+    lo = max(0, min(lo, a.R));
+    hi = max(lo, min(hi, a.R));
+    tl.krow0 = lo;
+    tl.krows = hi - lo;
+    tl.nkb = (tl.krows + BK - 1) / BK;
+  } else {
+    const RowTile r = decode_row_tile<P_TILE>(t, a.E, a.R, s_off, s_ts);
+    tl.e = r.e;
+    tl.row0 = r.row0;
+    tl.rows = r.rows;
+    tl.n0 = r.n_idx * (MODE == kUp ? BN / 2 : BN);
+    tl.nkb = a.kb_total;
+  }
   return tl;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs args) {
+// This CTA's share of k-block kb: 16 KB of A at sa, 16 KB of B at sb, both
+// counted on the even CTA's barrier `fb`.
+template <int MODE>
+__device__ __forceinline__ void issue_loads_pair(const Tile& tl, int kb, uint32_t rank, uint32_t sa,
+                                                 uint32_t sb, uint32_t fb, const CUtensorMap* a0,
+                                                 const CUtensorMap* a1, const CUtensorMap* b0,
+                                                 const CUtensorMap* b1, const GemmArgs& a) {
+  const int r128 = 128 * (int)rank;
+  if constexpr (MODE == kUp) {
+    const CUtensorMap* bm = rank == 0 ? b0 : b1;           // W1 or W3 columns n0 .. n0+127
+    tma_load_2d_pair(sa, a0, fb, kb * BK, tl.row0 + r128);
+    tma_load_3d_pair(sb, bm, fb, tl.n0, kb * BK, tl.e);
+    tma_load_3d_pair(sb + SUB, bm, fb, tl.n0 + 64, kb * BK, tl.e);
+  } else if constexpr (MODE == kDown) {
+    tma_load_2d_pair(sa, a0, fb, kb * BK, tl.row0 + r128);
+    tma_load_3d_pair(sb, b0, fb, tl.n0 + r128, kb * BK, tl.e);
+    tma_load_3d_pair(sb + SUB, b0, fb, tl.n0 + r128 + 64, kb * BK, tl.e);
+  } else if constexpr (MODE == kDX) {
+    const bool second = kb >= a.kb_split;
+    const int kk = (second ? kb - a.kb_split : kb) * BK;
+    tma_load_2d_pair(sa, second ? a1 : a0, fb, kk, tl.row0 + r128);
+    tma_load_3d_pair(sb, second ? b1 : b0, fb, kk, tl.n0 + r128, tl.e);
+  } else {  // kWG: the expert's own descriptors (rows past its end read as 0)
+    const CUtensorMap* em = a.wg_maps + (size_t)tl.e * kWgradMaps;
+    const CUtensorMap* am = em + (tl.which == 2 ? 1 : 0);
+    const CUtensorMap* bm = em + 2 + tl.which;
+    const int y = tl.krow0 + kb * BK;
+    tma_load_2d_pair(sa, am, fb, tl.m0 + r128, y);
+    tma_load_2d_pair(sa + SUB, am, fb, tl.m0 + r128 + 64, y);
+    tma_load_2d_pair(sb, bm, fb, tl.n0 + r128, y);
+    tma_load_2d_pair(sb + SUB, bm, fb, tl.n0 + r128 + 64, y);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                 const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -474,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs 
   uint8_t* sStage = sB + P_STAGES * P_HALF;
   PairShared* sh = reinterpret_cast<PairShared*>(sStage + kEpiWarps * kStageBytes);
   int* s_off = reinterpret_cast<int*>(sh + 1);
+  int* s_ts = s_off + (args.E + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -495,14 +552,27 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs 
     sh->abort_flag = 0;
     fence_mbar_init();
   }
-  const int total = args.E * (2 * args.wg_t1 + args.wg_t2);
-  // both CTAs' barriers exist before either CTA signals the other's
+  __syncthreads();
+  if constexpr (MODE == kWG) {
+    if (threadIdx.x == 0) sh->total_tiles = args.E * (2 * args.wg_t1 + args.wg_t2);
+  } else {
+    if (warp == 0) {
+      const int n = build_row_tile_table<P_TILE>(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
+      if (lane == 0) sh->total_tiles = n;
+    }
+  }
+  // both CTAs' barriers exist before either CTA signals the other's; both
+  // CTAs of a pair see the same offsets and so the same tile count
   cluster_sync();
+  const int total = sh->total_tiles;
   if (pair >= total) return;                 // uniform across the pair; no TMEM taken
 
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&sh->tmem_base), kTmemCols);
     tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0 && MODE != kWG) {
+    prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
   }
   tc_fence_before();
   cluster_sync();
@@ -515,24 +585,24 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs 
     uint32_t phase = 0, issued = 0, last_par = 0;
     bool ok = true;
     for (int t = pair; t < total && ok; t += npairs) {
-      const Tile tl = decode_pair_tile(t, args, s_off);
-      const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
-      const CUtensorMap* am = em + (tl.which == 2 ? 1 : 0);
-      const CUtensorMap* bm = em + 2 + tl.which;
-      if (lane == 0 && tl.nkb > 0) { tensormap_acquire(am); tensormap_acquire(bm); }
-      const int ma = tl.m0 + 128 * (int)rank, nb = tl.n0 + 128 * (int)rank;
+      const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+      if constexpr (MODE == kWG) {
+        // the descriptors were written by an earlier kernel through the
+        // generic proxy; make them visible to the tensormap proxy
+        if (lane == 0 && tl.nkb > 0) {
+          const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
+          tensormap_acquire(em + (tl.which == 2 ? 1 : 0));
+          tensormap_acquire(em + 2 + tl.which);
+        }
+      }
       for (int kb = 0; kb < tl.nkb; ++kb) {
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t fb_local = smem_u32(&sh->full[stage]);
-          const uint32_t fb = mapa_shared(fb_local, 0);
           if (leader) mbar_arrive_expect_tx(fb_local, 4 * P_HALF);   // both CTAs' copies
-          const int y = tl.krow0 + kb * BK;
-          const uint32_t sa = smem_u32(sA + stage * P_HALF), sb = smem_u32(sB + stage * P_HALF);
-          tma_load_2d_pair(sa, am, fb, ma, y);
-          tma_load_2d_pair(sa + SUB, am, fb, ma + 64, y);
-          tma_load_2d_pair(sb, bm, fb, nb, y);
-          tma_load_2d_pair(sb + SUB, bm, fb, nb + 64, y);
+          issue_loads_pair<MODE>(tl, kb, rank, smem_u32(sA + stage * P_HALF),
+                                 smem_u32(sB + stage * P_HALF), mapa_shared(fb_local, 0), &tmA0,
+                                 &tmA1, &tmB0, &tmB1, args);
         }
         __syncwarp();
         issued |= 1u << stage;
@@ -549,12 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs 
   } else if (warp == 1) {
     // ------------------------------------- MMA issuer (even CTA of the pair)
     if (leader) {
-      constexpr uint32_t idesc = idesc_bf16(P_TILE, P_TILE, true, true);
+      constexpr bool a_mn = (MODE == kWG);
+      constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kWG);
+      constexpr uint32_t idesc = idesc_bf16(P_TILE, P_TILE, a_mn, b_mn);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued_any = false;
       for (int t = pair; t < total && ok; t += npairs) {
-        const Tile tl = decode_pair_tile(t, args, s_off);
+        const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
         if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tf = smem_u32(&sh->tfull[acc]);
@@ -563,14 +635,20 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs 
         } else {
           const uint32_t dt = tmem + (uint32_t)(acc * P_TILE);
           for (int kb = 0; kb < tl.nkb; ++kb) {
-            const int nkk = wg_groups(tl, kb);
+            int nkk = BK / 16;
+            if constexpr (MODE == kWG) nkk = wg_groups(tl, kb);
             if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
             tc_fence_after();
             if (lane == 0) {
               const uint32_t sa = smem_u32(sA + stage * P_HALF), sb = smem_u32(sB + stage * P_HALF);
-              for (int kk = 0; kk < nkk; ++kk)
-                mma_f16_pair(dt, sdesc_sw128(sa + kk * 2048, SUB, 1024),
-                             sdesc_sw128(sb + kk * 2048, SUB, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < nkk; ++kk) {
+                uint64_t ad, bd;
+                if constexpr (a_mn) ad = sdesc_sw128(sa + kk * 2048, SUB, 1024);
+                else ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+                if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
+                else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+                mma_f16_pair(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              }
               const uint32_t eb = smem_u32(&sh->empty[stage]);
               mma_commit_pair(mapa_shared(eb, 0));
               mma_commit_pair(mapa_shared(eb, 1));
@@ -598,12 +676,18 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_pair_kernel(const GemmArgs 
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < total; t += npairs) {
-      Tile tl = decode_pair_tile(t, args, s_off);
-      tl.m0 += 128 * (int)rank;                 // this CTA's rows of the output tile
+      Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+      // this CTA's rows of the output tile
+      if constexpr (MODE == kWG) {
+        tl.m0 += 128 * (int)rank;
+      } else {
+        tl.row0 += 128 * (int)rank;
+        tl.rows = max(0, min(128, tl.rows - 128 * (int)rank));
+      }
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue_tile<kWG>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
-                         sStage + (warp - 2) * kStageBytes, args);
+      epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
+                          sStage + (warp - 2) * kStageBytes, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tempty[acc]), 0));
@@ -666,60 +750,61 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
 
 constexpr size_t pair_smem_bytes(int E) {
   return 1024 + (size_t)P_STAGES * 2 * P_HALF + (size_t)kEpiWarps * kStageBytes + sizeof(PairShared) +
-         (size_t)(E + 1) * 4;
+         2 * (size_t)(E + 1) * 4;
 }
 
-// 2-CTA clusters of wgrad_pair_kernel that fit on the device at once
-// (queried once per device, outside any stream capture that follows)
-int pair_cluster_limit(cudaStream_t s) {
-  static int limit[64] = {0};
-  const int dev = current_device();
-  if (dev < 0 || dev >= 64) return -1;
-  if (limit[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * sm_count());
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = pair_smem_bytes(kMaxExperts);
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, wgrad_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      return -1;
-    }
-    limit[dev] = n;
-  }
-  return limit[dev];
-}
-
-int launch_wgrad_pair(const GemmArgs& g, long long tiles, cudaStream_t s) {
-  static bool attr_done[64] = {false};
-  if (ensure_smem_attr(wgrad_pair_kernel, pair_smem_bytes(kMaxExperts), attr_done) != MOE_OK)
-    return MOE_ERR_CUDA;
-  const int limit = pair_cluster_limit(s);
-  if (limit <= 0) return MOE_ERR_CUDA;
-  const int npairs = (int)(tiles < limit ? tiles : limit);
+inline cudaLaunchConfig_t pair_config(int npairs, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = pair_smem_bytes(g.E);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, wgrad_pair_kernel, g) != cudaSuccess) {
+  return cfg;
+}
+
+// Launches pair_gemm_kernel<MODE> on min(tiles_upper, co-resident pairs)
+// clusters.  The co-resident cluster count is queried once per device, on
+// the first call (outside any stream capture that follows).
+template <int MODE>
+int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                const CUtensorMap& b1, const GemmArgs& g, long long tiles_upper, cudaStream_t s) {
+  static_assert(MODE != kDA, "the DA GEMM runs on single CTAs");
+  auto kern = pair_gemm_kernel<MODE>;
+  static bool attr_done[64] = {false};
+  static int limit[64] = {0};
+  if (ensure_smem_attr(kern, pair_smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  cudaLaunchAttribute at[1];
+  if (limit[dev] == 0) {
+    cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes(kMaxExperts), s, at);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    limit[dev] = n;
+  }
+  const long long ub = tiles_upper > 0 ? tiles_upper : 1;
+  const int npairs = (int)(ub < limit[dev] ? ub : limit[dev]);
+  cudaLaunchConfig_t cfg = pair_config(npairs, pair_smem_bytes(g.E), s, at);
+  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, g) != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_ERR_CUDA;
   }
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
+
+// UP, DOWN and DX run on CTA pairs (256-row tiles) unless the experts are
+// small on average: then the 128-row tiles of the single-CTA kernel waste
+// less on each expert's last, partial tile.
+constexpr long long kPairMinRowsPerExpert = 512;
+inline bool rows_on_pairs(int R, int E) { return (long long)R >= kPairMinRowsPerExpert * E; }
 
 int check_common(const void* ws, size_t ws_bytes, int R, int E, int d, int h) {
   if (R < 0 || E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
@@ -757,6 +842,8 @@ int run_up(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, in
   g.n_tiles = (h + BN / 2 - 1) / (BN / 2);      // 128 h-columns of W1 and of W3 per tile
   g.kb_total = d / BK;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.ldo = h;
+  if (rows_on_pairs(R, E))
+    return launch_pair<kUp>(mx, mx, mw1, mw3, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
   return launch<kUp>(mx, mx, mw1, mw3, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
@@ -770,6 +857,8 @@ int run_down(const moe_bf16_t* a, const int32_t* offsets, int R, int E, int d, i
   g.n_tiles = (d + BN - 1) / BN;
   g.kb_total = h / BK;
   g.out0 = yp; g.ldo = d;
+  if (rows_on_pairs(R, E))
+    return launch_pair<kDown>(ma, ma, mw2, mw2, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
   return launch<kDown>(ma, ma, mw2, mw2, mw2, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
@@ -794,15 +883,19 @@ int run_dx(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t*
            void* ws, cudaStream_t s) {
   MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3); MOE_CHECK_PTR(dh1);
   MOE_CHECK_PTR(dh3); MOE_CHECK_PTR(dxp);
+  const bool pairs = rows_on_pairs(R, E);
+  const uint32_t bn = pairs ? BN / 2 : BN;
   CUtensorMap m_dh1, m_dh3, m_w1k, m_w3k;
   if (!map2d(&m_dh1, dh1, h, R, 64, BM) || !map2d(&m_dh3, dh3, h, R, 64, BM) ||
-      !map3d(&m_w1k, W1, h, d, E, 64, BN) || !map3d(&m_w3k, W3, h, d, E, 64, BN))
+      !map3d(&m_w1k, W1, h, d, E, 64, bn) || !map3d(&m_w3k, W3, h, d, E, 64, bn))
     return MOE_ERR_CUDA;
   GemmArgs g = base_args(offsets, R, E, d, h, ws);
   g.n_tiles = (d + BN - 1) / BN;
   g.kb_total = 2 * (h / BK);
   g.kb_split = h / BK;
   g.out0 = dxp; g.ldo = d;
+  if (pairs)
+    return launch_pair<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
   return launch<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, m_w3k, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
@@ -845,7 +938,7 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   g.wg_t1 = g.wg_mt1 * ((h + P_TILE - 1) / P_TILE);
   g.wg_t2 = g.wg_mt2 * ((d + P_TILE - 1) / P_TILE);
   const long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
-  return launch_wgrad_pair(g, tiles, s);
+  return launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], g, tiles, s);
 }
 
 }  // namespace
