@@ -41,7 +41,7 @@ UNIT = "tok/s"
 FLUSH_BYTES = 512 << 20
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = {
-    "gemm": ["grouped_swiglu.cu", "sm103_ptx.cuh", "common.cuh"],
+    "gemm": ["grouped_swiglu.cu", "gemm_common.cuh", "sm103_ptx.cuh", "common.cuh"],
     "rows": ["permute.cu", "common.cuh"],
 }
 
