@@ -132,60 +132,70 @@ __device__ __forceinline__ uint4 scale8(uint4 a, float g) {
 }
 
 // dyp[row(t,j)] = g[t,j] * dout[t];  dg[t,j] = <dout[t], yp[row(t,j)]>
-template <int U>
+// K (= k) is a template parameter so that all K x U row loads of a pass are
+// issued before the first use (the scaled stores would otherwise order each
+// slot's loads after the previous slot's stores).
+template <int K, int U>
 __global__ void __launch_bounds__(kThreads)
 combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ yp,
                    const int32_t* __restrict__ row_of_slot, const float* __restrict__ gate,
-                   int T, int k, int d, uint16_t* __restrict__ dyp, float* __restrict__ dgate) {
+                   int T, int d, uint16_t* __restrict__ dyp, float* __restrict__ dgate) {
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const int nvec = d >> 3;
-  int rows[kMaxTopK];
-  float g[kMaxTopK], dot[kMaxTopK];
+  int rows[K];
+  float g[K], dot[K];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
-    g[j] = j < k ? __ldg(gate + (size_t)t * k + j) : 0.f;
+  for (int j = 0; j < K; ++j) {
+    rows[j] = __ldg(row_of_slot + (size_t)t * K + j);
+    g[j] = __ldg(gate + (size_t)t * K + j);
     dot[j] = 0.f;
   }
   const uint16_t* src = dout + (size_t)t * d;
   for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
-    uint4 dv[U];
+    uint4 dv[U], yv[K][U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      int v = v0 + 32 * u;
+      const int v = v0 + 32 * u;
       if (v < nvec) dv[u] = ld_nc_v4(src + (size_t)v * 8);
     }
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
-        const uint16_t* yr = yp + (size_t)rows[j] * d;
-        uint16_t* dr = dyp + (size_t)rows[j] * d;
-        uint4 yv[U];
+    for (int j = 0; j < K; ++j) {
+      const uint16_t* yr = yp + (size_t)rows[j] * d;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          int v = v0 + 32 * u;
-          if (v < nvec) yv[u] = ld_nc_v4(yr + (size_t)v * 8);
-        }
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) yv[j][u] = ld_nc_v4(yr + (size_t)v * 8);
+      }
+    }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          int v = v0 + 32 * u;
-          if (v < nvec) {
-            dot[j] = dot8(dv[u], yv[u], dot[j]);
-            st_v4(dr + (size_t)v * 8, scale8(dv[u], g[j]));
-          }
+    for (int j = 0; j < K; ++j) {
+      uint16_t* dr = dyp + (size_t)rows[j] * d;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) {
+          dot[j] = dot8(dv[u], yv[j][u], dot[j]);
+          st_v4(dr + (size_t)v * 8, scale8(dv[u], g[j]));
         }
       }
     }
   }
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j < k) {
-      float s = warp_sum(dot[j]);
-      if (lane == 0) dgate[(size_t)t * k + j] = s;
-    }
+  for (int j = 0; j < K; ++j) {
+    const float s = warp_sum(dot[j]);
+    if (lane == 0) dgate[(size_t)t * K + j] = s;
   }
+}
+
+template <int K>
+void launch_combine_bwd(dim3 grid, cudaStream_t s, const uint16_t* dout, const uint16_t* yp,
+                        const int32_t* row_of_slot, const float* gate, int T, int d, uint16_t* dyp,
+                        float* dgate) {
+  // 8 to 16 row vectors of 16 bytes in flight a lane
+  constexpr int U = K <= 2 ? 8 : (K <= 4 ? 4 : 2);
+  combine_bwd_kernel<K, U><<<grid, kThreads, 0, s>>>(dout, yp, row_of_slot, gate, T, d, dyp, dgate);
 }
 
 }  // namespace
@@ -213,7 +223,10 @@ int moe_combine(const moe_bf16_t* yp, const int32_t* row_of_slot, const float* g
   MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(out);
   if (gate && !aligned16(gate)) return MOE_ERR_INVALID_ARG;
   dim3 grid((T + kWarps - 1) / kWarps);
-  combine_kernel<4><<<grid, kThreads, 0, (cudaStream_t)stream>>>(yp, row_of_slot, gate, T, k, d, out);
+  // 8 vectors a lane: a 2048-wide row in one pass.  (A copy specialised on k
+  // issues all k x 8 loads up front, needs 136 registers and runs 1.8x slower
+  // at one block per SM; this one stays at 127 and two blocks.)
+  combine_kernel<8><<<grid, kThreads, 0, (cudaStream_t)stream>>>(yp, row_of_slot, gate, T, k, d, out);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -226,8 +239,17 @@ int moe_combine_bwd(const moe_bf16_t* dout, const moe_bf16_t* yp, const int32_t*
   MOE_CHECK_PTR(dout); MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(gate);
   MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dgate);
   dim3 grid((T + kWarps - 1) / kWarps);
-  combine_bwd_kernel<4><<<grid, kThreads, 0, (cudaStream_t)stream>>>(dout, yp, row_of_slot, gate,
-                                                                     T, k, d, dyp, dgate);
+  const cudaStream_t s = (cudaStream_t)stream;
+  switch (k) {
+    case 1: launch_combine_bwd<1>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 2: launch_combine_bwd<2>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 3: launch_combine_bwd<3>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 4: launch_combine_bwd<4>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 5: launch_combine_bwd<5>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 6: launch_combine_bwd<6>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 7: launch_combine_bwd<7>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+    default: launch_combine_bwd<8>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
+  }
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
