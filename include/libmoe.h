@@ -219,11 +219,14 @@ int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets,
  * The weight gradients reduce over each expert's own row count (zero rows
  * give exactly zero).  dh1/dh3[R,h] are caller-provided intermediates (also
  * outputs).  dW1/dW3[E,d,h], dW2[E,h,d] bf16 from fp32 accumulators, no
- * split-K, deterministic.  The weight-gradient phase keeps five TMA
+ * atomics, deterministic.  The weight-gradient phase keeps five TMA
  * descriptors per expert in ws (bytes [256, 256 + 640 E)), written on the
- * device from offsets: for R > 0 ws must be 128-byte aligned
- * (MOE_ERR_INVALID_ARG) and ws_bytes >= moe_workspace_size(...)
- * (MOE_ERR_WORKSPACE). */
+ * device from offsets, and, when the last round of its 256 x 256 tiles would
+ * leave most SMs idle, splits those tiles along the rows into chunks whose
+ * fp32 partial sums (up to 80 tiles of 256 KB after the descriptors) are
+ * added in a fixed order.  For R > 0 ws must be 128-byte aligned
+ * (MOE_ERR_INVALID_ARG) and hold at least the descriptors (else
+ * MOE_ERR_WORKSPACE); moe_workspace_size(...) also covers the partials. */
 int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets,
                            int R, int E, int d, int h,
                            const moe_bf16_t* W1, const moe_bf16_t* W3,

@@ -87,6 +87,9 @@ def compare_full(layer, w, inp, backward=True):
     (2700, 192, 4, 2, 320, (2,)),       # pair tiles, ragged tails, one empty expert
     (2100, 256, 2, 1, 128, ()),         # pair tiles, one 128-wide hidden tile
     (1100, 128, 1, 1, 64, ()),          # last tile's odd CTA holds no rows
+    # the weight-gradient tiles split along the rows (fp32 partials, ordered
+    # sum) with an empty expert among them
+    (3000, 256, 3, 1, 256, (0,)),
 ])
 def test_layer_small_full_compare(T, d, E, k, h, empty):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)

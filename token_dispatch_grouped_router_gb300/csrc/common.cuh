@@ -40,7 +40,9 @@ constexpr int kMaxTopK = 8;
 //                                  then in-chunk stable ranks [R] int32;
 //              moe_router_logits_bwd: dW_r split-K partials [splits][d][E] f32;
 //              moe_grouped_swiglu_bwd(_wgrad): per-expert TMA descriptors
-//                                  [E][5] x 128 B (needs a 128-byte aligned ws).
+//                                  [E][5] x 128 B (needs a 128-byte aligned ws),
+//                                  then up to kWgradParts fp32 256 x 256
+//                                  partial tiles of the K-split last round.
 constexpr size_t kStatusBytes = 256;
 constexpr int kRouteChunk = 1024;     // slots per route-map block
 constexpr int kRouterSplits = 16;     // deterministic split-K for dW_r
@@ -63,12 +65,17 @@ inline size_t router_scratch_end(int E, int d) {
 }
 
 constexpr int kWgradMaps = 5;          // xp, a, dh1, dh3, dyp
+constexpr int kWgradParts = 80;        // fp32 256 x 256 partial tiles (20 MB)
 inline size_t wgrad_maps_end(int E) { return kStatusBytes + (size_t)E * kWgradMaps * 128; }
+inline size_t wgrad_parts_offset(int E) { return round_up(wgrad_maps_end(E), 256); }
+inline size_t wgrad_parts_end(int E) {
+  return wgrad_parts_offset(E) + (size_t)kWgradParts * 256 * 256 * 4;
+}
 
 inline size_t workspace_bytes(long long T, int E, int k, int d) {
   size_t a = route_scratch(T * (long long)k, E).end;
   size_t b = router_scratch_end(E, d);
-  size_t c = wgrad_maps_end(E);
+  size_t c = wgrad_parts_end(E);
   a = a > b ? a : b;
   return a > c ? a : c;
 }

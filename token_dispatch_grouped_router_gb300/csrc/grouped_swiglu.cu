@@ -61,13 +61,19 @@ struct GemmArgs {
   int ldo;                  // row stride (elements) of the row-grouped outputs
   int* status;
   int wg_t1, wg_t2;         // WG: tiles per expert of dW1 (= dW3) and of dW2
-  int wg_mt1, wg_mt2;       // WG: M tiles of dW1 (d/128) and dW2 (h/128)
+  int wg_mt1, wg_mt2;       // WG: M tiles of dW1 and dW2
   const CUtensorMap* wg_maps;  // WG: [E][5] descriptors of xp, a, dh1, dh3, dyp
                                //     whose row extent ends at the expert's last row
+  // WG on CTA pairs, K split of the last round: work units [0, wg_whole) are
+  // whole tiles; unit wg_whole + v is k-chunk v % wg_split of tile
+  // wg_whole + v / wg_split, accumulated in fp32 into wg_part[v] (256 x 256)
+  int wg_whole, wg_split, wg_units;
+  float* wg_part;
 };
 
 struct Tile {
   int e, row0, rows, m0, n0, nkb, which, krow0, krows;
+  int part;                 // WG pair units: fp32 partial slot, or -1 for a whole tile
 };
 
 using Shared = PipeShared<STAGES>;
@@ -457,7 +463,15 @@ template <int MODE>
 __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const int* s_off,
                                                  const int* s_ts) {
   Tile tl{};
+  tl.part = -1;
   if constexpr (MODE == kWG) {
+    int chunk = 0;
+    if (a.wg_split > 0 && t >= a.wg_whole) {
+      const int v = t - a.wg_whole;
+      tl.part = v;
+      chunk = v % a.wg_split;
+      t = a.wg_whole + v / a.wg_split;
+    }
     const int per = 2 * a.wg_t1 + a.wg_t2;
     tl.e = t / per;
     int l = t - tl.e * per;
@@ -473,6 +487,14 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const
     tl.krow0 = lo;
     tl.krows = hi - lo;
     tl.nkb = (tl.krows + BK - 1) / BK;
+    if (tl.part >= 0) {
+      // k-blocks [kb0, kb1) of the expert's rows
+      const int kc = (tl.nkb + a.wg_split - 1) / a.wg_split;
+      const int kb0 = min(tl.nkb, chunk * kc), kb1 = min(tl.nkb, kb0 + kc);
+      tl.krow0 = lo + kb0 * BK;
+      tl.krows = max(0, min(tl.krows - kb0 * BK, (kb1 - kb0) * BK));
+      tl.nkb = kb1 - kb0;
+    }
   } else {
     const RowTile r = decode_row_tile<P_TILE>(t, a.E, a.R, s_off, s_ts);
     tl.e = r.e;
@@ -518,6 +540,52 @@ __device__ __forceinline__ void issue_loads_pair(const Tile& tl, int kb, uint32_
   }
 }
 
+// A K-chunk of a split wgrad tile: this CTA's 128 rows x 256 columns of the
+// fp32 accumulator (zeros for an empty chunk) to partial slot tl.part; each
+// lane writes its row's 32 values of a chunk as 128 contiguous bytes.
+__device__ __forceinline__ void epilogue_partial(const Tile& tl, uint32_t tacc, int lane_q, int half,
+                                                 int lane, uint32_t rank, const GemmArgs& a) {
+  const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
+  const int row = 128 * (int)rank + lane_q * 32 + lane;
+  float* dst = a.wg_part + (size_t)tl.part * (P_TILE * P_TILE) + (size_t)row * P_TILE;
+#pragma unroll 1
+  for (int c = half * 4; c < half * 4 + 4; ++c) {
+    uint32_t q[32];
+    if (tl.nkb > 0) {
+      tmem_ld32(tbase + c * 32, q);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) q[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      st_v4(dst + c * 32 + 4 * i, make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]));
+  }
+}
+
+// Sum of the K-chunks of every split wgrad tile, in chunk order (so the
+// result does not depend on timing), rounded once to bf16.  Block = one row of
+// one split tile, thread = one column.
+__global__ void __launch_bounds__(P_TILE) wgrad_fixup_kernel(const GemmArgs a) {
+  const int i = blockIdx.x / P_TILE, r = blockIdx.x % P_TILE, col = threadIdx.x;
+  const int t = a.wg_whole + i;
+  const int per = 2 * a.wg_t1 + a.wg_t2;
+  const int e = t / per;
+  int l = t - e * per, which, mt;
+  if (l < a.wg_t1) { which = 0; mt = a.wg_mt1; }
+  else if (l < 2 * a.wg_t1) { which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
+  else { which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
+  const int m = (l % mt) * P_TILE + r, n = (l / mt) * P_TILE + col;
+  const int M = which == 2 ? a.h : a.d, N = which == 2 ? a.d : a.h;
+  if (m >= M || n >= N) return;
+  const float* src = a.wg_part + (size_t)i * a.wg_split * (P_TILE * P_TILE) + (size_t)r * P_TILE + col;
+  float acc = 0.f;
+  for (int c = 0; c < a.wg_split; ++c) acc += src[(size_t)c * (P_TILE * P_TILE)];
+  uint16_t* out = which == 0 ? a.out0 : (which == 1 ? a.out1 : a.out2);
+  out[((size_t)e * M + m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -554,7 +622,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   }
   __syncthreads();
   if constexpr (MODE == kWG) {
-    if (threadIdx.x == 0) sh->total_tiles = args.E * (2 * args.wg_t1 + args.wg_t2);
+    if (threadIdx.x == 0) sh->total_tiles = args.wg_units;
   } else {
     if (warp == 0) {
       const int n = build_row_tile_table<P_TILE>(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
@@ -686,8 +754,16 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
       }
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
-                          sStage + (warp - 2) * kStageBytes, args);
+      bool whole = true;
+      if constexpr (MODE == kWG) {
+        if (tl.part >= 0) {
+          epilogue_partial(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane, rank, args);
+          whole = false;
+        }
+      }
+      if (whole)
+        epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
+                            sStage + (warp - 2) * kStageBytes, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tempty[acc]), 0));
@@ -766,31 +842,40 @@ inline cudaLaunchConfig_t pair_config(int npairs, size_t smem, cudaStream_t s, c
   return cfg;
 }
 
-// Launches pair_gemm_kernel<MODE> on min(tiles_upper, co-resident pairs)
-// clusters.  The co-resident cluster count is queried once per device, on
-// the first call (outside any stream capture that follows).
+// Co-resident 2-CTA clusters of pair_gemm_kernel<MODE>, queried once per
+// device on the first call (outside any stream capture that follows).
 template <int MODE>
-int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                const CUtensorMap& b1, const GemmArgs& g, long long tiles_upper, cudaStream_t s) {
+int pair_limit(cudaStream_t s) {
   static_assert(MODE != kDA, "the DA GEMM runs on single CTAs");
   auto kern = pair_gemm_kernel<MODE>;
   static bool attr_done[64] = {false};
   static int limit[64] = {0};
-  if (ensure_smem_attr(kern, pair_smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
+  if (ensure_smem_attr(kern, pair_smem_bytes(kMaxExperts), attr_done) != MOE_OK) return -1;
   const int dev = current_device();
-  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  cudaLaunchAttribute at[1];
+  if (dev < 0 || dev >= 64) return -1;
   if (limit[dev] == 0) {
+    cudaLaunchAttribute at[1];
     cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes(kMaxExperts), s, at);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
-      return MOE_ERR_CUDA;
+      return -1;
     }
     limit[dev] = n;
   }
+  return limit[dev];
+}
+
+// Launches pair_gemm_kernel<MODE> on min(tiles_upper, co-resident pairs) clusters.
+template <int MODE>
+int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                const CUtensorMap& b1, const GemmArgs& g, long long tiles_upper, cudaStream_t s) {
+  auto kern = pair_gemm_kernel<MODE>;
+  const int limit = pair_limit<MODE>(s);
+  if (limit <= 0) return MOE_ERR_CUDA;
+  cudaLaunchAttribute at[1];
   const long long ub = tiles_upper > 0 ? tiles_upper : 1;
-  const int npairs = (int)(ub < limit[dev] ? ub : limit[dev]);
+  const int npairs = (int)(ub < limit ? ub : limit);
   cudaLaunchConfig_t cfg = pair_config(npairs, pair_smem_bytes(g.E), s, at);
   if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, g) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -938,7 +1023,32 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   g.wg_t1 = g.wg_mt1 * ((h + P_TILE - 1) / P_TILE);
   g.wg_t2 = g.wg_mt2 * ((d + P_TILE - 1) / P_TILE);
   const long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
-  return launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], g, tiles, s);
+  // The pairs take whole tiles round-robin.  When the last round would keep
+  // at most half of them busy, its L tiles are split along K into S chunks
+  // (L * S <= pairs, 4 or more k-blocks a chunk on average) whose fp32 partial
+  // sums a second kernel adds in chunk order.
+  const int P = pair_limit<kWG>(s);
+  if (P <= 0) return MOE_ERR_CUDA;
+  const long long L = tiles % P;
+  g.wg_whole = (int)(tiles - L);
+  g.wg_split = 0;
+  g.wg_units = (int)tiles;
+  if (L > 0 && 2 * L <= P && ws_bytes >= wgrad_parts_end(E)) {
+    long long S = P / L;
+    S = S < kWgradParts / L ? S : kWgradParts / L;
+    const long long k_blocks = (long long)R / ((long long)E * BK);   // per expert, on average
+    S = S < k_blocks / 4 ? S : k_blocks / 4;
+    if (S >= 2) {
+      g.wg_split = (int)S;
+      g.wg_units = (int)(g.wg_whole + L * S);
+      g.wg_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wgrad_parts_offset(E));
+    }
+  }
+  const int st = launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], g, g.wg_units, s);
+  if (st != MOE_OK || g.wg_split == 0) return st;
+  wgrad_fixup_kernel<<<(unsigned)(L * P_TILE), P_TILE, 0, s>>>(g);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
 }
 
 }  // namespace
