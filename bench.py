@@ -298,6 +298,12 @@ def run_ours(args):
         res = timed_layer(layer, K, W, sample_clocks=sample_clocks)
         if with_e2e:
             res["e2e"] = e2e(layer, inp, K)
+            # the recompute policy (Xp gathered again, H1/H3/A recomputed in
+            # the backward): time against activation memory
+            layer.recompute = True
+            res["recompute"] = timed_layer(layer, K, W)
+            res["recompute"]["activation_bytes"] = layer.activation_bytes()
+            layer.recompute = False
         del layer
         torch.cuda.empty_cache()
         return res
@@ -423,6 +429,14 @@ def run_ours(args):
         "gpu_launches": main["launches"],
         "clocks": main["clocks"],
     }
+    rec = main["recompute"]
+    out["recompute"] = {
+        "value": throughput(w.T, world, rec["ms_per_step"]), "unit": UNIT,
+        "ms_per_step": rec["ms_per_step"], "ratio_to_main": ms / rec["ms_per_step"],
+        "activation_bytes_kept": rec["activation_bytes"],
+        "extra_ms": {k: rec["kernels_ms"][k] for k in ("dispatch_recompute", "gemm_up_recompute")},
+        "note": "backward gathers Xp from x again and recomputes H1/H3/A; only x, routing and Yp "
+                "live from forward to backward"}
     if cmp_res is not None:
         cv = world * wl.get_workload(args.compare).T / (cmp_res["ms_per_step"] / 1e3)
         out["compare"] = {"workload": cmp_res["workload"], "value": cv, "unit": UNIT,

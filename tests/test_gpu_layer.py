@@ -161,6 +161,29 @@ def test_deterministic_bitwise(T, E):
         assert torch.equal(getattr(layer, n), v), n
 
 
+@pytest.mark.parametrize("T,E", [(2000, 16), (2048, 4)])   # single-CTA / CTA-pair row GEMMs
+def test_recompute_backward_matches_saved_bitwise(T, E):
+    # the recompute policy gathers Xp again and recomputes H1, H3, A in the
+    # backward; with those buffers poisoned after the forward it must still
+    # reproduce the saved-activation step bit for bit
+    w = wl.small_workload(T=T, d=256, E=E, k=4, h=256)
+    inp = wl.generate(w, seed=7)
+    layer = make_layer(w, inp)
+    run(layer)
+    names = ("out", "dgate", "dh1", "dh3", "dxp", "dW1", "dW3", "dW2", "dX")
+    saved = {n: getattr(layer, n).clone() for n in names}
+    layer.recompute = True
+    L.moe_reset_status(layer.ws)
+    layer.forward()
+    for n in ("xp", "h1", "h3", "a"):
+        getattr(layer, n).fill_(float("nan"))
+    layer.backward()
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    for n, v in saved.items():
+        assert torch.equal(getattr(layer, n), v), n
+
+
 @pytest.mark.parametrize("T,E", [(333, 5), (1400, 2)])    # single-CTA / CTA-pair row GEMMs
 def test_outputs_stay_inside_their_buffers(T, E):
     # every output is a view at the front of a larger buffer whose tail holds a

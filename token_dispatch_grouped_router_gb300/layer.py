@@ -6,8 +6,14 @@ entry points:
 
 forward : [router_logits ->] router_topk | router_gates -> expert_offsets ->
           dispatch_rows -> grouped_swiglu_fwd (up, down) -> combine
-backward: combine_bwd -> grouped_swiglu_bwd (dact, dx, wgrad) -> combine(gates = None) ->
+backward: [dispatch_rows -> grouped_swiglu_fwd_up (recompute)] -> combine_bwd ->
+          grouped_swiglu_bwd (dact, dx, wgrad) -> combine(gates = None) ->
           router_topk_bwd [-> router_logits_bwd]
+
+With ``recompute=True`` the backward does not use the expert rows Xp or the
+SwiGLU intermediates H1, H3, A left by the forward: it gathers the rows again
+from x and recomputes H1, H3, A from them, so that only x, the routing and Yp
+(for the gate gradient) have to live from the forward to the backward.
 
 Nothing is copied back to the host and nothing waits on the host.
 """
@@ -40,11 +46,12 @@ class MoELayer:
     """Buffers and call sequence of one MoE layer step on one GPU."""
 
     def __init__(self, T: int, d: int, E: int, k: int, h: int, learned: bool,
-                 device="cuda", with_backward: bool = True):
+                 device="cuda", with_backward: bool = True, recompute: bool = False):
         self.T, self.d, self.E, self.k, self.h = T, d, E, k, h
         self.R = T * k
         self.learned = learned
         self.with_backward = with_backward
+        self.recompute = recompute
         dev = torch.device(device)
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
         e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
@@ -140,6 +147,12 @@ class MoELayer:
     # ----------------------------------------------------------- backward
     def backward(self, mark=None) -> None:
         mark = mark or _nomark
+        if self.recompute:
+            mark("dispatch_recompute")
+            L.moe_dispatch_rows(self.x, self.row_of_slot, self.k, self.xp)
+            mark("gemm_up_recompute")
+            L.moe_grouped_swiglu_fwd_up(self.xp, self.offsets, self.W1, self.W3, self.h1,
+                                        self.h3, self.a, self.ws)
         mark("combine_bwd")
         L.moe_combine_bwd(self.dY, self.yp, self.row_of_slot, self.gate, self.k,
                           self.dyp, self.dgate)
@@ -213,8 +226,9 @@ class MoELayer:
         if mark is not None:
             mark("end")
 
-    def launches_per_step(self) -> int:
-        n = (2 if self.learned and not self.logits_given else 1) + 3 + 1 + 2 + 1   # forward
-        if self.with_backward:
-            n += 1 + 3 + 1 + 1 + (4 if self.learned else 0)
-        return n
+    def activation_bytes(self) -> Dict[str, int]:
+        """Bytes the forward leaves for the backward, by policy: the expert
+        rows Xp and H1, H3, A when saved; Yp, the routing and x in both."""
+        R, d, h, T, k, E = self.R, self.d, self.h, self.T, self.k, self.E
+        common = 2 * R * d + 2 * T * d + 4 * (3 * T * k + 2 * R + 2 * E + 1)
+        return {"saved": common + 2 * R * d + 3 * 2 * R * h, "recompute": common}
