@@ -79,32 +79,32 @@ route_count_kernel(const int32_t* __restrict__ idx, int R, int E,
   }
 }
 
-// Single block of 1024 threads.
+// Single block of 1024 threads.  Warp w scans the block histograms of experts
+// w, w + 32, ... over the chunks, 32 chunks a step (one per lane, a warp
+// prefix sum, the running total carried in a register).
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   __shared__ int32_t tot[kMaxExperts];
   __shared__ int32_t warp_sums[32];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    int b = 0;
-    for (; b + 4 <= nchunks; b += 4) {
-      int c0 = chunk_counts[(size_t)(b + 0) * E + e];
-      int c1 = chunk_counts[(size_t)(b + 1) * E + e];
-      int c2 = chunk_counts[(size_t)(b + 2) * E + e];
-      int c3 = chunk_counts[(size_t)(b + 3) * E + e];
-      chunk_counts[(size_t)(b + 0) * E + e] = run; run += c0;
-      chunk_counts[(size_t)(b + 1) * E + e] = run; run += c1;
-      chunk_counts[(size_t)(b + 2) * E + e] = run; run += c2;
-      chunk_counts[(size_t)(b + 3) * E + e] = run; run += c3;
+  {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = warp; e < E; e += 32) {
+      int carry = 0;
+      for (int b0 = 0; b0 < nchunks; b0 += 32) {
+        const int b = b0 + lane;
+        const int c = b < nchunks ? chunk_counts[(size_t)b * E + e] : 0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (b < nchunks) chunk_counts[(size_t)b * E + e] = carry + incl - c;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) { tot[e] = carry; counts[e] = carry; }
     }
-    for (; b < nchunks; ++b) {
-      int c = chunk_counts[(size_t)b * E + e];
-      chunk_counts[(size_t)b * E + e] = run;
-      run += c;
-    }
-    tot[e] = run;
-    counts[e] = run;
   }
   __syncthreads();
   // exclusive scan of tot[0..E) -> offsets (E <= 1024: one element per thread)
