@@ -130,6 +130,10 @@ def _mx_layer(w, inp):
     (300, 256, 6, 2, 384, (2,)),       # ragged rows, three 128-column blocks of h
     (1000, 512, 16, 4, 256, (0, 15)),
     (64, 128, 1, 1, 128, ()),
+    # several 128-row tiles per expert, ragged tails
+    (1500, 256, 2, 1, 384, ()),
+    (2600, 512, 4, 2, 256, (1,)),
+    (700, 128, 1, 1, 128, ()),
 ])
 def test_grouped_forward_mxfp8_small(T, d, E, k, h, empty):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
