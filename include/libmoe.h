@@ -305,7 +305,9 @@ int moe_dispatch_rows_mxfp8(const moe_bf16_t* x, int T, int d, int k,
  * a = silu(h1) * h3 (bf16 h1, h3, a for the bf16 backward), a quantised along
  * h into aq[R][h] / as[R][h/32], yp = Aq_e W2q[e] (bf16).  Weights come from
  * moe_mxfp8_quantize_weights (w1q/w3q [E][h][d], w2q [E][d][h]).  d and h
- * must be multiples of 128. */
+ * must be multiples of 128 and E <= 768 (MOE_ERR_UNSUPPORTED otherwise: the
+ * kernels keep an E-sized tile table beside 128 x 256 operand tiles in shared
+ * memory). */
 int moe_grouped_swiglu_fwd_mxfp8(const uint8_t* xq, const uint8_t* xs,
                                  const int32_t* offsets, int R, int E, int d, int h,
                                  const uint8_t* w1q, const uint8_t* w1s,

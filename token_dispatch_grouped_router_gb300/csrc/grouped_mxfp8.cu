@@ -9,17 +9,24 @@
 // accumulate in fp32; outputs are bf16 (the backward stays bf16).
 //
 // Two modes of one persistent kernel, same warp roles as the bf16 kernel:
-//   UP8  : [h1 | h3] = Xq_e @ [W1q[e] | W3q[e]]  (64 + 64 columns per tile);
+//   UP8  : [h1 | h3] = Xq_e @ [W1q[e] | W3q[e]]  (128 + 128 columns per tile);
 //          epilogue writes h1, h3, a = silu(h1) * h3 (bf16) and quantises a
 //          (one 32-column block per thread: Aq codes + As scale bytes)
 //   DOWN8: yp = Aq_e @ W2q[e]
-// Tiles are 128 x 128 with BK = 128 fp8 (one 128-byte swizzled row per
-// operand row), 5 pipeline stages.  Operands are K-major: activations
+// Tiles are 128 x 256 with BK = 128 fp8 (one 128-byte swizzled row per
+// operand row), 4 pipeline stages.  Operands are K-major: activations
 // [R][K], weights [E][N][K] (moe_mxfp8_quantize_weights transposes).
-// Scale factors: per stage a 512-byte atom per operand, byte (r, 4j + k) =
-// scale of row 32j + r for the stage's k-th 32-element block, gathered by the
-// producer warp with zero-filling cp.async (row-major scales in HBM) and moved
-// to tensor memory with tcgen05.cp .32x128b.warpx4 (which replicates the atom
+// Block-scaled MMAs of N = 256 run at the full fp8 rate with their scale
+// copies hidden, while at N = 128 the per-k-block copies cost about a third
+// (measured on the GB300 with operands resident in shared memory); a 128 x
+// 256 fp32 accumulator takes 256 TMEM columns, so the tile has one
+// accumulator (the epilogue does not overlap the next tile's mainloop) and
+// the other columns hold the scale factors.
+// Scale factors: per stage 512-byte atoms, byte (r, 4j + k) = scale of row
+// (or column) 32j + r of the atom for the stage's k-th 32-element block, one
+// for A and two for B (columns 0-127 and 128-255), gathered by the producer
+// warp with zero-filling cp.async (row-major scales in HBM) and moved to
+// tensor memory with tcgen05.cp .32x128b.warpx4 (which replicates an atom
 // into the four lane quarters).  The MMA then reads row m's A scale at lane
 // m, column base + m/32, and column n's B scale at lane n%32 of the issuing
 // quarter, column base + n/32, byte = the MMA's scale-factor id (0..3).
@@ -34,13 +41,14 @@ using namespace gemm;
 
 enum Mode8 : int { kUp8 = 0, kDown8 = 1 };
 
-constexpr int BM = 128, BN = 128, BK = 128, STAGES = 5;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
 constexpr int A_STAGE = BM * BK;                // 16 KB of E4M3
-constexpr int B_STAGE = BN * BK;                // 16 KB
-constexpr int SF_STAGE = 1024;                  // A atom + B atom
-constexpr int kAccCols = 2 * BN;                // two accumulators
-constexpr int kSfCol0 = kAccCols;               // stage s: A at +8s, B at +8s+4
+constexpr int B_STAGE = BN * BK;                // 32 KB
+constexpr int SF_STAGE = 1536;                  // A atom + two B atoms
+constexpr int kAccCols = BN;                    // one accumulator
+constexpr int kSfCol0 = kAccCols;               // stage s: A at +12s, B at +12s+4 (8 columns)
 constexpr int kTmemCols = 512;
+constexpr int kMaxExperts8 = 768;               // shared-memory tile table bound
 
 struct Args8 {
   const int32_t* offsets;
@@ -108,45 +116,49 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
   const int nrows = min(32, rt.rows - lane_q * 32);
   const size_t r0 = (size_t)rt.row0 + (nrows > 0 ? lane_q * 32 : 0);
   if constexpr (MODE == kUp8) {
-    // columns 0..63: h1[:, n0..n0+63]; 64..127: h3[:, n0..n0+63]
-    const int c = half;                            // 32-column chunk of this warp
-    uint32_t q1[32], q3[32];
-    tmem_ld32(tbase + c * 32, q1);
-    tmem_ld32(tbase + 64 + c * 32, q3);
-    tmem_ld_wait();
-    const int col = n0 + c * 32;
-    float h1[32], h3[32], av[32];
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      h1[i] = __uint_as_float(q1[i]);
-      h3[i] = __uint_as_float(q3[i]);
-      av[i] = silu_f(h1[i]) * h3[i];
-      amax = fmaxf(amax, fabsf(av[i]));
-    }
-    store_chunk(stg, h1, lane, a.out0 + r0 * a.h + col, a.h, nrows);
-    store_chunk(stg, h3, lane, a.out1 + r0 * a.h + col, a.h, nrows);
-    store_chunk(stg, av, lane, a.out2 + r0 * a.h + col, a.h, nrows);
-    // quantise this row's 32-column block of a (fp32 values, before rounding)
-    const int ex = mx::block_exponent(amax);
-    const float inv = mx::inv_scale(ex);
-    uint4 o[2];
-    uint32_t* w = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      w[i] = mx::e4m3x4(av[4 * i] * inv, av[4 * i + 1] * inv, av[4 * i + 2] * inv, av[4 * i + 3] * inv);
-    store_chunk_bytes32(stg, o, lane, a.aq + r0 * a.h + col, a.h, nrows);
-    if (lane < nrows) a.as[(r0 + lane) * (a.h / 32) + col / 32] = (uint8_t)(ex + 127);
-  } else {
+    // columns 0..127: h1[:, n0..n0+127]; 128..255: h3[:, n0..n0+127]
 #pragma unroll 1
     for (int c = half * 2; c < half * 2 + 2; ++c) {
+      uint32_t q1[32], q3[32];
+      tmem_ld32(tbase + c * 32, q1);
+      tmem_ld32(tbase + 128 + c * 32, q3);
+      tmem_ld_wait();
+      const int col = n0 + c * 32;
+      float h1[32], h3[32], av[32];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        h1[i] = __uint_as_float(q1[i]);
+        h3[i] = __uint_as_float(q3[i]);
+        av[i] = silu_f(h1[i]) * h3[i];
+        amax = fmaxf(amax, fabsf(av[i]));
+      }
+      store_chunk(stg, h1, lane, a.out0 + r0 * a.h + col, a.h, nrows);
+      store_chunk(stg, h3, lane, a.out1 + r0 * a.h + col, a.h, nrows);
+      store_chunk(stg, av, lane, a.out2 + r0 * a.h + col, a.h, nrows);
+      // quantise this row's 32-column block of a (fp32 values, before rounding)
+      const int ex = mx::block_exponent(amax);
+      const float inv = mx::inv_scale(ex);
+      uint4 o[2];
+      uint32_t* w = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = mx::e4m3x4(av[4 * i] * inv, av[4 * i + 1] * inv, av[4 * i + 2] * inv, av[4 * i + 3] * inv);
+      store_chunk_bytes32(stg, o, lane, a.aq + r0 * a.h + col, a.h, nrows);
+      if (lane < nrows) a.as[(r0 + lane) * (a.h / 32) + col / 32] = (uint8_t)(ex + 127);
+    }
+  } else {
+#pragma unroll 1
+    for (int c = half * 4; c < half * 4 + 4; ++c) {
+      const int col = n0 + c * 32;
+      if (col >= a.d) break;                      // warp-uniform
       uint32_t q[32];
       tmem_ld32(tbase + c * 32, q);
       tmem_ld_wait();
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(q[i]);
-      store_chunk(stg, v, lane, a.out0 + r0 * a.d + n0 + c * 32, a.d, nrows);
+      store_chunk(stg, v, lane, a.out0 + r0 * a.d + col, a.d, nrows);
     }
   }
 }
@@ -214,13 +226,17 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
           tma_load_2d(sa, &tmA, fb, kb * BK, rt.row0);
           if constexpr (MODE == kUp8) {
+            // 128 rows of W1 then the same 128 rows of W3, 64-row boxes
             tma_load_3d(sb, &tmB0, fb, kb * BK, n0, rt.e);
-            tma_load_3d(sb + 64 * BK, &tmB1, fb, kb * BK, n0, rt.e);
+            tma_load_3d(sb + 64 * BK, &tmB0, fb, kb * BK, n0 + 64, rt.e);
+            tma_load_3d(sb + 128 * BK, &tmB1, fb, kb * BK, n0, rt.e);
+            tma_load_3d(sb + 192 * BK, &tmB1, fb, kb * BK, n0 + 64, rt.e);
           } else {
             tma_load_3d(sb, &tmB0, fb, kb * BK, n0, rt.e);
           }
         }
-        // scale atoms: this lane gathers rows 32j + lane (j = 0..3) of A and B
+        // scale atoms: this lane gathers rows 32j + lane (j = 0..3) of A and
+        // columns 32j + lane of each 128-column half of B
         const uint32_t sfa_s = smem_u32(sSF + stage * SF_STAGE);
         const uint32_t sfb_s = sfa_s + 512;
 #pragma unroll
@@ -229,14 +245,20 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           const bool v = row < args.R;
           cp_async4(sfa_s + 16 * lane + 4 * j,
                     args.sfa + (size_t)(v ? row : 0) * ksf + kb * 4, v);
-          const uint8_t* bsrc;
-          if constexpr (MODE == kUp8) {
-            const int n = n0 + 32 * (j & 1) + lane;
-            bsrc = (j < 2 ? args.sfb0 : args.sfb1) + ((size_t)rt.e * args.N + n) * ksf + kb * 4;
-          } else {
-            bsrc = args.sfb0 + ((size_t)rt.e * args.N + n0 + 32 * j + lane) * ksf + kb * 4;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint8_t* bsrc;
+            bool bv = true;
+            if constexpr (MODE == kUp8) {
+              const int n = n0 + 32 * j + lane;                  // < h: h % 128 == 0
+              bsrc = (hb == 0 ? args.sfb0 : args.sfb1) + ((size_t)rt.e * args.N + n) * ksf + kb * 4;
+            } else {
+              const int n = n0 + 128 * hb + 32 * j + lane;
+              bv = n < args.N;
+              bsrc = args.sfb0 + ((size_t)rt.e * args.N + (bv ? n : 0)) * ksf + kb * 4;
+            }
+            cp_async4(sfb_s + 512 * hb + 16 * lane + 4 * j, bsrc, bv);
           }
-          cp_async4(sfb_s + 16 * lane + 4 * j, bsrc, true);
         }
         cp_async_arrive_noinc(fb);
         __syncwarp();
@@ -258,7 +280,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t dt = tmem + (uint32_t)(acc * BN);
+      const uint32_t dt = tmem;
       for (int kb = 0; kb < args.kb_total; ++kb) {
         if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
@@ -266,10 +288,11 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           // the scale bytes were written by cp.async (generic proxy); make them
           // visible to the tensor core's async proxy before tcgen05.cp reads them
           fence_proxy_async_smem();
-          const uint32_t sfa_t = tmem + kSfCol0 + 8 * stage, sfb_t = sfa_t + 4;
+          const uint32_t sfa_t = tmem + kSfCol0 + 12 * stage, sfb_t = sfa_t + 4;
           const uint32_t sf_s = smem_u32(sSF + stage * SF_STAGE);
           tmem_cp_warpx4(sfa_t, sdesc_atom(sf_s));
-          tmem_cp_warpx4(sfb_t, sdesc_atom(sf_s + 512));
+          tmem_cp_warpx4(sfb_t, sdesc_atom(sf_s + 512));          // B columns 0..127
+          tmem_cp_warpx4(sfb_t + 4, sdesc_atom(sf_s + 1024));     // B columns 128..255
           const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
@@ -286,7 +309,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       if (!ok) break;
       if (lane == 0) mma_commit(smem_u32(&sh->tfull[acc]));
       __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      acc_phase ^= 1u;                      // one accumulator: acc stays 0
     }
     if (!ok && issued_any && lane == 0) {
       mma_commit(smem_u32(&sh->drain));
@@ -304,11 +327,11 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       const int n0 = rt.n_idx * (MODE == kUp8 ? BN / 2 : BN);
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue8<MODE>(rt, n0, tmem + (uint32_t)(acc * BN), lane_q, half, lane, stg, args);
+      epilogue8<MODE>(rt, n0, tmem, lane_q, half, lane, stg, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      acc_phase ^= 1u;
     }
   }
 
@@ -330,7 +353,7 @@ int launch8(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, 
             int grid, cudaStream_t s) {
   auto kern = grouped_mxfp8_kernel<MODE>;
   static bool attr_done[64] = {false};
-  if (ensure_smem_attr(kern, smem_bytes8(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
+  if (ensure_smem_attr(kern, smem_bytes8(kMaxExperts8), attr_done) != MOE_OK) return MOE_ERR_CUDA;
   kern<<<grid, kThreads, smem_bytes8(args.E), s>>>(a, b0, b1, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
@@ -348,7 +371,7 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
     const uint8_t* w2q, const uint8_t* w2s, moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a,
     uint8_t* aq, uint8_t* as, moe_bf16_t* yp, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (R < 0 || E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
-  if (d % 128 != 0 || h % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d % 128 != 0 || h % 128 != 0 || E > kMaxExperts8) return MOE_ERR_UNSUPPORTED;
   if (ws == nullptr || ws_bytes < kStatusBytes) return MOE_ERR_WORKSPACE;
   if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (R == 0) return MOE_OK;
@@ -363,19 +386,19 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   CUtensorMap mx, mw1, mw3, ma, mw2;
   if (!map2d(&mx, xq, d, R, BK, BM, U8, 1) || !map3d(&mw1, w1q, d, h, E, BK, 64, U8, 1) ||
       !map3d(&mw3, w3q, d, h, E, BK, 64, U8, 1) || !map2d(&ma, aq, h, R, BK, BM, U8, 1) ||
-      !map3d(&mw2, w2q, h, d, E, BK, BN, U8, 1))
+      !map3d(&mw2, w2q, h, d, E, BK, BN, U8, 1))   // 256-row box of W2^T
     return MOE_ERR_CUDA;
   Args8 g{};
   g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
-  // up-projection: K = d, 64 columns of W1 and of W3 per tile
-  g.K = d; g.kb_total = d / BK; g.n_tiles = h / 64; g.N = h;
+  // up-projection: K = d, 128 columns of W1 and of W3 per tile
+  g.K = d; g.kb_total = d / BK; g.n_tiles = h / 128; g.N = h;
   g.sfa = xs; g.sfb0 = w1s; g.sfb1 = w3s;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.aq = aq; g.as = as;
   int st = launch8<kUp8>(mx, mw1, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
   if (st != MOE_OK) return st;
   // down-projection: K = h
   Args8 g2 = g;
-  g2.K = h; g2.kb_total = h / BK; g2.n_tiles = d / BN; g2.N = d;
+  g2.K = h; g2.kb_total = h / BK; g2.n_tiles = (d + BN - 1) / BN; g2.N = d;
   g2.sfa = as; g2.sfb0 = w2s; g2.sfb1 = w2s;
   g2.out0 = yp; g2.out1 = nullptr; g2.out2 = nullptr; g2.aq = nullptr; g2.as = nullptr;
   return launch8<kDown8>(ma, mw2, mw2, g2, row_grid_upper(R, E, g2.n_tiles), s);
