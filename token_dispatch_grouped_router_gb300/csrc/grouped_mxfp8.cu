@@ -9,22 +9,22 @@
 // accumulate in fp32; outputs are bf16 (the backward stays bf16).
 //
 // Two modes of one persistent kernel, same warp roles as the bf16 kernel:
-//   UP8  : [h1 | h3] = Xq_e @ [W1q[e] | W3q[e]]  (128 + 128 columns per tile);
+//   UP8  : [h1 | h3] = Xq_e @ [W1q[e] | W3q[e]]  (96 + 96 columns per tile);
 //          epilogue writes h1, h3, a = silu(h1) * h3 (bf16) and quantises a
 //          (one 32-column block per thread: Aq codes + As scale bytes)
 //   DOWN8: yp = Aq_e @ W2q[e]
-// Tiles are 128 x 256 with BK = 128 fp8 (one 128-byte swizzled row per
+// Tiles are 128 x 192 with BK = 128 fp8 (one 128-byte swizzled row per
 // operand row), 4 pipeline stages.  Operands are K-major: activations
 // [R][K], weights [E][N][K] (moe_mxfp8_quantize_weights transposes).
-// Block-scaled MMAs of N = 256 run at the full fp8 rate with their scale
-// copies hidden, while at N = 128 the per-k-block copies cost about a third
-// (measured on the GB300 with operands resident in shared memory); a 128 x
-// 256 fp32 accumulator takes 256 TMEM columns, so the tile has one
-// accumulator (the epilogue does not overlap the next tile's mainloop) and
-// the other columns hold the scale factors.
+// Issue rates of block-scaled MMAs with their per-k-block scale copies,
+// measured on the GB300 with operands resident in shared memory: N = 256 runs
+// at the full fp8 rate, N = 192 at 93% and N = 128 at 65-68%.  Two 192-column
+// fp32 accumulators (at TMEM columns 0 and 256) leave room for the scale
+// factors, so the epilogue of one tile overlaps the next tile's mainloop
+// (a 256-column tile would fit only one accumulator).
 // Scale factors: per stage 512-byte atoms, byte (r, 4j + k) = scale of row
 // (or column) 32j + r of the atom for the stage's k-th 32-element block, one
-// for A and two for B (columns 0-127 and 128-255), gathered by the producer
+// for A and two for B (columns 0-127 and 128-191), gathered by the producer
 // warp with zero-filling cp.async (row-major scales in HBM) and moved to
 // tensor memory with tcgen05.cp .32x128b.warpx4 (which replicates an atom
 // into the four lane quarters).  The MMA then reads row m's A scale at lane
@@ -41,12 +41,12 @@ using namespace gemm;
 
 enum Mode8 : int { kUp8 = 0, kDown8 = 1 };
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 192, BK = 128, STAGES = 4;
 constexpr int A_STAGE = BM * BK;                // 16 KB of E4M3
-constexpr int B_STAGE = BN * BK;                // 32 KB
+constexpr int B_STAGE = BN * BK;                // 24 KB
 constexpr int SF_STAGE = 1536;                  // A atom + two B atoms
-constexpr int kAccCols = BN;                    // one accumulator
-constexpr int kSfCol0 = kAccCols;               // stage s: A at +12s, B at +12s+4 (8 columns)
+constexpr int kAccStride = 256;                 // accumulators at TMEM columns 0 and 256
+constexpr int kSfCol0 = 448;                    // stage s: A at +12s, B at +12s+4 (8 columns)
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts8 = 768;               // shared-memory tile table bound
 
@@ -116,14 +116,16 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
   const int nrows = min(32, rt.rows - lane_q * 32);
   const size_t r0 = (size_t)rt.row0 + (nrows > 0 ? lane_q * 32 : 0);
   if constexpr (MODE == kUp8) {
-    // columns 0..127: h1[:, n0..n0+127]; 128..255: h3[:, n0..n0+127]
+    // columns 0..95: h1[:, n0..n0+95]; 96..191: h3[:, n0..n0+95]; three
+    // 32-column chunks, two for the first half of the warps, one for the second
 #pragma unroll 1
-    for (int c = half * 2; c < half * 2 + 2; ++c) {
+    for (int c = half * 2; c < min(half * 2 + 2, 3); ++c) {
+      const int col = n0 + c * 32;
+      if (col >= a.h) break;                      // warp-uniform
       uint32_t q1[32], q3[32];
       tmem_ld32(tbase + c * 32, q1);
-      tmem_ld32(tbase + 128 + c * 32, q3);
+      tmem_ld32(tbase + 96 + c * 32, q3);
       tmem_ld_wait();
-      const int col = n0 + c * 32;
       float h1[32], h3[32], av[32];
       float amax = 0.f;
 #pragma unroll
@@ -149,7 +151,7 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
     }
   } else {
 #pragma unroll 1
-    for (int c = half * 4; c < half * 4 + 4; ++c) {
+    for (int c = half * 3; c < half * 3 + 3; ++c) {
       const int col = n0 + c * 32;
       if (col >= a.d) break;                      // warp-uniform
       uint32_t q[32];
@@ -226,17 +228,15 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
           tma_load_2d(sa, &tmA, fb, kb * BK, rt.row0);
           if constexpr (MODE == kUp8) {
-            // 128 rows of W1 then the same 128 rows of W3, 64-row boxes
+            // 96 rows of W1 then the same 96 rows of W3
             tma_load_3d(sb, &tmB0, fb, kb * BK, n0, rt.e);
-            tma_load_3d(sb + 64 * BK, &tmB0, fb, kb * BK, n0 + 64, rt.e);
-            tma_load_3d(sb + 128 * BK, &tmB1, fb, kb * BK, n0, rt.e);
-            tma_load_3d(sb + 192 * BK, &tmB1, fb, kb * BK, n0 + 64, rt.e);
+            tma_load_3d(sb + 96 * BK, &tmB1, fb, kb * BK, n0, rt.e);
           } else {
             tma_load_3d(sb, &tmB0, fb, kb * BK, n0, rt.e);
           }
         }
         // scale atoms: this lane gathers rows 32j + lane (j = 0..3) of A and
-        // columns 32j + lane of each 128-column half of B
+        // columns 128hb + 32j + lane (< 192) of B
         const uint32_t sfa_s = smem_u32(sSF + stage * SF_STAGE);
         const uint32_t sfb_s = sfa_s + 512;
 #pragma unroll
@@ -247,17 +247,15 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     args.sfa + (size_t)(v ? row : 0) * ksf + kb * 4, v);
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
-            const uint8_t* bsrc;
-            bool bv = true;
+            const int c = 128 * hb + 32 * j + lane;               // tile column
+            const uint8_t* tab = args.sfb0;
+            int n = n0 + c;
             if constexpr (MODE == kUp8) {
-              const int n = n0 + 32 * j + lane;                  // < h: h % 128 == 0
-              bsrc = (hb == 0 ? args.sfb0 : args.sfb1) + ((size_t)rt.e * args.N + n) * ksf + kb * 4;
-            } else {
-              const int n = n0 + 128 * hb + 32 * j + lane;
-              bv = n < args.N;
-              bsrc = args.sfb0 + ((size_t)rt.e * args.N + (bv ? n : 0)) * ksf + kb * 4;
+              if (c >= BN / 2) { tab = args.sfb1; n -= BN / 2; }  // W3 half
             }
-            cp_async4(sfb_s + 512 * hb + 16 * lane + 4 * j, bsrc, bv);
+            const bool bv = c < BN && n < args.N;
+            cp_async4(sfb_s + 512 * hb + 16 * lane + 4 * j,
+                      tab + ((size_t)rt.e * args.N + (bv ? n : 0)) * ksf + kb * 4, bv);
           }
         }
         cp_async_arrive_noinc(fb);
@@ -280,7 +278,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t dt = tmem;
+      const uint32_t dt = tmem + (uint32_t)(acc * kAccStride);
       for (int kb = 0; kb < args.kb_total; ++kb) {
         if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
@@ -292,7 +290,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           const uint32_t sf_s = smem_u32(sSF + stage * SF_STAGE);
           tmem_cp_warpx4(sfa_t, sdesc_atom(sf_s));
           tmem_cp_warpx4(sfb_t, sdesc_atom(sf_s + 512));          // B columns 0..127
-          tmem_cp_warpx4(sfb_t + 4, sdesc_atom(sf_s + 1024));     // B columns 128..255
+          tmem_cp_warpx4(sfb_t + 4, sdesc_atom(sf_s + 1024));     // B columns 128..191
           const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
@@ -309,7 +307,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       if (!ok) break;
       if (lane == 0) mma_commit(smem_u32(&sh->tfull[acc]));
       __syncwarp();
-      acc_phase ^= 1u;                      // one accumulator: acc stays 0
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (!ok && issued_any && lane == 0) {
       mma_commit(smem_u32(&sh->drain));
@@ -327,11 +325,11 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       const int n0 = rt.n_idx * (MODE == kUp8 ? BN / 2 : BN);
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue8<MODE>(rt, n0, tmem, lane_q, half, lane, stg, args);
+      epilogue8<MODE>(rt, n0, tmem + (uint32_t)(acc * kAccStride), lane_q, half, lane, stg, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
-      acc_phase ^= 1u;
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -384,14 +382,14 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   cudaStream_t s = (cudaStream_t)stream;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap mx, mw1, mw3, ma, mw2;
-  if (!map2d(&mx, xq, d, R, BK, BM, U8, 1) || !map3d(&mw1, w1q, d, h, E, BK, 64, U8, 1) ||
-      !map3d(&mw3, w3q, d, h, E, BK, 64, U8, 1) || !map2d(&ma, aq, h, R, BK, BM, U8, 1) ||
-      !map3d(&mw2, w2q, h, d, E, BK, BN, U8, 1))   // 256-row box of W2^T
+  if (!map2d(&mx, xq, d, R, BK, BM, U8, 1) || !map3d(&mw1, w1q, d, h, E, BK, BN / 2, U8, 1) ||
+      !map3d(&mw3, w3q, d, h, E, BK, BN / 2, U8, 1) || !map2d(&ma, aq, h, R, BK, BM, U8, 1) ||
+      !map3d(&mw2, w2q, h, d, E, BK, BN, U8, 1))
     return MOE_ERR_CUDA;
   Args8 g{};
   g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
-  // up-projection: K = d, 128 columns of W1 and of W3 per tile
-  g.K = d; g.kb_total = d / BK; g.n_tiles = h / 128; g.N = h;
+  // up-projection: K = d, 96 columns of W1 and of W3 per tile
+  g.K = d; g.kb_total = d / BK; g.n_tiles = (h + BN / 2 - 1) / (BN / 2); g.N = h;
   g.sfa = xs; g.sfb0 = w1s; g.sfb1 = w3s;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.aq = aq; g.as = as;
   int st = launch8<kUp8>(mx, mw1, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
