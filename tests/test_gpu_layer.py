@@ -12,7 +12,7 @@ import torch
 import oracle.layer as ol
 from token_dispatch_grouped_router_gb300 import libmoe as L
 from token_dispatch_grouped_router_gb300 import workloads as wl
-from token_dispatch_grouped_router_gb300.layer import MoELayer
+from token_dispatch_grouped_router_gb300.layer import HostPipeline, MoELayer, bf16_tensor
 
 from gpu_helpers import assert_close, as_f64, ensure_built, i32
 
@@ -354,3 +354,35 @@ def test_combined_calls_equal_the_phase_calls():
     torch.cuda.synchronize()
     for n, v in keep.items():
         assert torch.equal(getattr(layer, n), v), n
+
+
+def test_host_pipeline_matches_sequential_steps():
+    # three steps with different token inputs: the pipelined runner, whose
+    # input and output copies of neighbouring steps overlap the compute on
+    # their own streams, must reproduce each step's results bit for bit
+    w = wl.small_workload(T=1500, d=256, E=4, k=2, h=256)
+    base = wl.generate(w, seed=11)
+    steps = [base]
+    for seed in (12, 13):
+        other = wl.generate(w, seed=seed)
+        steps.append({**base, **{n: other[n] for n in ("x", "dY", "idx", "glogit")}})
+    layer = make_layer(w, base)
+    ref = []
+    for inp in steps:
+        layer.load_inputs(inp)
+        run(layer)
+        ref.append({n: getattr(layer, n).cpu() for n in ("out", "dX")})
+    hin = [{"x": bf16_tensor(i["x"], "cpu").pin_memory(),
+            "dY": bf16_tensor(i["dY"], "cpu").pin_memory(),
+            "idx": torch.from_numpy(i["idx"]).pin_memory(),
+            "glogit": torch.from_numpy(i["glogit"]).pin_memory()} for i in steps]
+    hout = [{n: torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory() for n in ("out", "dX")}
+            for _ in steps]
+    pipe = HostPipeline(layer, input_names=tuple(hin[0]), output_names=("out", "dX"))
+    L.moe_reset_status(layer.ws)
+    pipe.run(hin, hout)
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    for i, (r, o) in enumerate(zip(ref, hout)):
+        for n in ("out", "dX"):
+            assert torch.equal(r[n], o[n]), (i, n)

@@ -232,3 +232,72 @@ class MoELayer:
         R, d, h, T, k, E = self.R, self.d, self.h, self.T, self.k, self.E
         common = 2 * R * d + 2 * T * d + 4 * (3 * T * k + 2 * R + 2 * E + 1)
         return {"saved": common + 2 * R * d + 3 * 2 * R * h, "recompute": common}
+
+
+class HostPipeline:
+    """Layer steps fed from and drained to (pinned) host memory, with the
+    host-to-device copy of step i+1's inputs and the device-to-host copy of
+    step i-1's results running on their own streams while step i computes.
+
+    The named input and output tensors of the layer get a second device copy
+    and the steps alternate between the two; every other buffer of the layer
+    is used by one step at a time, in stream order.  A slot's inputs are
+    overwritten only after the step that read them has finished, and its
+    outputs only after they have been copied out.
+    """
+
+    def __init__(self, layer: MoELayer, input_names=("x", "dY", "idx", "glogit"),
+                 output_names=("out", "dX")):
+        self.layer = layer
+        self.inputs = [n for n in input_names if hasattr(layer, n)]
+        self.outputs = list(output_names)
+        names = self.inputs + self.outputs
+        self.slots = [{n: getattr(layer, n) for n in names},
+                      {n: torch.empty_like(getattr(layer, n)) for n in names}]
+        self.h2d = torch.cuda.Stream(device=layer.x.device)
+        self.d2h = torch.cuda.Stream(device=layer.x.device)
+
+    def _use(self, slot: int) -> None:
+        for n, t in self.slots[slot].items():
+            setattr(self.layer, n, t)
+
+    def run(self, host_inputs, host_outputs, before_step=None) -> None:
+        """Run len(host_inputs) steps: host_inputs[i] maps input names to the
+        host tensors of step i, host_outputs[i] maps output names to host
+        tensors that receive step i's results.  `before_step()`, if given, is
+        enqueued on the compute stream before each step.  Returns when every
+        copy has been issued; the caller synchronises."""
+        compute = torch.cuda.current_stream()
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        start = torch.cuda.Event()
+        start.record(compute)
+        self.h2d.wait_event(start)
+        try:
+            for i, (hin, hout) in enumerate(zip(host_inputs, host_outputs)):
+                s = i % 2
+                dev = self.slots[s]
+                with torch.cuda.stream(self.h2d):
+                    if i >= 2:
+                        self.h2d.wait_event(ev_done[s])      # step i-2 has read this slot
+                    for n in self.inputs:
+                        dev[n].copy_(hin[n], non_blocking=True)
+                    ev_in[s].record(self.h2d)
+                compute.wait_event(ev_in[s])
+                if i >= 2:
+                    compute.wait_event(ev_out[s])            # step i-2's results are out
+                self._use(s)
+                if before_step is not None:
+                    before_step()
+                self.layer.step()
+                ev_done[s].record(compute)
+                with torch.cuda.stream(self.d2h):
+                    self.d2h.wait_event(ev_done[s])
+                    for n in self.outputs:
+                        hout[n].copy_(dev[n], non_blocking=True)
+                    ev_out[s].record(self.d2h)
+            for s in range(min(2, len(host_inputs))):
+                compute.wait_event(ev_out[s])
+        finally:
+            self._use(0)
