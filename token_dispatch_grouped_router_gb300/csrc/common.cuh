@@ -9,6 +9,8 @@
 
 #include "../../include/libmoe.h"
 
+#include <utility>
+
 namespace moe {
 
 // ---------------------------------------------------------------- host side
@@ -80,7 +82,34 @@ inline size_t workspace_bytes(long long T, int E, int k, int d) {
   return a > c ? a : c;
 }
 
+// Programmatic dependent launch: every kernel of this library is launched
+// with programmatic stream serialisation, lets the next launch on its stream
+// be scheduled at once (griddepcontrol.launch_dependents) and waits for the
+// kernel before it to complete and flush its memory (griddepcontrol.wait)
+// before touching global memory, so stream order still holds while the next
+// grid's launch overlaps the tail of the current one.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // -------------------------------------------------------------- device side
+
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __device__ __forceinline__ void set_status(int* status, int code) {
   atomicCAS(status, 0, code);

@@ -169,6 +169,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                      const __grid_constant__ CUtensorMap tmB1, const Args8 args) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -352,7 +353,7 @@ int launch8(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, 
   auto kern = grouped_mxfp8_kernel<MODE>;
   static bool attr_done[64] = {false};
   if (ensure_smem_attr(kern, smem_bytes8(kMaxExperts8), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  kern<<<grid, kThreads, smem_bytes8(args.E), s>>>(a, b0, b1, args);
+  (void)launch_pdl(kern, grid, kThreads, smem_bytes8(args.E), s, a, b0, b1, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }

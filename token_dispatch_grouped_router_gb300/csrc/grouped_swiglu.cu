@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -568,6 +569,7 @@ __device__ __forceinline__ void epilogue_partial(const Tile& tl, uint32_t tacc, 
 // result does not depend on timing), rounded once to bf16.  Block = one row of
 // one split tile, thread = one column.
 __global__ void __launch_bounds__(P_TILE) wgrad_fixup_kernel(const GemmArgs a) {
+  pdl_enter();
   const int i = blockIdx.x / P_TILE, r = blockIdx.x % P_TILE, col = threadIdx.x;
   const int t = a.wg_whole + i;
   const int per = 2 * a.wg_t1 + a.wg_t2;
@@ -591,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                  const GemmArgs args) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -789,6 +792,7 @@ struct WgradTemplates { CUtensorMap m[kWgradMaps]; };
 __global__ void __launch_bounds__(128)
 wgrad_maps_kernel(const __grid_constant__ WgradTemplates tp, const int32_t* __restrict__ offsets,
                   int E, int R, CUtensorMap* __restrict__ maps) {
+  pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= E * kWgradMaps) return;
   const int e = i / kWgradMaps, op = i - e * kWgradMaps;
@@ -819,7 +823,7 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
   static bool attr_done[64] = {false};
   // set once per device for the largest size (E = 1024)
   if (ensure_smem_attr(kern, smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, b2, args);
+  (void)launch_pdl(kern, grid, kThreads, smem, s, a0, a1, b0, b1, b2, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -829,6 +833,8 @@ constexpr size_t pair_smem_bytes(int E) {
          2 * (size_t)(E + 1) * 4;
 }
 
+// at[] must hold two attributes: the 2-CTA cluster shape and programmatic
+// stream serialisation (see launch_pdl)
 inline cudaLaunchConfig_t pair_config(int npairs, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs);
@@ -837,8 +843,10 @@ inline cudaLaunchConfig_t pair_config(int npairs, size_t smem, cudaStream_t s, c
   cfg.stream = s;
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -854,7 +862,7 @@ int pair_limit(cudaStream_t s) {
   const int dev = current_device();
   if (dev < 0 || dev >= 64) return -1;
   if (limit[dev] == 0) {
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes(kMaxExperts), s, at);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
@@ -873,7 +881,7 @@ int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   auto kern = pair_gemm_kernel<MODE>;
   const int limit = pair_limit<MODE>(s);
   if (limit <= 0) return MOE_ERR_CUDA;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   const long long ub = tiles_upper > 0 ? tiles_upper : 1;
   const int npairs = (int)(ub < limit ? ub : limit);
   cudaLaunchConfig_t cfg = pair_config(npairs, pair_smem_bytes(g.E), s, at);
@@ -1012,7 +1020,7 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
       !map2d(&tp.m[4], dyp, d, R, 64, 64))
     return MOE_ERR_CUDA;
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  wgrad_maps_kernel<<<(E * kWgradMaps + 127) / 128, 128, 0, s>>>(tp, offsets, E, R, maps);
+  (void)launch_pdl(wgrad_maps_kernel, (E * kWgradMaps + 127) / 128, 128, 0, s, tp, offsets, E, R, maps);
   MOE_LAUNCH_CHECK(1);
   GemmArgs g = base_args(offsets, R, E, d, h, ws);
   g.wg_maps = maps;
@@ -1046,7 +1054,7 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   }
   const int st = launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], g, g.wg_units, s);
   if (st != MOE_OK || g.wg_split == 0) return st;
-  wgrad_fixup_kernel<<<(unsigned)(L * P_TILE), P_TILE, 0, s>>>(g);
+  (void)launch_pdl(wgrad_fixup_kernel, (unsigned)(L * P_TILE), P_TILE, 0, s, g);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }

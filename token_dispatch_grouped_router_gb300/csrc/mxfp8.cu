@@ -24,6 +24,7 @@ using mx::inv_scale;
 // One thread per 32-element block.
 __global__ void quantize_rows_kernel(const uint16_t* __restrict__ src, long long nblocks, int K,
                                      uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  pdl_enter();
   const long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (b >= nblocks) return;
   const uint16_t* p = src + b * 32;
@@ -57,6 +58,7 @@ __global__ void quantize_rows_kernel(const uint16_t* __restrict__ src, long long
 __global__ void __launch_bounds__(128)
 quantize_weights_kernel(const uint16_t* __restrict__ W, int K, int N, uint8_t* __restrict__ wq,
                         uint8_t* __restrict__ ws) {
+  pdl_enter();
   __shared__ uint16_t tile[32][128 + 8];
   const int e = blockIdx.z, kb = blockIdx.y, n0 = blockIdx.x * 128;
   const uint16_t* src = W + ((size_t)e * K + (size_t)kb * 32) * N + n0;
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(256)
 dispatch_mxfp8_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
                       const int32_t* __restrict__ row_of_slot, uint8_t* __restrict__ xq,
                       uint8_t* __restrict__ xs, uint16_t* __restrict__ xp) {
+  pdl_enter();
   const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -153,7 +156,7 @@ int moe_mxfp8_quantize_rows(const moe_bf16_t* src, int rows, int K, uint8_t* q, 
   MOE_CHECK_PTR(src); MOE_CHECK_PTR(q);
   if (scale == nullptr) return MOE_ERR_INVALID_ARG;
   const long long nb = (long long)rows * (K / 32);
-  quantize_rows_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, (cudaStream_t)stream>>>(src, nb, K, q, scale);
+  (void)launch_pdl(quantize_rows_kernel, (unsigned)((nb + 255) / 256), 256, 0, (cudaStream_t)stream, src, nb, K, q, scale);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -166,7 +169,7 @@ int moe_mxfp8_quantize_weights(const moe_bf16_t* W, int E, int K, int N, uint8_t
   if (ws == nullptr) return MOE_ERR_INVALID_ARG;
   if (K / 32 > 65535 || E > 65535) return MOE_ERR_UNSUPPORTED;
   dim3 grid(N / 128, K / 32, E);
-  quantize_weights_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(W, K, N, wq, ws);
+  (void)launch_pdl(quantize_weights_kernel, grid, 128, 0, (cudaStream_t)stream, W, K, N, wq, ws);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -180,7 +183,7 @@ int moe_dispatch_rows_mxfp8(const moe_bf16_t* x, int T, int d, int k, const int3
   if (xs == nullptr) return MOE_ERR_INVALID_ARG;
   if (xp && !aligned16(xp)) return MOE_ERR_INVALID_ARG;
   dim3 grid((T + 7) / 8);
-  dispatch_mxfp8_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, T, d, k, row_of_slot, xq, xs, xp);
+  (void)launch_pdl(dispatch_mxfp8_kernel, grid, 256, 0, (cudaStream_t)stream, x, T, d, k, row_of_slot, xq, xs, xp);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }

@@ -23,6 +23,7 @@ template <int U>
 __global__ void __launch_bounds__(kThreads)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
                 const int32_t* __restrict__ row_of_slot, uint16_t* __restrict__ xp) {
+  pdl_enter();
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -64,6 +65,7 @@ template <int U>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint16_t* __restrict__ yp, const int32_t* __restrict__ row_of_slot,
                const float* __restrict__ gate, int T, int k, int d, uint16_t* __restrict__ out) {
+  pdl_enter();
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(kThreads)
 combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ yp,
                    const int32_t* __restrict__ row_of_slot, const float* __restrict__ gate,
                    int T, int d, uint16_t* __restrict__ dyp, float* __restrict__ dgate) {
+  pdl_enter();
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -195,7 +198,7 @@ void launch_combine_bwd(dim3 grid, cudaStream_t s, const uint16_t* dout, const u
                         float* dgate) {
   // 8 to 16 row vectors of 16 bytes in flight a lane
   constexpr int U = K <= 2 ? 8 : (K <= 4 ? 4 : 2);
-  combine_bwd_kernel<K, U><<<grid, kThreads, 0, s>>>(dout, yp, row_of_slot, gate, T, d, dyp, dgate);
+  (void)launch_pdl(combine_bwd_kernel<K, U>, grid, kThreads, 0, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate);
 }
 
 }  // namespace
@@ -211,7 +214,7 @@ int moe_dispatch_rows(const moe_bf16_t* x, int T, int d, int k, const int32_t* r
   if (T == 0) return MOE_OK;
   MOE_CHECK_PTR(x); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(xp);
   dim3 grid((T + kWarps - 1) / kWarps);
-  dispatch_kernel<8><<<grid, kThreads, 0, (cudaStream_t)stream>>>(x, T, d, k, row_of_slot, xp);
+  (void)launch_pdl(dispatch_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, x, T, d, k, row_of_slot, xp);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -226,7 +229,7 @@ int moe_combine(const moe_bf16_t* yp, const int32_t* row_of_slot, const float* g
   // 8 vectors a lane: a 2048-wide row in one pass.  (A copy specialised on k
   // issues all k x 8 loads up front, needs 136 registers and runs 1.8x slower
   // at one block per SM; this one stays at 127 and two blocks.)
-  combine_kernel<8><<<grid, kThreads, 0, (cudaStream_t)stream>>>(yp, row_of_slot, gate, T, k, d, out);
+  (void)launch_pdl(combine_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, yp, row_of_slot, gate, T, k, d, out);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }

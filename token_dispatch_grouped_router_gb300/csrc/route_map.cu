@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kRCThreads)
 route_count_kernel(const int32_t* __restrict__ idx, int R, int E,
                    int32_t* __restrict__ chunk_counts, int32_t* __restrict__ local_rank,
                    int* __restrict__ status) {
+  pdl_enter();
   extern __shared__ int32_t hist[];                 // [kRCWarps][E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kRCWarps * E; i += kRCThreads) hist[i] = 0;
@@ -85,6 +86,7 @@ route_count_kernel(const int32_t* __restrict__ idx, int R, int E,
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  pdl_enter();
   __shared__ int32_t tot[kMaxExperts];
   __shared__ int32_t warp_sums[32];
   {
@@ -140,6 +142,7 @@ __global__ void route_place_kernel(const int32_t* __restrict__ idx, int R, int E
                                    const int32_t* __restrict__ offsets,
                                    int32_t* __restrict__ row_of_slot,
                                    int32_t* __restrict__ slot_of_row) {
+  pdl_enter();
   int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= R) return;
   int e = __ldg(idx + s);
@@ -181,10 +184,10 @@ extern "C" int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E, 
     return MOE_OK;
   }
   size_t smem = sizeof(int32_t) * kRCWarps * E;
-  route_count_kernel<<<nchunks, kRCThreads, smem, s>>>(topk_idx, (int)R, E, chunk_counts,
+  (void)launch_pdl(route_count_kernel, nchunks, kRCThreads, smem, s, topk_idx, (int)R, E, chunk_counts,
                                                        local_rank, status);
-  route_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, counts, offsets);
-  route_place_kernel<<<(int)((R + 255) / 256), 256, 0, s>>>(topk_idx, (int)R, E, chunk_counts,
+  (void)launch_pdl(route_scan_kernel, 1, 1024, 0, s, chunk_counts, nchunks, E, counts, offsets);
+  (void)launch_pdl(route_place_kernel, (int)((R + 255) / 256), 256, 0, s, topk_idx, (int)R, E, chunk_counts,
                                                              local_rank, offsets, row_of_slot,
                                                              slot_of_row);
   MOE_LAUNCH_CHECK(3);
@@ -267,10 +270,10 @@ extern "C" int moe_expert_offsets_noalloc(const int32_t* topk_idx, int T, int k,
   int32_t* local_rank = chunk_counts + kNoAllocChunkInts;
   const int nchunks = (int)((R + kRouteChunk - 1) / kRouteChunk);
   size_t smem = sizeof(int32_t) * kRCWarps * E;
-  route_count_kernel<<<nchunks, kRCThreads, smem, s>>>(topk_idx, (int)R, E, chunk_counts,
+  (void)launch_pdl(route_count_kernel, nchunks, kRCThreads, smem, s, topk_idx, (int)R, E, chunk_counts,
                                                        local_rank, st);
-  route_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, counts, offsets);
-  route_place_kernel<<<(int)((R + 255) / 256), 256, 0, s>>>(topk_idx, (int)R, E, chunk_counts,
+  (void)launch_pdl(route_scan_kernel, 1, 1024, 0, s, chunk_counts, nchunks, E, counts, offsets);
+  (void)launch_pdl(route_place_kernel, (int)((R + 255) / 256), 256, 0, s, topk_idx, (int)R, E, chunk_counts,
                                                              local_rank, offsets, row_of_slot,
                                                              slot_of_row);
   MOE_LAUNCH_CHECK(3);

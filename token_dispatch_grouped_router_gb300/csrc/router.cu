@@ -37,6 +37,7 @@ simt_gemm_kernel(const TA* __restrict__ A, int lda, const float* __restrict__ B,
                  int M, int N, int K, int k_per_split,
                  float* __restrict__ outf, __nv_bfloat16* __restrict__ outb, int ldo,
                  const float* __restrict__ bias) {
+  pdl_enter();
   __shared__ float As[SK][SB + 4];
   __shared__ float Bs[SK][SB + 4];
   const int tid = threadIdx.x;
@@ -105,6 +106,7 @@ simt_gemm_kernel(const TA* __restrict__ A, int lda, const float* __restrict__ B,
 // dW_r[m][n] = sum over splits of the partials (fixed order: deterministic)
 __global__ void reduce_splits_kernel(const float* __restrict__ part, int splits, int MN,
                                      float* __restrict__ out) {
+  pdl_enter();
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= MN) return;
   float s = 0.f;
@@ -114,6 +116,7 @@ __global__ void reduce_splits_kernel(const float* __restrict__ part, int splits,
 
 // db[e] = sum_t dz[t][e]: one block per expert, fixed-order block reduction
 __global__ void column_sum_kernel(const float* __restrict__ dz, int T, int E, float* __restrict__ db) {
+  pdl_enter();
   __shared__ float red[256];
   int e = blockIdx.x;
   float s = 0.f;
@@ -142,6 +145,7 @@ template <int VPL>
 __global__ void __launch_bounds__(256)
 topk_kernel(const float* __restrict__ logits, int T, int E, int k,
             int32_t* __restrict__ idx_out, float* __restrict__ gate_out) {
+  pdl_enter();
   const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -194,6 +198,7 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int k,
 }
 
 __global__ void gates_kernel(const float* __restrict__ sel, int T, int k, float* __restrict__ gate) {
+  pdl_enter();
   int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const float* z = sel + (size_t)t * k;
@@ -214,6 +219,7 @@ __global__ void gates_kernel(const float* __restrict__ sel, int T, int k, float*
 __global__ void __launch_bounds__(256)
 topk_bwd_kernel(const float* __restrict__ gate, const float* __restrict__ dgate,
                 const int32_t* __restrict__ idx, int T, int E, int k, float* __restrict__ dz) {
+  pdl_enter();
   const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -254,8 +260,7 @@ int moe_router_logits(const moe_bf16_t* x, const float* W_r, const float* b, int
   MOE_CHECK_PTR(x); MOE_CHECK_PTR(W_r); MOE_CHECK_PTR(logits);
   if (b && !aligned16(b)) return MOE_ERR_INVALID_ARG;
   dim3 grid((T + SB - 1) / SB, (E + SB - 1) / SB, 1);
-  simt_gemm_kernel<__nv_bfloat16, Lay::RowMK, LayB::RowKN, Epi::StoreBias>
-      <<<grid, 256, 0, (cudaStream_t)stream>>>(
+  (void)launch_pdl(simt_gemm_kernel<__nv_bfloat16, Lay::RowMK, LayB::RowKN, Epi::StoreBias>, grid, 256, 0, (cudaStream_t)stream, 
           reinterpret_cast<const __nv_bfloat16*>(x), d, W_r, E, T, E, d, d,
           logits, nullptr, E, b);
   MOE_LAUNCH_CHECK(1);
@@ -271,12 +276,12 @@ int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
   dim3 grid((T + warps - 1) / warps);
   cudaStream_t s = (cudaStream_t)stream;
   int vpl = (E + 31) / 32;
-  if (vpl <= 1) topk_kernel<1><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
-  else if (vpl <= 2) topk_kernel<2><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
-  else if (vpl <= 4) topk_kernel<4><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
-  else if (vpl <= 8) topk_kernel<8><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
-  else if (vpl <= 16) topk_kernel<16><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
-  else topk_kernel<32><<<grid, threads, 0, s>>>(logits, T, E, k, topk_idx, topk_gate);
+  if (vpl <= 1) (void)launch_pdl(topk_kernel<1>, grid, threads, 0, s, logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 2) (void)launch_pdl(topk_kernel<2>, grid, threads, 0, s, logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 4) (void)launch_pdl(topk_kernel<4>, grid, threads, 0, s, logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 8) (void)launch_pdl(topk_kernel<8>, grid, threads, 0, s, logits, T, E, k, topk_idx, topk_gate);
+  else if (vpl <= 16) (void)launch_pdl(topk_kernel<16>, grid, threads, 0, s, logits, T, E, k, topk_idx, topk_gate);
+  else (void)launch_pdl(topk_kernel<32>, grid, threads, 0, s, logits, T, E, k, topk_idx, topk_gate);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -285,7 +290,7 @@ int moe_router_gates(const float* sel_logits, int T, int k, float* topk_gate, mo
   MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= kMaxTopK);
   if (T == 0) return MOE_OK;
   MOE_CHECK_PTR(sel_logits); MOE_CHECK_PTR(topk_gate);
-  gates_kernel<<<(T + 255) / 256, 256, 0, (cudaStream_t)stream>>>(sel_logits, T, k, topk_gate);
+  (void)launch_pdl(gates_kernel, (T + 255) / 256, 256, 0, (cudaStream_t)stream, sel_logits, T, k, topk_gate);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -296,7 +301,7 @@ int moe_router_topk_bwd(const float* topk_gate, const float* d_gate, const int32
   if (T == 0) return MOE_OK;
   MOE_CHECK_PTR(topk_gate); MOE_CHECK_PTR(d_gate); MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(d_logits);
   dim3 grid((T + 7) / 8);
-  topk_bwd_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(topk_gate, d_gate, topk_idx, T, E, k, d_logits);
+  (void)launch_pdl(topk_bwd_kernel, grid, 256, 0, (cudaStream_t)stream, topk_gate, d_gate, topk_idx, T, E, k, d_logits);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -319,7 +324,7 @@ int moe_router_logits_bwd(const moe_bf16_t* x, const float* W_r, const float* d_
   // dx += dz @ W_r^T : M = T, N = d, K = E; B(k=e, n) = W_r[n*E + e]
   {
     dim3 grid((T + SB - 1) / SB, (d + SB - 1) / SB, 1);
-    simt_gemm_kernel<float, Lay::RowMK, LayB::ColKN, Epi::AddBf16><<<grid, 256, 0, s>>>(
+    (void)launch_pdl(simt_gemm_kernel<float, Lay::RowMK, LayB::ColKN, Epi::AddBf16>, grid, 256, 0, s, 
         d_logits, E, W_r, E, T, d, E, E, nullptr, reinterpret_cast<__nv_bfloat16*>(dx), d, nullptr);
   }
   // dW_r = x^T @ dz : M = d, N = E, K = T, split into kRouterSplits partials
@@ -328,14 +333,14 @@ int moe_router_logits_bwd(const moe_bf16_t* x, const float* W_r, const float* d_
     int kps = (T + kRouterSplits - 1) / kRouterSplits;
     kps = (kps + SK - 1) / SK * SK;
     dim3 grid((d + SB - 1) / SB, (E + SB - 1) / SB, kRouterSplits);
-    simt_gemm_kernel<__nv_bfloat16, Lay::ColMK, LayB::RowKN, Epi::StorePartial><<<grid, 256, 0, s>>>(
+    (void)launch_pdl(simt_gemm_kernel<__nv_bfloat16, Lay::ColMK, LayB::RowKN, Epi::StorePartial>, grid, 256, 0, s, 
         reinterpret_cast<const __nv_bfloat16*>(x), d, d_logits, E, d, E, T, kps, part, nullptr, E,
         nullptr);
     int MN = d * E;
-    reduce_splits_kernel<<<(MN + 255) / 256, 256, 0, s>>>(part, kRouterSplits, MN, dW_r);
+    (void)launch_pdl(reduce_splits_kernel, (MN + 255) / 256, 256, 0, s, part, kRouterSplits, MN, dW_r);
   }
   int n = 3;
-  if (db) { column_sum_kernel<<<E, 256, 0, s>>>(d_logits, T, E, db); ++n; }
+  if (db) { (void)launch_pdl(column_sum_kernel, E, 256, 0, s, d_logits, T, E, db); ++n; }
   MOE_LAUNCH_CHECK(n);
   return MOE_OK;
 }
