@@ -87,6 +87,7 @@ def compare_full(layer, w, inp, backward=True):
     (2700, 192, 4, 2, 320, (2,)),       # pair tiles, ragged tails, one empty expert
     (2100, 256, 2, 1, 128, ()),         # pair tiles, one 128-wide hidden tile
     (1100, 128, 1, 1, 64, ()),          # last tile's odd CTA holds no rows
+    (1000, 256, 8, 8, 192, ()),         # top-8 of 8: every token in every expert
     # the weight-gradient tiles split along the rows (fp32 partials, ordered
     # sum) with an empty expert among them
     (3000, 256, 3, 1, 256, (0,)),
@@ -279,9 +280,15 @@ def _sampled_reference(inp, w, idx, g, ros, toks, hs, experts):
     return res, wg
 
 
-@pytest.mark.parametrize("key", ["dense_e8", "pool_e128", "skew_e128", "train_e128"])
+@pytest.mark.parametrize("key", ["dense_e8", "pool_e128", "skew_e128", "train_e128",
+                                 "max_experts_top8"])
 def test_full_size_sampled(key):
-    w = wl.get_workload(key)
+    if key == "max_experts_top8":
+        # the largest expert count the library takes, top-8 routing, 512 rows per
+        # expert: pair GEMMs and a K-split wgrad with 1024-expert tile tables
+        w = wl.small_workload(T=65536, d=128, E=1024, k=8, h=128)
+    else:
+        w = wl.get_workload(key)
     inp = wl.generate(w, seed=0)
     zref = None
     if w.routing == "learned":
