@@ -89,6 +89,15 @@ __device__ __forceinline__ void pack_row32(const float* v, uint4 (&o)[4]) {
   for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
 }
 
+// The staging buffer may still be the source of this warp's last TMA store:
+// lane 0 waits until the copy engine has read it, then the warp goes on.
+// (store_chunk and chunk_to_row do not wait: a caller that mixes them with
+// TMA stores calls this first.)
+__device__ __forceinline__ void stg_acquire(int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+
 // The warp's 32 rows (one per lane, 32 values each) -> global memory at
 // g[row * ld + 0..31] for rows < nrows, through the staging buffer so that each
 // store instruction writes 8 rows x 64 contiguous bytes.
@@ -149,6 +158,45 @@ __device__ __forceinline__ void chunk_to_row(const uint4 (&q)[4], uint8_t* stg, 
     const uint4 t = *reinterpret_cast<const uint4*>(stg + lane * kStagePitch + 16 * i);
     w[4 * i + 0] = t.x; w[4 * i + 1] = t.y; w[4 * i + 2] = t.z; w[4 * i + 3] = t.w;
   }
+  __syncwarp();
+}
+
+// The warp's 32 x 32 chunk (one row per lane) stored by TMA: the lanes write
+// it to the staging buffer in the 64-byte swizzled layout of the output
+// descriptor (CU_TENSOR_MAP_SWIZZLE_64B, 32 x 32 box; 16-byte piece c of row
+// r at piece position c ^ ((r >> 1) & 3), buffer on a 512-byte boundary, so
+// every 8 lanes cover all banks), then lane 0 issues one bulk store.  The
+// descriptor clips rows and columns outside the tensor; rows inside it are
+// all written, so callers use this only for slices whose 32 rows are theirs.
+__device__ __forceinline__ void stage_chunk_sw64(uint8_t* stg, const float* v, int lane) {
+  uint4 o[4];
+  pack_row32(v, o);
+  stg_acquire(lane);
+  const int x = (lane >> 1) & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stg + lane * 64 + 16 * (i ^ x)) = o[i];
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+__device__ __forceinline__ void store_chunk_tma(uint8_t* stg, const float* v, int lane,
+                                                const CUtensorMap* map, int col, int row) {
+  stage_chunk_sw64(stg, v, lane);
+  if (lane == 0) {
+    tma_store_2d(map, smem_u32(stg), col, row);
+    bulk_commit();
+  }
+}
+__device__ __forceinline__ void store_chunk_tma3(uint8_t* stg, const float* v, int lane,
+                                                 const CUtensorMap* map, int col, int row, int z) {
+  stage_chunk_sw64(stg, v, lane);
+  if (lane == 0) {
+    tma_store_3d(map, smem_u32(stg), col, row, z);
+    bulk_commit();
+  }
+}
+// end of a warp's epilogue: its bulk stores have completed
+__device__ __forceinline__ void stg_finish(int lane) {
+  if (lane == 0) bulk_wait_all();
   __syncwarp();
 }
 
@@ -239,6 +287,31 @@ inline bool map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t oute
   return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output descriptors for the TMA-stored epilogue: bf16 [rows, cols] with row
+// stride ld (elements), or [outer, mid, inner]; 32 x 32 boxes, 64-byte swizzle.
+inline bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+inline bool map3d_out(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t mid, uint64_t outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D map over a row-major [outer, mid, inner] tensor, box [1, box_mid, box_inner]

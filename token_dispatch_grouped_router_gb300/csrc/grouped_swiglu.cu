@@ -153,21 +153,28 @@ __device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa,
   }
 }
 
+// TMA descriptors of the epilogue's outputs (kernel parameters): UP h1, h3, a;
+// DOWN yp; DA dh1, dh3; DX dxp; WG dW1, dW3, dW2 ([E, M, N] each).
+struct OutMaps {
+  const CUtensorMap *o0, *o1, *o2;
+};
+
 // Epilogue of one tile for the 32 rows of this warp's TMEM lane quarter and
 // the half `half` of the tile's columns (two warps share a lane quarter).
-// Accumulator rows arrive one per lane (tcgen05.ld 32x32b); global traffic is
-// coalesced through the warp's staging buffer `stg`.
+// Accumulator rows arrive one per lane (tcgen05.ld 32x32b) and leave through
+// the warp's staging buffer `stg`: a 32 x 32 chunk whose 32 rows all belong to
+// the tile goes out as one TMA store; a slice cut short by the end of an
+// expert's rows is written by coalesced stores of its own rows only.
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int lane_q, int half,
-                                              int lane, uint8_t* stg, const GemmArgs& a) {
+                                              int lane, uint8_t* stg, const GemmArgs& a,
+                                              const OutMaps& om) {
   const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
   if constexpr (MODE == kWG) {
     const int M = tl.which == 2 ? a.h : a.d;
     const int N = tl.which == 2 ? a.d : a.h;
-    uint16_t* out = tl.which == 0 ? a.out0 : (tl.which == 1 ? a.out1 : a.out2);
     const int r0 = tl.m0 + lane_q * 32;               // first row of this warp's slice
     const int nrows = min(32, M - r0);
-    uint16_t* g = out + ((size_t)tl.e * M + (nrows > 0 ? r0 : 0)) * N;
 #pragma unroll 1
     for (int c = half * 4; c < half * 4 + 4; ++c) {
       float v[32];
@@ -182,11 +189,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
       const int col = tl.n0 + c * 32;
-      if (col < N) store_chunk(stg, v, lane, g + col, N, nrows);
+      if (col < N && nrows > 0)
+        store_chunk_tma3(stg, v, lane, tl.which == 0 ? om.o0 : (tl.which == 1 ? om.o1 : om.o2),
+                         col, r0, tl.e);
     }
   } else {
     const int nrows = min(32, tl.rows - lane_q * 32);  // rows of this slice in the segment
     const size_t r0 = (size_t)tl.row0 + (nrows > 0 ? lane_q * 32 : 0);
+    const bool whole = nrows == 32;                     // TMA store of the whole slice
     if constexpr (MODE == kUp) {
 #pragma unroll 1
       for (int c = half * 2; c < half * 2 + 2; ++c) {
@@ -203,9 +213,16 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
             h3[i] = __uint_as_float(q3[i]);
             av[i] = silu_f(h1[i]) * h3[i];
           }
-          store_chunk(stg, h1, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
-          store_chunk(stg, h3, lane, a.out1 + r0 * a.ldo + col, a.ldo, nrows);
-          store_chunk(stg, av, lane, a.out2 + r0 * a.ldo + col, a.ldo, nrows);
+          if (whole) {
+            store_chunk_tma(stg, h1, lane, om.o0, col, (int)r0);
+            store_chunk_tma(stg, h3, lane, om.o1, col, (int)r0);
+            store_chunk_tma(stg, av, lane, om.o2, col, (int)r0);
+          } else {
+            stg_acquire(lane);
+            store_chunk(stg, h1, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
+            store_chunk(stg, h3, lane, a.out1 + r0 * a.ldo + col, a.ldo, nrows);
+            store_chunk(stg, av, lane, a.out2 + r0 * a.ldo + col, a.ldo, nrows);
+          }
         }
       }
     } else if constexpr (MODE == kDA) {
@@ -244,6 +261,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
             g1[i] = da * h3 * sg * (1.f + h1 * (1.f - sg));
             q[i] = __float_as_uint(da * h1 * sg);                    // dh3 in place
           }
+          // (plain coalesced stores: two TMA stores a chunk through the one
+          // staging buffer made this epilogue slower)
           store_chunk(stg, g1, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
           store_chunk(stg, reinterpret_cast<const float*>(q), lane, a.out1 + r0 * a.ldo + col,
                       a.ldo, nrows);
@@ -261,7 +280,12 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(q[i]);
-          store_chunk(stg, v, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
+          if (whole) {
+            store_chunk_tma(stg, v, lane, om.o0, col, (int)r0);
+          } else {
+            stg_acquire(lane);
+            store_chunk(stg, v, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
+          }
         }
       }
     }
@@ -272,7 +296,9 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
+                    const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
+                    const GemmArgs args) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -318,6 +344,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmB0);
     prefetch_tmap(&tmB1); prefetch_tmap(&tmB2);
+    prefetch_tmap(&tmO0); prefetch_tmap(&tmO1); prefetch_tmap(&tmO2);
   }
   tc_fence_before();
   __syncthreads();
@@ -417,6 +444,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     // --------------------------------------------------------------- epilogue
     const int lane_q = warp & 3;          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;     // which half of the tile's columns
+    const OutMaps om{&tmO0, &tmO1, &tmO2};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -424,12 +452,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
       epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * BN), lane_q, half, lane,
-                          sStage + (warp - 2) * kStageBytes, args);
+                          sStage + (warp - 2) * kStageBytes, args, om);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    stg_finish(lane);
   }
 
   tc_fence_before();
@@ -592,7 +621,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-                 const GemmArgs args) {
+                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
+                 const __grid_constant__ CUtensorMap tmO2, const GemmArgs args) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -642,8 +672,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     tmem_alloc_pair(smem_u32(&sh->tmem_base), kTmemCols);
     tmem_relinquish_pair();
   }
-  if (warp == 0 && lane == 0 && MODE != kWG) {
-    prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+  if (warp == 0 && lane == 0) {
+    if (MODE != kWG) {
+      prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+    }
+    prefetch_tmap(&tmO0); prefetch_tmap(&tmO1); prefetch_tmap(&tmO2);
   }
   tc_fence_before();
   cluster_sync();
@@ -744,6 +777,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     // --------------------------------------------------------------- epilogue
     const int lane_q = warp & 3;
     const int half = (warp - 2) >> 2;
+    const OutMaps om{&tmO0, &tmO1, &tmO2};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < total; t += npairs) {
@@ -766,12 +800,13 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
       }
       if (whole)
         epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
-                            sStage + (warp - 2) * kStageBytes, args);
+                            sStage + (warp - 2) * kStageBytes, args, om);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tempty[acc]), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    stg_finish(lane);
   }
 
   tc_fence_before();
@@ -814,16 +849,21 @@ constexpr size_t smem_bytes(int E) {
          sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
 }
 
+// output descriptors of one GEMM launch (see OutMaps); unused slots repeat one
+struct OutDescs {
+  CUtensorMap m[3];
+};
+
 template <int MODE>
 int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-           const CUtensorMap& b1, const CUtensorMap& b2, const GemmArgs& args, int grid,
-           cudaStream_t s) {
+           const CUtensorMap& b1, const CUtensorMap& b2, const OutDescs& o, const GemmArgs& args,
+           int grid, cudaStream_t s) {
   const size_t smem = smem_bytes(args.E);
   auto kern = grouped_gemm_kernel<MODE>;
   static bool attr_done[64] = {false};
   // set once per device for the largest size (E = 1024)
   if (ensure_smem_attr(kern, smem_bytes(kMaxExperts), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  (void)launch_pdl(kern, grid, kThreads, smem, s, a0, a1, b0, b1, b2, args);
+  (void)launch_pdl(kern, grid, kThreads, smem, s, a0, a1, b0, b1, b2, o.m[0], o.m[1], o.m[2], args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -877,7 +917,8 @@ int pair_limit(cudaStream_t s) {
 // Launches pair_gemm_kernel<MODE> on min(tiles_upper, co-resident pairs) clusters.
 template <int MODE>
 int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                const CUtensorMap& b1, const GemmArgs& g, long long tiles_upper, cudaStream_t s) {
+                const CUtensorMap& b1, const OutDescs& o, const GemmArgs& g, long long tiles_upper,
+                cudaStream_t s) {
   auto kern = pair_gemm_kernel<MODE>;
   const int limit = pair_limit<MODE>(s);
   if (limit <= 0) return MOE_ERR_CUDA;
@@ -885,7 +926,7 @@ int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   const long long ub = tiles_upper > 0 ? tiles_upper : 1;
   const int npairs = (int)(ub < limit ? ub : limit);
   cudaLaunchConfig_t cfg = pair_config(npairs, pair_smem_bytes(g.E), s, at);
-  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, g) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, o.m[0], o.m[1], o.m[2], g) != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -915,6 +956,15 @@ using namespace moe;
 namespace moe {
 namespace {
 
+// descriptors of up to three row-grouped [R, cols] bf16 outputs (row stride cols)
+bool row_outs(OutDescs* o, int R, uint64_t cols, const void* p0, const void* p1 = nullptr,
+              const void* p2 = nullptr) {
+  const void* p[3] = {p0, p1 ? p1 : p0, p2 ? p2 : p0};
+  for (int i = 0; i < 3; ++i)
+    if (!map2d_out(&o->m[i], p[i], cols, (uint64_t)R, cols)) return false;
+  return true;
+}
+
 GemmArgs base_args(const int32_t* offsets, int R, int E, int d, int h, void* ws) {
   GemmArgs g{};
   g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
@@ -935,9 +985,11 @@ int run_up(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d, in
   g.n_tiles = (h + BN / 2 - 1) / (BN / 2);      // 128 h-columns of W1 and of W3 per tile
   g.kb_total = d / BK;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.ldo = h;
+  OutDescs o;
+  if (!row_outs(&o, R, h, h1, h3, a)) return MOE_ERR_CUDA;
   if (rows_on_pairs(R, E))
-    return launch_pair<kUp>(mx, mx, mw1, mw3, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
-  return launch<kUp>(mx, mx, mw1, mw3, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
+    return launch_pair<kUp>(mx, mx, mw1, mw3, o, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
+  return launch<kUp>(mx, mx, mw1, mw3, mw3, o, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
 // yp = a_e @ W2[e]
@@ -950,9 +1002,11 @@ int run_down(const moe_bf16_t* a, const int32_t* offsets, int R, int E, int d, i
   g.n_tiles = (d + BN - 1) / BN;
   g.kb_total = h / BK;
   g.out0 = yp; g.ldo = d;
+  OutDescs o;
+  if (!row_outs(&o, R, d, yp)) return MOE_ERR_CUDA;
   if (rows_on_pairs(R, E))
-    return launch_pair<kDown>(ma, ma, mw2, mw2, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
-  return launch<kDown>(ma, ma, mw2, mw2, mw2, g, row_grid_upper(R, E, g.n_tiles), s);
+    return launch_pair<kDown>(ma, ma, mw2, mw2, o, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
+  return launch<kDown>(ma, ma, mw2, mw2, mw2, o, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
 // dA = dyp_e @ W2[e]^T with the SwiGLU backward epilogue -> dh1, dh3
@@ -967,7 +1021,9 @@ int run_dact(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_
   g.n_tiles = (h + BN - 1) / BN;
   g.kb_total = d / BK;
   g.out0 = dh1; g.out1 = dh3; g.in0 = h1; g.in1 = h3; g.ldo = h;
-  return launch<kDA>(m_dyp, m_dyp, m_w2k, m_w2k, m_w2k, g, row_grid_upper(R, E, g.n_tiles), s);
+  OutDescs o;   // DA stores without TMA; the descriptors are carried along unused
+  if (!row_outs(&o, R, h, dh1, dh3)) return MOE_ERR_CUDA;
+  return launch<kDA>(m_dyp, m_dyp, m_w2k, m_w2k, m_w2k, o, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
 // dxp = dh1_e @ W1[e]^T + dh3_e @ W3[e]^T (one reduction over K = 2h)
@@ -987,9 +1043,11 @@ int run_dx(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t*
   g.kb_total = 2 * (h / BK);
   g.kb_split = h / BK;
   g.out0 = dxp; g.ldo = d;
+  OutDescs o;
+  if (!row_outs(&o, R, d, dxp)) return MOE_ERR_CUDA;
   if (pairs)
-    return launch_pair<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
-  return launch<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, m_w3k, g, row_grid_upper(R, E, g.n_tiles), s);
+    return launch_pair<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, o, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
+  return launch<kDX>(m_dh1, m_dh3, m_w1k, m_w3k, m_w3k, o, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
 // dW1[e] = xp_e^T dh1_e, dW3[e] = xp_e^T dh3_e, dW2[e] = a_e^T dyp_e (one launch)
@@ -1052,7 +1110,11 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
       g.wg_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wgrad_parts_offset(E));
     }
   }
-  const int st = launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], g, g.wg_units, s);
+  OutDescs o;
+  if (!map3d_out(&o.m[0], dW1, h, d, E) || !map3d_out(&o.m[1], dW3, h, d, E) ||
+      !map3d_out(&o.m[2], dW2, d, h, E))
+    return MOE_ERR_CUDA;
+  const int st = launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], o, g, g.wg_units, s);
   if (st != MOE_OK || g.wg_split == 0) return st;
   (void)launch_pdl(wgrad_fixup_kernel, (unsigned)(L * P_TILE), P_TILE, 0, s, g);
   MOE_LAUNCH_CHECK(1);
