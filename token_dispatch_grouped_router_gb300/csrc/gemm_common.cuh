@@ -28,6 +28,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s; a step takes millisec
 template <int STAGES>
 struct PipeShared {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  uint64_t rfull[4], rempty[4];   // CTA-pair DA: the epilogue's h1/h3 ring
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
@@ -290,13 +291,15 @@ inline bool map2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t oute
 }
 
 // Output descriptors for the TMA-stored epilogue: bf16 [rows, cols] with row
-// stride ld (elements), or [outer, mid, inner]; 32 x 32 boxes, 64-byte swizzle.
-inline bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld) {
+// stride ld (elements), or [outer, mid, inner]; 32-column boxes (32 rows, or
+// box_rows) in the 64-byte swizzle.
+inline bool map2d_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld,
+                      uint32_t box_rows = 32) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {32, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,

@@ -480,14 +480,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 // an accumulator on the even CTA's `tempty` barrier.
 //   UP, DOWN, DX:      256-row tiles of an expert's rows; UP splits B into
 //                      W1 columns (even CTA) and W3 columns (odd CTA), so the
-//                      accumulator keeps the single-CTA column layout.  (The
-//                      DA epilogue, which reads h1 and h3 for every output,
-//                      bounds that GEMM already on a single CTA; it stays there.)
+//                      accumulator keeps the single-CTA column layout.
+//   DA:                256-row tiles like DOWN, 4 stages; a ring loader warp
+//                      brings the h1 / h3 the epilogue needs into shared
+//                      memory by TMA ahead of time (see epilogue_da_ring).
 //   WG:                256 x 256 tiles of dW over the expert's rows.
 constexpr int P_STAGES = 6;
 constexpr int P_HALF = 128 * BK * 2;                  // 16 KB: 128 rows x 64 deep
 constexpr int P_TILE = 256;
-using PairShared = PipeShared<P_STAGES>;
+// DA's epilogue ring: slot = one 32-column chunk of h1 and of h3 for the
+// CTA's 128 rows (64-byte swizzled 32 x 128 boxes)
+constexpr int kRingSlots = 4;
+constexpr int kRingChunk = 128 * 32 * 2;              // 8 KB
+constexpr int kRingSlotBytes = 2 * kRingChunk;
+template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 4 : P_STAGES; }
+template <int MODE> __host__ __device__ constexpr int pair_ring_bytes() { return MODE == kDA ? kRingSlots * kRingSlotBytes : 0; }
+template <int MODE> using PairSharedT = PipeShared<pair_stages<MODE>()>;
+constexpr int kPairThreads = kThreads + 32;           // + DA's ring loader warp
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const int* s_off,
@@ -553,6 +562,10 @@ __device__ __forceinline__ void issue_loads_pair(const Tile& tl, int kb, uint32_
     tma_load_2d_pair(sa, a0, fb, kb * BK, tl.row0 + r128);
     tma_load_3d_pair(sb, b0, fb, tl.n0 + r128, kb * BK, tl.e);
     tma_load_3d_pair(sb + SUB, b0, fb, tl.n0 + r128 + 64, kb * BK, tl.e);
+  } else if constexpr (MODE == kDA) {
+    (void)a1; (void)b1;
+    tma_load_2d_pair(sa, a0, fb, kb * BK, tl.row0 + r128);
+    tma_load_3d_pair(sb, b0, fb, kb * BK, tl.n0 + r128, tl.e);
   } else if constexpr (MODE == kDX) {
     const bool second = kb >= a.kb_split;
     const int kk = (second ? kb - a.kb_split : kb) * BK;
@@ -568,6 +581,90 @@ __device__ __forceinline__ void issue_loads_pair(const Tile& tl, int kb, uint32_
     tma_load_2d_pair(sb, bm, fb, tl.n0 + r128, y);
     tma_load_2d_pair(sb + SUB, bm, fb, tl.n0 + r128 + 64, y);
   }
+}
+
+// DA epilogue on CTA pairs.  The ring loader warp streams, tile after tile,
+// the 8 column chunks of the CTA's 128 rows of h1 and h3 into ring slots
+// (slot g % kRingSlots for chunk g of the sequence); the warps of half h take
+// chunks h, h + 2, h + 4, h + 6.  Each warp reads its 32 rows of the chunk
+// (row r of a slot box at r * 64 bytes, 16-byte piece c at c ^ ((r >> 1) & 3)),
+// forms dh1, dh3 with the accumulator, writes them back over its rows of the
+// slot and stores them from there by TMA (a warp whose rows end inside the
+// chunk writes its rows directly); the slot is released to the loader once
+// the copy engine has read it.  rn = chunks of the sequence before this tile.
+__device__ __forceinline__ bool epilogue_da_ring(const Tile& tl, uint32_t tacc, int lane_q, int half,
+                                                 int lane, uint8_t* ring, uint64_t* rfull,
+                                                 uint64_t* rempty, int* abort_flag, uint32_t rn,
+                                                 const GemmArgs& a, const OutMaps& om) {
+  const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
+  const int nrows = min(32, tl.rows - lane_q * 32);   // this warp's rows in the expert (may be <= 0)
+  const int r0 = tl.row0 + lane_q * 32;
+  const int x = (lane >> 1) & 3;
+#pragma unroll 1
+  for (int s = 0; s < 4; ++s) {
+    const int c = 2 * s + half;
+    const uint32_t g = rn + (uint32_t)c;
+    const int slot = (int)(g % kRingSlots);
+    if (!bounded_wait(smem_u32(&rfull[slot]), (g / kRingSlots) & 1u, abort_flag, a.status)) return false;
+    uint8_t* p1 = ring + slot * kRingSlotBytes + lane_q * 2048 + lane * 64;
+    uint8_t* p3 = p1 + kRingChunk;
+    uint32_t w1[16], w3[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 t1 = *reinterpret_cast<const uint4*>(p1 + 16 * (i ^ x));
+      const uint4 t3 = *reinterpret_cast<const uint4*>(p3 + 16 * (i ^ x));
+      w1[4 * i] = t1.x; w1[4 * i + 1] = t1.y; w1[4 * i + 2] = t1.z; w1[4 * i + 3] = t1.w;
+      w3[4 * i] = t3.x; w3[4 * i + 1] = t3.y; w3[4 * i + 2] = t3.z; w3[4 * i + 3] = t3.w;
+    }
+    uint32_t q[32];
+    tmem_ld32(tbase + c * 32, q);
+    tmem_ld_wait();
+    float g1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float h1 = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+      const float h3 = (i & 1) ? bf16_hi(w3[i >> 1]) : bf16_lo(w3[i >> 1]);
+      const float da = __uint_as_float(q[i]);
+      const float sg = sigmoid_f(h1);
+      g1[i] = da * h3 * sg * (1.f + h1 * (1.f - sg));
+      q[i] = __float_as_uint(da * h1 * sg);                      // dh3 in place
+    }
+    uint4 o1[4], o3[4];
+    pack_row32(g1, o1);
+    pack_row32(reinterpret_cast<const float*>(q), o3);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      *reinterpret_cast<uint4*>(p1 + 16 * (i ^ x)) = o1[i];
+      *reinterpret_cast<uint4*>(p3 + 16 * (i ^ x)) = o3[i];
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    const int col = tl.n0 + c * 32;
+    if (col < a.h && nrows > 0) {
+      if (nrows == 32) {
+        if (lane == 0) {
+          uint8_t* b1 = ring + slot * kRingSlotBytes + lane_q * 2048;
+          tma_store_2d(om.o0, smem_u32(b1), col, r0);
+          tma_store_2d(om.o1, smem_u32(b1 + kRingChunk), col, r0);
+          bulk_commit();
+        }
+      } else if (lane < nrows) {
+        uint16_t* d1 = a.out0 + (size_t)(r0 + lane) * a.ldo + col;
+        uint16_t* d3 = a.out1 + (size_t)(r0 + lane) * a.ldo + col;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          st_v4(d1 + 8 * i, o1[i]);
+          st_v4(d3 + 8 * i, o3[i]);
+        }
+      }
+    }
+    if (lane == 0) {
+      bulk_wait_read_all();
+      mbar_arrive(smem_u32(&rempty[slot]));
+    }
+    __syncwarp();
+  }
+  return true;
 }
 
 // A K-chunk of a split wgrad tile: this CTA's 128 rows x 256 columns of the
@@ -618,7 +715,7 @@ __global__ void __launch_bounds__(P_TILE) wgrad_fixup_kernel(const GemmArgs a) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
 pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                  const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
@@ -627,8 +724,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + P_STAGES * P_HALF;
-  uint8_t* sStage = sB + P_STAGES * P_HALF;
+  constexpr int PS = pair_stages<MODE>();
+  using PairShared = PairSharedT<MODE>;
+  uint8_t* sB = smem + PS * P_HALF;
+  uint8_t* ring = sB + PS * P_HALF;                          // DA only
+  uint8_t* sStage = ring + pair_ring_bytes<MODE>();
   PairShared* sh = reinterpret_cast<PairShared*>(sStage + kEpiWarps * kStageBytes);
   int* s_off = reinterpret_cast<int*>(sh + 1);
   int* s_ts = s_off + (args.E + 1);
@@ -641,13 +741,17 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < P_STAGES; ++s) {
+    for (int s = 0; s < PS; ++s) {
       mbar_init(smem_u32(&sh->full[s]), 1);
       mbar_init(smem_u32(&sh->empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sh->tfull[s]), 1);
       mbar_init(smem_u32(&sh->tempty[s]), 2 * kEpiWarps);
+    }
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(smem_u32(&sh->rfull[s]), 1);
+      mbar_init(smem_u32(&sh->rempty[s]), 4);              // the 4 warps of one half
     }
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
@@ -711,12 +815,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
         __syncwarp();
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == PS) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok && leader && lane == 0) {
       // the even CTA's full barriers count both CTAs' copies
-      for (int s = 0; s < P_STAGES; ++s)
+      for (int s = 0; s < PS; ++s)
         if (issued & (1u << s)) drain_wait(smem_u32(&sh->full[s]), (last_par >> s) & 1u);
     }
     __syncwarp();
@@ -759,7 +863,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
             }
             issued_any = true;
             __syncwarp();
-            if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+            if (++stage == PS) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
           if (lane == 0) { mma_commit_pair(mapa_shared(tf, 0)); mma_commit_pair(mapa_shared(tf, 1)); }
@@ -773,14 +877,15 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
       }
     }
     // the odd CTA's MMA warp only holds its half of the TMEM allocation
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // --------------------------------------------------------------- epilogue
     const int lane_q = warp & 3;
     const int half = (warp - 2) >> 2;
     const OutMaps om{&tmO0, &tmO1, &tmO2};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = pair; t < total; t += npairs) {
+    uint32_t rn = 0;                          // DA: ring chunks of the tiles before
+    for (int t = pair; t < total; t += npairs, rn += 8) {
       Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
       // this CTA's rows of the output tile
       if constexpr (MODE == kWG) {
@@ -798,15 +903,50 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
           whole = false;
         }
       }
-      if (whole)
+      if constexpr (MODE == kDA) {
+        if (!epilogue_da_ring(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane, ring, sh->rfull,
+                              sh->rempty, &sh->abort_flag, rn, args, om))
+          break;
+      } else if (whole) {
         epilogue_tile<MODE>(tl, tmem + (uint32_t)(acc * P_TILE), lane_q, half, lane,
                             sStage + (warp - 2) * kStageBytes, args, om);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tempty[acc]), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     stg_finish(lane);
+  } else if constexpr (MODE == kDA) {
+    // ------------------------------------------------ DA: h1 / h3 ring loader
+    // chunk c of every tile (this CTA's 128 rows, columns n0 + 32c ..) into
+    // slot g % kRingSlots, g counting the chunks in order
+    uint32_t g = 0, issued = 0, last_par = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+      const int y = tl.row0 + 128 * (int)rank;
+      for (int c = 0; c < 8; ++c, ++g) {
+        const int slot = (int)(g % kRingSlots);
+        const uint32_t par = (g / kRingSlots) & 1u;
+        if (!bounded_wait(smem_u32(&sh->rempty[slot]), par ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&sh->rfull[slot]);
+          const uint32_t dst = smem_u32(ring + slot * kRingSlotBytes);
+          mbar_arrive_expect_tx(fb, kRingSlotBytes);
+          tma_load_2d(dst, &tmA1, fb, tl.n0 + 32 * c, y);                  // h1
+          tma_load_2d(dst + kRingChunk, &tmB1, fb, tl.n0 + 32 * c, y);     // h3
+        }
+        __syncwarp();
+        issued |= 1u << slot;
+        last_par = (last_par & ~(1u << slot)) | (par << slot);
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < kRingSlots; ++s)
+        if (issued & (1u << s)) drain_wait(smem_u32(&sh->rfull[s]), (last_par >> s) & 1u);
+    }
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -868,9 +1008,10 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
   return MOE_OK;
 }
 
+template <int MODE>
 constexpr size_t pair_smem_bytes(int E) {
-  return 1024 + (size_t)P_STAGES * 2 * P_HALF + (size_t)kEpiWarps * kStageBytes + sizeof(PairShared) +
-         2 * (size_t)(E + 1) * 4;
+  return 1024 + (size_t)pair_stages<MODE>() * 2 * P_HALF + pair_ring_bytes<MODE>() +
+         (size_t)kEpiWarps * kStageBytes + sizeof(PairSharedT<MODE>) + 2 * (size_t)(E + 1) * 4;
 }
 
 // at[] must hold two attributes: the 2-CTA cluster shape and programmatic
@@ -878,7 +1019,7 @@ constexpr size_t pair_smem_bytes(int E) {
 inline cudaLaunchConfig_t pair_config(int npairs, size_t smem, cudaStream_t s, cudaLaunchAttribute* at) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * npairs);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -894,16 +1035,15 @@ inline cudaLaunchConfig_t pair_config(int npairs, size_t smem, cudaStream_t s, c
 // device on the first call (outside any stream capture that follows).
 template <int MODE>
 int pair_limit(cudaStream_t s) {
-  static_assert(MODE != kDA, "the DA GEMM runs on single CTAs");
   auto kern = pair_gemm_kernel<MODE>;
   static bool attr_done[64] = {false};
   static int limit[64] = {0};
-  if (ensure_smem_attr(kern, pair_smem_bytes(kMaxExperts), attr_done) != MOE_OK) return -1;
+  if (ensure_smem_attr(kern, pair_smem_bytes<MODE>(kMaxExperts), attr_done) != MOE_OK) return -1;
   const int dev = current_device();
   if (dev < 0 || dev >= 64) return -1;
   if (limit[dev] == 0) {
     cudaLaunchAttribute at[2];
-    cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes(kMaxExperts), s, at);
+    cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes<MODE>(kMaxExperts), s, at);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
@@ -925,7 +1065,7 @@ int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   cudaLaunchAttribute at[2];
   const long long ub = tiles_upper > 0 ? tiles_upper : 1;
   const int npairs = (int)(ub < limit ? ub : limit);
-  cudaLaunchConfig_t cfg = pair_config(npairs, pair_smem_bytes(g.E), s, at);
+  cudaLaunchConfig_t cfg = pair_config(npairs, pair_smem_bytes<MODE>(g.E), s, at);
   if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, o.m[0], o.m[1], o.m[2], g) != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_ERR_CUDA;
@@ -1015,14 +1155,22 @@ int run_dact(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_
              moe_bf16_t* dh3, void* ws, cudaStream_t s) {
   MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W2); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3);
   MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dh1); MOE_CHECK_PTR(dh3);
+  const bool pairs = rows_on_pairs(R, E);
   CUtensorMap m_dyp, m_w2k;
-  if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, BN)) return MOE_ERR_CUDA;
+  if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, pairs ? BN / 2 : BN))
+    return MOE_ERR_CUDA;
   GemmArgs g = base_args(offsets, R, E, d, h, ws);
   g.n_tiles = (h + BN - 1) / BN;
   g.kb_total = d / BK;
   g.out0 = dh1; g.out1 = dh3; g.in0 = h1; g.in1 = h3; g.ldo = h;
-  OutDescs o;   // DA stores without TMA; the descriptors are carried along unused
+  OutDescs o;   // TMA stores on pairs; the single-CTA kernel stores without them
   if (!row_outs(&o, R, h, dh1, dh3)) return MOE_ERR_CUDA;
+  if (pairs) {
+    // the epilogue's h1 / h3 ring: 32-column x 128-row boxes
+    CUtensorMap m_h1, m_h3;
+    if (!map2d_out(&m_h1, h1, h, R, h, 128) || !map2d_out(&m_h3, h3, h, R, h, 128)) return MOE_ERR_CUDA;
+    return launch_pair<kDA>(m_dyp, m_h1, m_w2k, m_h3, o, g, row_tiles_upper(R, E, g.n_tiles, P_TILE), s);
+  }
   return launch<kDA>(m_dyp, m_dyp, m_w2k, m_w2k, m_w2k, o, g, row_grid_upper(R, E, g.n_tiles), s);
 }
 
