@@ -236,7 +236,9 @@ struct RowTile {
 };
 
 // Tile t -> expert, first row, valid rows (<= TM) and column-block index;
-// within an expert the row block varies fastest.
+// within an expert the column block varies fastest, so the CTAs working at
+// the same time on one row block read its rows from DRAM once (the expert's
+// weights stay in L2 while its row blocks go by).
 template <int TM = 128>
 __device__ __forceinline__ RowTile decode_row_tile(int t, int E, int R, const int* s_off,
                                                    const int* s_ts) {
@@ -251,8 +253,9 @@ __device__ __forceinline__ RowTile decode_row_tile(int t, int E, int R, const in
   const int seg1 = max(seg0, min(s_off[lo + 1], R));
   const int mt = (seg1 - seg0 + TM - 1) / TM;
   const int l = t - s_ts[lo];
-  const int m_idx = l % mt;
-  r.n_idx = l / mt;
+  const int nt = (s_ts[lo + 1] - s_ts[lo]) / mt;     // column blocks
+  const int m_idx = l / nt;
+  r.n_idx = l % nt;
   r.row0 = seg0 + m_idx * TM;
   r.rows = min(TM, seg1 - r.row0);
   return r;

@@ -19,19 +19,19 @@
 //   WG : dW1[e] = xp_e^T dh1_e, dW3[e] = xp_e^T dh3_e, dW2[e] = a_e^T dyp_e
 //        (the reduction runs over the expert's own rows; K = n_e varies)
 //
-// Tiles are 128 x 256 (BM x BN) with BK = 64; every CTA loops over tiles
-// t = blockIdx.x, blockIdx.x + gridDim.x, ... in expert-major order, so the
-// CTAs working at one time share an expert's weight tile in L2.  The row
-// groups come from `offsets` read on the device: nothing is padded and the
-// host never learns the row counts.
+// Single-CTA tiles are 128 x 256 (BM x BN) with BK = 64; every CTA loops over
+// tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... in expert-major order
+// (column blocks fastest, see decode_row_tile).  The row groups come from
+// `offsets` read on the device: nothing is padded and the host never learns
+// the row counts.  The CTA-pair kernel further down takes 256-row tiles.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads into a 4-stage shared
+// Warp roles (320 threads): warp 0 issues TMA loads into a 4-stage shared
 // memory ring; warp 1 allocates 512 TMEM columns (two 128x256 fp32
-// accumulators) and one of its lanes issues tcgen05.mma; warps 2-5 drain a
-// finished accumulator (tcgen05.ld) while the next tile accumulates into the
-// other one.  Every mbarrier wait is bounded: on timeout the kernel records
-// MOE_DEV_WAIT_TIMEOUT, waits (bounded) for its own in-flight copies and
-// MMAs, frees TMEM and returns.
+// accumulators) and one of its lanes issues tcgen05.mma; warps 2-9 drain a
+// finished accumulator (tcgen05.ld, two warps per TMEM lane quarter) while
+// the next tile accumulates into the other one.  Every mbarrier wait is
+// bounded: on timeout the kernel records MOE_DEV_WAIT_TIMEOUT, waits
+// (bounded) for its own in-flight copies and MMAs, frees TMEM and returns.
 #include "gemm_common.cuh"
 
 namespace moe {
