@@ -356,16 +356,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     // the whole warp walks the schedule (converged); lane 0 issues the copies
     int stage = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
+    int wg_e = -1;                          // WG: expert of the descriptors acquired
+    uint32_t wg_seen = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
       if constexpr (MODE == kWG) {
         // the descriptors were written by an earlier kernel through the
-        // generic proxy; make them visible to the tensormap proxy
+        // generic proxy; make them visible to the tensormap proxy, once per
+        // descriptor (a CTA meets the experts in increasing order)
         if (lane == 0 && tl.nkb > 0) {
+          if (tl.e != wg_e) { wg_e = tl.e; wg_seen = 0; }
           const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
-          tensormap_acquire(em + (tl.which == 2 ? 1 : 0));
-          tensormap_acquire(em + 2 + tl.which);
+          const int oa = tl.which == 2 ? 1 : 0, ob = 2 + tl.which;
+          if (!(wg_seen & (1u << oa))) { tensormap_acquire(em + oa); wg_seen |= 1u << oa; }
+          if (!(wg_seen & (1u << ob))) { tensormap_acquire(em + ob); wg_seen |= 1u << ob; }
         }
       }
       for (int kb = 0; kb < tl.nkb; ++kb) {
@@ -791,16 +796,21 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     // ------------------------------------------------------------ TMA producer
     int stage = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
+    int wg_e = -1;                          // WG: expert of the descriptors acquired
+    uint32_t wg_seen = 0;
     bool ok = true;
     for (int t = pair; t < total && ok; t += npairs) {
       const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
       if constexpr (MODE == kWG) {
         // the descriptors were written by an earlier kernel through the
-        // generic proxy; make them visible to the tensormap proxy
+        // generic proxy; make them visible to the tensormap proxy, once per
+        // descriptor (a CTA meets the experts in increasing order)
         if (lane == 0 && tl.nkb > 0) {
+          if (tl.e != wg_e) { wg_e = tl.e; wg_seen = 0; }
           const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
-          tensormap_acquire(em + (tl.which == 2 ? 1 : 0));
-          tensormap_acquire(em + 2 + tl.which);
+          const int oa = tl.which == 2 ? 1 : 0, ob = 2 + tl.which;
+          if (!(wg_seen & (1u << oa))) { tensormap_acquire(em + oa); wg_seen |= 1u << oa; }
+          if (!(wg_seen & (1u << ob))) { tensormap_acquire(em + ob); wg_seen |= 1u << ob; }
         }
       }
       for (int kb = 0; kb < tl.nkb; ++kb) {

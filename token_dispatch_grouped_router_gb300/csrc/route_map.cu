@@ -80,32 +80,57 @@ route_count_kernel(const int32_t* __restrict__ idx, int R, int E,
   }
 }
 
-// Single block of 1024 threads.  Warp w scans the block histograms of experts
-// w, w + 32, ... over the chunks, 32 chunks a step (one per lane, a warp
-// prefix sum, the running total carried in a register).
+// Single block of 1024 threads.  The block histograms are scanned per expert
+// over the chunks with coalesced accesses: lane = expert (32 consecutive
+// experts per warp), the 32 warps split into G = ceil(E / 32) expert groups
+// times S = 32 / G chunk ranges.  Pass 1: each warp sums its chunk range per
+// expert; the S range sums of an expert are scanned in shared memory; pass 2:
+// each warp rewrites its range with the running exclusive prefix.
+constexpr int kScanWarps = 32;
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   pdl_enter();
   __shared__ int32_t tot[kMaxExperts];
   __shared__ int32_t warp_sums[32];
+  __shared__ int32_t part[kScanWarps * 32];         // [warp] x [lane]: range sums, then bases
   {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int e = warp; e < E; e += 32) {
-      int carry = 0;
-      for (int b0 = 0; b0 < nchunks; b0 += 32) {
-        const int b = b0 + lane;
-        const int c = b < nchunks ? chunk_counts[(size_t)b * E + e] : 0;
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        if (b < nchunks) chunk_counts[(size_t)b * E + e] = carry + incl - c;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+    const int G = (E + 31) / 32, S = kScanWarps / G;
+    const int g = warp / S, j = warp - g * S;
+    const int e = 32 * g + lane;
+    const int C = (nchunks + S - 1) / S;
+    const int b0 = j * C, b1 = min(nchunks, b0 + C);
+    const bool active = g < G && e < E;
+    int sum = 0;
+    if (active) {
+#pragma unroll 8
+      for (int b = b0; b < b1; ++b) sum += chunk_counts[(size_t)b * E + e];
+    }
+    part[warp * 32 + lane] = sum;
+    __syncthreads();
+    // per expert: exclusive scan of its S range sums (thread = expert)
+    for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+      const int gg = ee / 32, l = ee - 32 * gg;
+      int run = 0;
+      for (int jj = 0; jj < S; ++jj) {
+        int* p = &part[(gg * S + jj) * 32 + l];
+        const int v = *p;
+        *p = run;
+        run += v;
       }
-      if (lane == 0) { tot[e] = carry; counts[e] = carry; }
+      tot[ee] = run;
+      counts[ee] = run;
+    }
+    __syncthreads();
+    if (active) {
+      int run = part[warp * 32 + lane];
+      for (int b = b0; b < b1; ++b) {
+        const size_t at = (size_t)b * E + e;
+        const int c = chunk_counts[at];
+        chunk_counts[at] = run;
+        run += c;
+      }
     }
   }
   __syncthreads();
