@@ -84,7 +84,9 @@ def test_router_logits_and_backward(T, d, E, bias):
 
 
 @pytest.mark.parametrize("T,k,E", [(1, 1, 1), (5, 2, 3), (1000, 4, 8), (4096, 4, 128),
-                                   (3000, 8, 1024), (257, 2, 700), (16384, 4, 128)])
+                                   (3000, 8, 1024), (257, 2, 700), (16384, 4, 128),
+                                   # many chunk histograms per expert group of the scan
+                                   (65536, 4, 128), (40000, 8, 33), (33000, 8, 8)])
 def test_route_map_bit_exact(T, k, E):
     rng = np.random.default_rng(T + E)
     if E >= 64:

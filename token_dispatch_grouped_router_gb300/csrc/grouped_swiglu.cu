@@ -486,9 +486,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 //   UP, DOWN, DX:      256-row tiles of an expert's rows; UP splits B into
 //                      W1 columns (even CTA) and W3 columns (odd CTA), so the
 //                      accumulator keeps the single-CTA column layout.
-//   DA:                256-row tiles like DOWN, 4 stages; a ring loader warp
+//   DA:                256-row tiles like DOWN, 5 stages; a ring loader warp
 //                      brings the h1 / h3 the epilogue needs into shared
-//                      memory by TMA ahead of time (see epilogue_da_ring).
+//                      memory by TMA ahead of time (see epilogue_da_ring); no
+//                      staging buffers (its stores go out of the ring slots),
+//                      and at most pair_max_experts<kDA>() experts (the tile
+//                      table shares the 227 KB).
 //   WG:                256 x 256 tiles of dW over the expert's rows.
 constexpr int P_STAGES = 6;
 constexpr int P_HALF = 128 * BK * 2;                  // 16 KB: 128 rows x 64 deep
@@ -498,8 +501,9 @@ constexpr int P_TILE = 256;
 constexpr int kRingSlots = 4;
 constexpr int kRingChunk = 128 * 32 * 2;              // 8 KB
 constexpr int kRingSlotBytes = 2 * kRingChunk;
-template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 4 : P_STAGES; }
+template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_STAGES; }
 template <int MODE> __host__ __device__ constexpr int pair_ring_bytes() { return MODE == kDA ? kRingSlots * kRingSlotBytes : 0; }
+template <int MODE> __host__ __device__ constexpr int pair_stage_bytes() { return MODE == kDA ? 0 : kEpiWarps * kStageBytes; }
 template <int MODE> using PairSharedT = PipeShared<pair_stages<MODE>()>;
 constexpr int kPairThreads = kThreads + 32;           // + DA's ring loader warp
 
@@ -733,8 +737,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   using PairShared = PairSharedT<MODE>;
   uint8_t* sB = smem + PS * P_HALF;
   uint8_t* ring = sB + PS * P_HALF;                          // DA only
-  uint8_t* sStage = ring + pair_ring_bytes<MODE>();
-  PairShared* sh = reinterpret_cast<PairShared*>(sStage + kEpiWarps * kStageBytes);
+  uint8_t* sStage = ring + pair_ring_bytes<MODE>();                 // not DA
+  PairShared* sh = reinterpret_cast<PairShared*>(sStage + pair_stage_bytes<MODE>());
   int* s_off = reinterpret_cast<int*>(sh + 1);
   int* s_ts = s_off + (args.E + 1);
 
@@ -1021,8 +1025,20 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
 template <int MODE>
 constexpr size_t pair_smem_bytes(int E) {
   return 1024 + (size_t)pair_stages<MODE>() * 2 * P_HALF + pair_ring_bytes<MODE>() +
-         (size_t)kEpiWarps * kStageBytes + sizeof(PairSharedT<MODE>) + 2 * (size_t)(E + 1) * 4;
+         (size_t)pair_stage_bytes<MODE>() + sizeof(PairSharedT<MODE>) + 2 * (size_t)(E + 1) * 4;
 }
+// the largest expert count whose tile table still fits beside the pipeline
+// in the 227 KB of shared memory a block may opt in to
+constexpr size_t kSmemOptIn = 227 * 1024;
+template <int MODE>
+constexpr int pair_max_experts() {
+  const long long room = (long long)kSmemOptIn - (long long)pair_smem_bytes<MODE>(0) + 8;
+  const long long e = room / 8 - 1;
+  return e < kMaxExperts ? (int)e : kMaxExperts;
+}
+static_assert(pair_max_experts<kUp>() == kMaxExperts && pair_max_experts<kWG>() == kMaxExperts,
+              "the 6-stage pair GEMMs fit every expert count");
+static_assert(pair_max_experts<kDA>() >= 128, "DA on pairs covers pools of 128 experts");
 
 // at[] must hold two attributes: the 2-CTA cluster shape and programmatic
 // stream serialisation (see launch_pdl)
@@ -1048,12 +1064,12 @@ int pair_limit(cudaStream_t s) {
   auto kern = pair_gemm_kernel<MODE>;
   static bool attr_done[64] = {false};
   static int limit[64] = {0};
-  if (ensure_smem_attr(kern, pair_smem_bytes<MODE>(kMaxExperts), attr_done) != MOE_OK) return -1;
+  if (ensure_smem_attr(kern, pair_smem_bytes<MODE>(pair_max_experts<MODE>()), attr_done) != MOE_OK) return -1;
   const int dev = current_device();
   if (dev < 0 || dev >= 64) return -1;
   if (limit[dev] == 0) {
     cudaLaunchAttribute at[2];
-    cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes<MODE>(kMaxExperts), s, at);
+    cudaLaunchConfig_t q = pair_config(sm_count(), pair_smem_bytes<MODE>(pair_max_experts<MODE>()), s, at);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
@@ -1165,7 +1181,7 @@ int run_dact(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_
              moe_bf16_t* dh3, void* ws, cudaStream_t s) {
   MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W2); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3);
   MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dh1); MOE_CHECK_PTR(dh3);
-  const bool pairs = rows_on_pairs(R, E);
+  const bool pairs = rows_on_pairs(R, E) && E <= pair_max_experts<kDA>();
   CUtensorMap m_dyp, m_w2k;
   if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, pairs ? BN / 2 : BN))
     return MOE_ERR_CUDA;
