@@ -7,8 +7,8 @@ One step = one pass of the whole layer over one batch: router gates (or
 router GEMM + top-k), device route map, rowwise dispatch, grouped SwiGLU GEMMs
 (up, down), combine, combine backward, grouped GEMM backward (dact, dx,
 wgrad), unpermute-sum and router backward.  Inputs are seeded synthetic
-tensors resident in HBM.  Between timed steps a 512 MB buffer is written to
-flush the 129 MB L2; every library call of a step is bracketed by CUDA events
+tensors resident in HBM.  Between timed steps a 256 MB buffer is written to
+flush the 129 MB L2 (twice over); every library call of a step is bracketed by CUDA events
 on the launching stream, so the per-kernel times below come from the timed
 steps themselves.
 
@@ -38,7 +38,7 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tok/s fwd+bwd at E=8..128, k=4; grouped-GEMM % peak; dispatch GB/s"
 UNIT = "tok/s"
-FLUSH_BYTES = 512 << 20
+FLUSH_BYTES = 256 << 20   # twice the L2
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = {
     "gemm": ["grouped_swiglu.cu", "gemm_common.cuh", "sm103_ptx.cuh", "common.cuh"],
@@ -415,7 +415,7 @@ def run_ours(args):
         "data": "synthetic: seeded normals (x, W, dY), uniform random top-4 routing",
         "config": {"workload": w.name, "key": w.key, "T": w.T, "d": w.d, "E": w.E, "k": w.k,
                    "h": w.h, "routing": w.routing, "tokens_per_gpu": w.T,
-                   "l2": "flushed between timed steps (512 MB write)",
+                   "l2": "flushed between timed steps (256 MB write, twice the L2)",
                    "parallelism": f"{world} replica(s), token-sharded, no data-path collective"},
         "roofline": roof,
         "gemm": {"tflops": gemm_tflops, "frac_of_peak": gemm_tflops / peaks["bf16_tflops_sustained"],
