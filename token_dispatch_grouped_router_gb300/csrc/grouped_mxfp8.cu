@@ -109,12 +109,18 @@ __device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr) {
   return d;
 }
 
+// Whole 32-row slices of the bf16 outputs leave by TMA store (o0..o2: UP8
+// h1, h3, a; DOWN8 yp; see store_chunk_tma); a slice cut by the end of an
+// expert's rows, and the fp8 codes of a, by coalesced stores of its own rows.
 template <int MODE>
 __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t tacc, int lane_q,
-                                          int half, int lane, uint8_t* stg, const Args8& a) {
+                                          int half, int lane, uint8_t* stg, const Args8& a,
+                                          const CUtensorMap* o0, const CUtensorMap* o1,
+                                          const CUtensorMap* o2) {
   const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
   const int nrows = min(32, rt.rows - lane_q * 32);
   const size_t r0 = (size_t)rt.row0 + (nrows > 0 ? lane_q * 32 : 0);
+  const bool whole = nrows == 32;
   if constexpr (MODE == kUp8) {
     // columns 0..95: h1[:, n0..n0+95]; 96..191: h3[:, n0..n0+95]; three
     // 32-column chunks, two for the first half of the warps, one for the second
@@ -135,9 +141,16 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
         av[i] = silu_f(h1[i]) * h3[i];
         amax = fmaxf(amax, fabsf(av[i]));
       }
-      store_chunk(stg, h1, lane, a.out0 + r0 * a.h + col, a.h, nrows);
-      store_chunk(stg, h3, lane, a.out1 + r0 * a.h + col, a.h, nrows);
-      store_chunk(stg, av, lane, a.out2 + r0 * a.h + col, a.h, nrows);
+      if (whole) {
+        store_chunk_tma(stg, h1, lane, o0, col, (int)r0);
+        store_chunk_tma(stg, h3, lane, o1, col, (int)r0);
+        store_chunk_tma(stg, av, lane, o2, col, (int)r0);
+      } else {
+        stg_acquire(lane);
+        store_chunk(stg, h1, lane, a.out0 + r0 * a.h + col, a.h, nrows);
+        store_chunk(stg, h3, lane, a.out1 + r0 * a.h + col, a.h, nrows);
+        store_chunk(stg, av, lane, a.out2 + r0 * a.h + col, a.h, nrows);
+      }
       // quantise this row's 32-column block of a (fp32 values, before rounding)
       const int ex = mx::block_exponent(amax);
       const float inv = mx::inv_scale(ex);
@@ -146,6 +159,7 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         w[i] = mx::e4m3x4(av[4 * i] * inv, av[4 * i + 1] * inv, av[4 * i + 2] * inv, av[4 * i + 3] * inv);
+      stg_acquire(lane);
       store_chunk_bytes32(stg, o, lane, a.aq + r0 * a.h + col, a.h, nrows);
       if (lane < nrows) a.as[(r0 + lane) * (a.h / 32) + col / 32] = (uint8_t)(ex + 127);
     }
@@ -160,7 +174,12 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(q[i]);
-      store_chunk(stg, v, lane, a.out0 + r0 * a.d + col, a.d, nrows);
+      if (whole) {
+        store_chunk_tma(stg, v, lane, o0, col, (int)r0);
+      } else {
+        stg_acquire(lane);
+        store_chunk(stg, v, lane, a.out0 + r0 * a.d + col, a.d, nrows);
+      }
     }
   }
 }
@@ -168,7 +187,9 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, const Args8 args) {
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
+                     const Args8 args) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -206,7 +227,10 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) { prefetch_tmap(&tmA); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1); }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmO0); prefetch_tmap(&tmO1); prefetch_tmap(&tmO2);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -326,12 +350,14 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       const int n0 = rt.n_idx * (MODE == kUp8 ? BN / 2 : BN);
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue8<MODE>(rt, n0, tmem + (uint32_t)(acc * kAccStride), lane_q, half, lane, stg, args);
+      epilogue8<MODE>(rt, n0, tmem + (uint32_t)(acc * kAccStride), lane_q, half, lane, stg, args,
+                      &tmO0, &tmO1, &tmO2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    stg_finish(lane);
   }
 
   tc_fence_before();
@@ -348,12 +374,12 @@ constexpr size_t smem_bytes8(int E) {
 }
 
 template <int MODE>
-int launch8(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Args8& args,
-            int grid, cudaStream_t s) {
+int launch8(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& o0,
+            const CUtensorMap& o1, const CUtensorMap& o2, const Args8& args, int grid, cudaStream_t s) {
   auto kern = grouped_mxfp8_kernel<MODE>;
   static bool attr_done[64] = {false};
   if (ensure_smem_attr(kern, smem_bytes8(kMaxExperts8), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  (void)launch_pdl(kern, grid, kThreads, smem_bytes8(args.E), s, a, b0, b1, args);
+  (void)launch_pdl(kern, grid, kThreads, smem_bytes8(args.E), s, a, b0, b1, o0, o1, o2, args);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -393,12 +419,16 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   g.K = d; g.kb_total = d / BK; g.n_tiles = (h + BN / 2 - 1) / (BN / 2); g.N = h;
   g.sfa = xs; g.sfb0 = w1s; g.sfb1 = w3s;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.aq = aq; g.as = as;
-  int st = launch8<kUp8>(mx, mw1, mw3, g, row_grid_upper(R, E, g.n_tiles), s);
+  CUtensorMap mo_h1, mo_h3, mo_a, mo_yp;
+  if (!map2d_out(&mo_h1, h1, h, R, h) || !map2d_out(&mo_h3, h3, h, R, h) ||
+      !map2d_out(&mo_a, a, h, R, h) || !map2d_out(&mo_yp, yp, d, R, d))
+    return MOE_ERR_CUDA;
+  int st = launch8<kUp8>(mx, mw1, mw3, mo_h1, mo_h3, mo_a, g, row_grid_upper(R, E, g.n_tiles), s);
   if (st != MOE_OK) return st;
   // down-projection: K = h
   Args8 g2 = g;
   g2.K = h; g2.kb_total = h / BK; g2.n_tiles = (d + BN - 1) / BN; g2.N = d;
   g2.sfa = as; g2.sfb0 = w2s; g2.sfb1 = w2s;
   g2.out0 = yp; g2.out1 = nullptr; g2.out2 = nullptr; g2.aq = nullptr; g2.as = nullptr;
-  return launch8<kDown8>(ma, mw2, mw2, g2, row_grid_upper(R, E, g2.n_tiles), s);
+  return launch8<kDown8>(ma, mw2, mw2, mo_yp, mo_yp, mo_yp, g2, row_grid_upper(R, E, g2.n_tiles), s);
 }
