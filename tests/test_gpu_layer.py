@@ -91,6 +91,9 @@ def compare_full(layer, w, inp, backward=True):
     # the weight-gradient tiles split along the rows (fp32 partials, ordered
     # sum) with an empty expert among them
     (3000, 256, 3, 1, 256, (0,)),
+    # more experts than DA's CTA-pair tile table holds: DA on single CTAs
+    # beside the CTA-pair UP, DOWN, DX and wgrad GEMMs
+    (31000, 64, 240, 4, 64, ()),
 ])
 def test_layer_small_full_compare(T, d, E, k, h, empty):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
