@@ -293,9 +293,17 @@ def run_ours(args):
                 "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
                 "launches": launches, "clocks": clocks, "wall_s": wall}
 
+    def tile_overhead(layer):
+        """Rows the row-grouped GEMMs multiply beyond the T*k routed rows: each
+        expert's last tile of 256 (CTA pairs) or 128 rows (single CTAs) is only
+        partly filled.  Read from the device counts after the timed steps."""
+        c = layer.counts.cpu().numpy().astype(np.int64)
+        return {f"tiles_{t}": float((-(-c // t) * t).sum() / layer.R - 1.0) for t in (256, 128)}
+
     def timed(w, inp, K, W, with_e2e, sample_clocks=True):
         layer = make_layer(w, inp)
         res = timed_layer(layer, K, W, sample_clocks=sample_clocks)
+        res["row_tile_overhead"] = tile_overhead(layer)
         if with_e2e:
             res["e2e"] = e2e(layer, inp, K)
             # the recompute policy (Xp gathered again, H1/H3/A recomputed in
@@ -430,6 +438,7 @@ def run_ours(args):
         "e2e": main["e2e"],
         "gpu_launches": main["launches"],
         "clocks": main["clocks"],
+        "row_tile_overhead": main["row_tile_overhead"],
     }
     rec = main["recompute"]
     out["recompute"] = {
@@ -443,7 +452,8 @@ def run_ours(args):
         cv = world * wl.get_workload(args.compare).T / (cmp_res["ms_per_step"] / 1e3)
         out["compare"] = {"workload": cmp_res["workload"], "value": cv, "unit": UNIT,
                           "ms_per_step": cmp_res["ms_per_step"], "ratio_to_main": cv / value,
-                          "kernels_ms": cmp_res["kernels_ms"], "gpu_launches": cmp_res["launches"]}
+                          "kernels_ms": cmp_res["kernels_ms"], "gpu_launches": cmp_res["launches"],
+                          "row_tile_overhead": cmp_res["row_tile_overhead"]}
     if mx_res is not None:
         w3, bf, mx, mxc = mx_res
         fl, _ = work_per_launch(w3)

@@ -1100,11 +1100,19 @@ int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   return MOE_OK;
 }
 
-// UP, DOWN and DX run on CTA pairs (256-row tiles) unless the experts are
+// UP, DOWN, DA and DX run on CTA pairs (256-row tiles) unless the experts are
 // small on average: then the 128-row tiles of the single-CTA kernel waste
-// less on each expert's last, partial tile.
+// less on each expert's last, partial tile.  DX (K = 2h, the longest
+// mainloop per tile) gains least from the pairs: with about 512 rows per
+// expert its single-CTA form is the faster one (event-timed on the GB300,
+// T = 16384, d = 2048, h = 1024, E = 128, top-4: 404 vs 417 us uniform,
+// 348 vs 357 us Zipf-skewed; at 1024 rows per expert 718 vs 718 us), so it
+// moves to pairs only from 1024 rows per expert.
 constexpr long long kPairMinRowsPerExpert = 512;
-inline bool rows_on_pairs(int R, int E) { return (long long)R >= kPairMinRowsPerExpert * E; }
+constexpr long long kPairMinRowsPerExpertDX = 1024;
+inline bool rows_on_pairs(int R, int E, long long min_rows = kPairMinRowsPerExpert) {
+  return (long long)R >= min_rows * E;
+}
 
 int check_common(const void* ws, size_t ws_bytes, int R, int E, int d, int h) {
   if (R < 0 || E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
@@ -1206,7 +1214,7 @@ int run_dx(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t*
            void* ws, cudaStream_t s) {
   MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W1); MOE_CHECK_PTR(W3); MOE_CHECK_PTR(dh1);
   MOE_CHECK_PTR(dh3); MOE_CHECK_PTR(dxp);
-  const bool pairs = rows_on_pairs(R, E);
+  const bool pairs = rows_on_pairs(R, E, kPairMinRowsPerExpertDX);
   const uint32_t bn = pairs ? BN / 2 : BN;
   CUtensorMap m_dh1, m_dh3, m_w1k, m_w3k;
   if (!map2d(&m_dh1, dh1, h, R, 64, BM) || !map2d(&m_dh3, dh3, h, R, 64, BM) ||
