@@ -292,6 +292,22 @@ int moe_mxfp8_quantize_rows(const moe_bf16_t* src, int rows, int K, uint8_t* q,
 int moe_mxfp8_quantize_weights(const moe_bf16_t* W, int E, int K, int N,
                                uint8_t* wq, uint8_t* ws, moe_stream_t stream);
 
+/* The same from fp32 master weights W[E][K][N] (one rounding, fp32 -> E4M3).
+ * The page keeps the FP32 master weights authoritative and re-makes the
+ * low-precision copies after each optimizer step (same section).  Same layout,
+ * limits and errors as moe_mxfp8_quantize_weights. */
+int moe_mxfp8_quantize_weights_f32(const float* W, int E, int K, int N,
+                                   uint8_t* wq, uint8_t* ws, moe_stream_t stream);
+
+/* q[rows][K] codes with scale[rows][K/32] -> out[rows][K] bf16, each value
+ * code * 2^(scale - 127) rounded to bf16 (RNE; exact for every value at or
+ * above 2^-126).  For activations kept in MXFP8 between the forward and the
+ * backward (the page also quantises saved activations, same section): the
+ * bf16 backward reads them back through this call.  K % 32 == 0; q and out
+ * 16-byte aligned; scale bytes of 255 (E8M0 NaN) are out of contract. */
+int moe_mxfp8_dequantize_rows(const uint8_t* q, const uint8_t* scale, int rows, int K,
+                              moe_bf16_t* out, moe_stream_t stream);
+
 /* Rowwise dispatch of quantised rows: each token row is quantised once along d
  * and written to its k expert rows: xq[R][d] codes, xs[R][d/32] scales; the
  * bf16 row also goes to xp[R][d] when xp != NULL (the backward stays bf16).
@@ -303,7 +319,9 @@ int moe_dispatch_rows_mxfp8(const moe_bf16_t* x, int T, int d, int k,
 /* Forward of the grouped SwiGLU FFN with MXFP8 GEMM operands and fp32
  * accumulation (block-scaled tcgen05 MMA): h1 = Xq_e W1q[e], h3 = Xq_e W3q[e],
  * a = silu(h1) * h3 (bf16 h1, h3, a for the bf16 backward), a quantised along
- * h into aq[R][h] / as[R][h/32], yp = Aq_e W2q[e] (bf16).  Weights come from
+ * h into aq[R][h] / as[R][h/32], yp = Aq_e W2q[e] (bf16).  a may be NULL:
+ * then only its quantised form is written (a caller that keeps the saved
+ * activation in MXFP8 and dequantises it for the backward).  Weights come from
  * moe_mxfp8_quantize_weights (w1q/w3q [E][h][d], w2q [E][d][h]).  d and h
  * must be multiples of 128 and E <= 768 (MOE_ERR_UNSUPPORTED otherwise: the
  * kernels keep an E-sized tile table beside 128 x 256 operand tiles in shared

@@ -69,6 +69,43 @@ def test_quantize_weights_bit_exact(E, K, N):
         assert np.array_equal(gq[e], qr.T), e
 
 
+@pytest.mark.parametrize("E,K,N", [(2, 64, 128), (3, 256, 384), (8, 2048, 1024)])
+def test_quantize_weights_from_fp32_masters_bit_exact(E, K, N):
+    # fp32 masters carry bits below bf16's mantissa: one rounding to E4M3
+    rng = np.random.default_rng(E * K + 1)
+    W = (rng.standard_normal((E, K, N)) / np.sqrt(K)).astype(np.float32)
+    W[0, :32, 0] = 0.0                                      # an all-zero block
+    W[0, :32, 1] = np.float32(448.0) * np.float32(2.0) ** -7  # a block max that fits exactly
+    W[-1, -32:, -1] *= np.float32(1e-35)                    # fp32 subnormals and tiny values
+    W[-1, -32:, -2] *= np.float32(1e30)
+    wq = torch.empty(E, N, K, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(E, N, K // 32, dtype=torch.uint8, device=DEV)
+    L.moe_mxfp8_quantize_weights_f32(torch.from_numpy(W).to(DEV), wq, ws)
+    gq, gs = u8(wq), u8(ws)
+    for e in range(E):
+        qr, sr = om.quantize_blocks(W[e].astype(np.float64), axis=0)
+        assert np.array_equal(gs[e], sr.T), e
+        assert np.array_equal(gq[e], qr.T), e
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (37, 96), (513, 2048)])
+def test_dequantize_rows_bit_exact(rows, K):
+    # codes and scales from the oracle's quantiser, including tiny and huge
+    # scales; the device value code * 2^(s-127) rounded to bf16 must equal the
+    # oracle's exact value rounded to bf16 (RNE, by torch)
+    rng = np.random.default_rng(rows * K)
+    x = _edge_values(rng, max(rows, 5), K)[:rows]
+    qr, sr = om.quantize_blocks(x, axis=1)
+    q = torch.from_numpy(qr).to(DEV)
+    s = torch.from_numpy(np.ascontiguousarray(sr)).to(DEV)
+    out = torch.empty(rows, K, dtype=torch.bfloat16, device=DEV)
+    L.moe_mxfp8_dequantize_rows(q, s, out)
+    exact = om.dequantize_blocks(qr, sr, axis=1)
+    assert np.array_equal(exact.astype(np.float32).astype(np.float64), exact)   # exact in fp32
+    ref = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+
+
 @pytest.mark.parametrize("T,d,k", [(5, 32, 1), (300, 2048, 4), (77, 96, 2)])
 def test_dispatch_mxfp8_bit_exact(T, d, k):
     E = 8
@@ -208,6 +245,45 @@ def test_layer_step_mxfp8_forward_bf16_backward():
     assert_close(layer.out, ol.combine(f["Yp"], ros, g, k), "out", rel_l2=MX_REL_L2, max_abs=0.1)
     dYp, dg = ol.combine_backward(inp["dY"], f["Yp"], ros, g, k)
     b = ol.expert_ffn_backward(Xp, off, inp["W1"], inp["W3"], inp["W2"], f["H1"], f["H3"], f["A"], dYp)
+    for n, key in (("dxp", "dXp"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2")):
+        assert_close(getattr(layer, n), b[key], n, rel_l2=MX_REL_L2, max_abs=0.1)
+    assert_close(layer.dgate, dg, "dgate", rel_l2=MX_REL_L2, max_abs=0.1)
+
+
+@pytest.mark.parametrize("T,E,k", [(500, 8, 2), (2600, 4, 2)])   # 128-row tiles / several per expert
+def test_layer_step_mxfp8_saved_activations(T, E, k):
+    # the MXFP8 step that keeps Xp and A only as codes + scales: the forward
+    # writes no bf16 copy of either, the backward reads them back dequantised.
+    # The oracle composes its quantise->dequantise forward with the analytic
+    # backward at the dequantised Xp and A.
+    from token_dispatch_grouped_router_gb300.layer import MoELayer
+    w = wl.small_workload(T=T, d=256, E=E, k=k, h=256)
+    inp = wl.generate(w, seed=6)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=False, device=DEV)
+    layer.load_inputs(inp)
+    layer.enable_mxfp8()
+    layer.xp.fill_(float("nan")); layer.a.fill_(float("nan"))     # nothing may read stale copies
+    L.moe_reset_status(layer.ws)
+    layer.quantize_weights()
+    layer.forward_mxfp8(saved="mxfp8")
+    torch.cuda.synchronize()
+    assert torch.isnan(layer.xp.float()).all() and torch.isnan(layer.a.float()).all()
+    layer.restore_saved_mxfp8()
+    layer.backward()
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    g = ol.softmax_gates(inp["glogit"])
+    _, off, ros, _ = ol.route_map(inp["idx"], E)
+    Xp = ol.dispatch(inp["x"], ros, k)
+    f = om.expert_ffn_forward_mxfp8(Xp, off, inp["W1"], inp["W3"], inp["W2"])
+    Xq = om.qdq(Xp, axis=1)
+    # the dequantised rows are exactly the oracle's quantise->dequantise rows
+    assert np.array_equal(as_f64(layer.xp), Xq)
+    Aq = om.qdq(f["A"], axis=1)
+    assert_close(layer.a, Aq, "a (dequantised)", rel_l2=MX_REL_L2, max_abs=0.1)
+    assert_close(layer.out, ol.combine(f["Yp"], ros, g, k), "out", rel_l2=MX_REL_L2, max_abs=0.1)
+    dYp, dg = ol.combine_backward(inp["dY"], f["Yp"], ros, g, k)
+    b = ol.expert_ffn_backward(Xq, off, inp["W1"], inp["W3"], inp["W2"], f["H1"], f["H3"], Aq, dYp)
     for n, key in (("dxp", "dXp"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2")):
         assert_close(getattr(layer, n), b[key], n, rel_l2=MX_REL_L2, max_abs=0.1)
     assert_close(layer.dgate, dg, "dgate", rel_l2=MX_REL_L2, max_abs=0.1)

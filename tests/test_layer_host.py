@@ -14,3 +14,16 @@ def test_recompute_keeps_fewer_activation_bytes():
     assert b["saved"] - b["recompute"] == 2 * R * d + 3 * 2 * R * h
     # what both keep: Yp and x (bf16) and the int32 / fp32 routing tensors
     assert b["recompute"] == 2 * R * d + 2 * T * d + 4 * (3 * T * k + 2 * R + 2 * E + 1)
+
+
+def test_mxfp8_saved_activations_keep_codes_and_scales():
+    B.build()
+    T, d, E, k, h = 64, 128, 4, 2, 192
+    layer = MoELayer(T, d, E, k, h, learned=False, device="cpu")
+    b = layer.activation_bytes()
+    R = T * k
+    # Xp and A go from bf16 (2 bytes) to one E4M3 byte plus one scale byte per
+    # 32 values; H1 and H3 stay bf16
+    assert b["saved"] - b["mxfp8_saved"] == (2 * R * d - (R * d + R * d // 32)) + \
+        (2 * R * h - (R * h + R * h // 32))
+    assert b["recompute"] < b["mxfp8_saved"] < b["saved"]

@@ -141,15 +141,16 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
         av[i] = silu_f(h1[i]) * h3[i];
         amax = fmaxf(amax, fabsf(av[i]));
       }
+      // (a caller that keeps only the quantised a passes no bf16 a)
       if (whole) {
         store_chunk_tma(stg, h1, lane, o0, col, (int)r0);
         store_chunk_tma(stg, h3, lane, o1, col, (int)r0);
-        store_chunk_tma(stg, av, lane, o2, col, (int)r0);
+        if (a.out2) store_chunk_tma(stg, av, lane, o2, col, (int)r0);
       } else {
         stg_acquire(lane);
         store_chunk(stg, h1, lane, a.out0 + r0 * a.h + col, a.h, nrows);
         store_chunk(stg, h3, lane, a.out1 + r0 * a.h + col, a.h, nrows);
-        store_chunk(stg, av, lane, a.out2 + r0 * a.h + col, a.h, nrows);
+        if (a.out2) store_chunk(stg, av, lane, a.out2 + r0 * a.h + col, a.h, nrows);
       }
       // quantise this row's 32-column block of a (fp32 values, before rounding)
       const int ex = mx::block_exponent(amax);
@@ -401,8 +402,9 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (R == 0) return MOE_OK;
   MOE_CHECK_PTR(xq); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(w1q); MOE_CHECK_PTR(w3q);
-  MOE_CHECK_PTR(w2q); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(a); MOE_CHECK_PTR(aq);
+  MOE_CHECK_PTR(w2q); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(aq);
   MOE_CHECK_PTR(yp);
+  if (a != nullptr && !aligned16(a)) return MOE_ERR_INVALID_ARG;      // a may be NULL
   // scale tables are read 4 bytes at a time
   auto al4 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
   if (!al4(xs) || !al4(w1s) || !al4(w3s) || !al4(w2s) || as == nullptr) return MOE_ERR_INVALID_ARG;
@@ -421,7 +423,7 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.aq = aq; g.as = as;
   CUtensorMap mo_h1, mo_h3, mo_a, mo_yp;
   if (!map2d_out(&mo_h1, h1, h, R, h) || !map2d_out(&mo_h3, h3, h, R, h) ||
-      !map2d_out(&mo_a, a, h, R, h) || !map2d_out(&mo_yp, yp, d, R, d))
+      !map2d_out(&mo_a, a ? a : h1, h, R, h) || !map2d_out(&mo_yp, yp, d, R, d))
     return MOE_ERR_CUDA;
   int st = launch8<kUp8>(mx, mw1, mw3, mo_h1, mo_h3, mo_a, g, row_grid_upper(R, E, g.n_tiles), s);
   if (st != MOE_OK) return st;

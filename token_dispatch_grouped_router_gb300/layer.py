@@ -195,26 +195,51 @@ class MoELayer:
         L.moe_mxfp8_quantize_weights(self.W3, self.w3q, self.w3s)
         L.moe_mxfp8_quantize_weights(self.W2, self.w2q, self.w2s)
 
-    def forward_mxfp8(self, mark=None) -> torch.Tensor:
-        """Forward with MXFP8 GEMM operands; h1, h3, a and xp are also kept in
-        bf16 so that the backward (bf16) can follow unchanged."""
+    def quantize_weights_from_masters(self, W1m: torch.Tensor, W3m: torch.Tensor,
+                                      W2m: torch.Tensor) -> None:
+        """Re-make the MXFP8 weight copies from fp32 master weights (shapes of
+        W1, W3, W2): one rounding instead of fp32 -> bf16 -> E4M3."""
+        L.moe_mxfp8_quantize_weights_f32(W1m, self.w1q, self.w1s)
+        L.moe_mxfp8_quantize_weights_f32(W3m, self.w3q, self.w3s)
+        L.moe_mxfp8_quantize_weights_f32(W2m, self.w2q, self.w2s)
+
+    def forward_mxfp8(self, mark=None, saved: str = "bf16") -> torch.Tensor:
+        """Forward with MXFP8 GEMM operands.  saved="bf16": h1, h3, a and xp
+        are also written in bf16 for the bf16 backward.  saved="mxfp8": the
+        expert rows and the SwiGLU activation are kept only quantised (xq/xs,
+        aq/as); ``restore_saved_mxfp8`` dequantises them for the backward."""
+        if saved not in ("bf16", "mxfp8"):
+            raise ValueError(f"saved must be 'bf16' or 'mxfp8', not {saved!r}")
         mark = mark or _nomark
+        keep_bf16 = saved == "bf16"
         self.route(mark)
         mark("dispatch_mxfp8")
-        L.moe_dispatch_rows_mxfp8(self.x, self.row_of_slot, self.k, self.xq, self.xs, self.xp)
+        L.moe_dispatch_rows_mxfp8(self.x, self.row_of_slot, self.k, self.xq, self.xs,
+                                  self.xp if keep_bf16 else None)
         mark("gemm_fwd_mxfp8")
         L.moe_grouped_swiglu_fwd_mxfp8(self.xq, self.xs, self.offsets, self.w1q, self.w1s,
                                        self.w3q, self.w3s, self.w2q, self.w2s, self.h1, self.h3,
-                                       self.a, self.aq, self.as_, self.yp, self.ws)
+                                       self.a if keep_bf16 else None, self.aq, self.as_, self.yp,
+                                       self.ws)
         mark("combine")
         L.moe_combine(self.yp, self.row_of_slot, self.gate, self.k, self.out)
         return self.out
 
-    def step_mxfp8(self, mark=None, requantize: bool = True) -> None:
+    def restore_saved_mxfp8(self, mark=None) -> None:
+        """bf16 Xp and A for the backward from their MXFP8 forms (each value is
+        code * 2^(scale - 127), exact in bf16 for these magnitudes)."""
+        mark = mark or _nomark
+        mark("mx_dequantize_saved")
+        L.moe_mxfp8_dequantize_rows(self.xq, self.xs, self.xp)
+        L.moe_mxfp8_dequantize_rows(self.aq, self.as_, self.a)
+
+    def step_mxfp8(self, mark=None, requantize: bool = True, saved: str = "bf16") -> None:
         if requantize:
             self.quantize_weights(mark)
-        self.forward_mxfp8(mark)
+        self.forward_mxfp8(mark, saved=saved)
         if self.with_backward:
+            if saved == "mxfp8":
+                self.restore_saved_mxfp8(mark)
             self.backward(mark)
         if mark is not None:
             mark("end")
@@ -228,10 +253,15 @@ class MoELayer:
 
     def activation_bytes(self) -> Dict[str, int]:
         """Bytes the forward leaves for the backward, by policy: the expert
-        rows Xp and H1, H3, A when saved; Yp, the routing and x in both."""
+        rows Xp and H1, H3, A in bf16 ("saved"); Xp and A as MXFP8 codes with
+        their scales and H1, H3 in bf16 ("mxfp8_saved"); none of them
+        ("recompute").  Yp, the routing and x are kept in every policy."""
         R, d, h, T, k, E = self.R, self.d, self.h, self.T, self.k, self.E
         common = 2 * R * d + 2 * T * d + 4 * (3 * T * k + 2 * R + 2 * E + 1)
-        return {"saved": common + 2 * R * d + 3 * 2 * R * h, "recompute": common}
+        mx = R * d + R * d // 32 + R * h + R * h // 32
+        return {"saved": common + 2 * R * d + 3 * 2 * R * h,
+                "mxfp8_saved": common + mx + 2 * 2 * R * h,
+                "recompute": common}
 
 
 class HostPipeline:

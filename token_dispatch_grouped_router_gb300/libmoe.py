@@ -44,6 +44,8 @@ SIGNATURES = {
                                     _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_mxfp8_quantize_rows": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_mxfp8_quantize_weights": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_mxfp8_quantize_weights_f32": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_mxfp8_dequantize_rows": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_dispatch_rows_mxfp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
@@ -334,6 +336,22 @@ def moe_mxfp8_quantize_weights(W, wq, ws) -> None:
         _ptr(W), E, K, N, _ptr(wq), _ptr(ws), _stream()))
 
 
+def moe_mxfp8_quantize_weights_f32(W, wq, ws) -> None:
+    E, K, N = W.shape
+    _want(W, torch.float32, (E, K, N), "W"); _want(wq, torch.uint8, (E, N, K), "wq")
+    _want(ws, torch.uint8, (E, N, K // 32), "ws")
+    _ok("moe_mxfp8_quantize_weights_f32", load().moe_mxfp8_quantize_weights_f32(
+        _ptr(W), E, K, N, _ptr(wq), _ptr(ws), _stream()))
+
+
+def moe_mxfp8_dequantize_rows(q, scale, out) -> None:
+    rows, K = q.shape
+    _want(q, torch.uint8, (rows, K), "q"); _want(scale, torch.uint8, (rows, K // 32), "scale")
+    _want(out, torch.bfloat16, (rows, K), "out")
+    _ok("moe_mxfp8_dequantize_rows", load().moe_mxfp8_dequantize_rows(
+        _ptr(q), _ptr(scale), rows, K, _ptr(out), _stream()))
+
+
 def moe_dispatch_rows_mxfp8(x, row_of_slot, k: int, xq, xs, xp=None) -> None:
     T, d = x.shape
     _want(x, torch.bfloat16, (T, d), "x"); _want(xq, torch.uint8, (T * k, d), "xq")
@@ -355,7 +373,8 @@ def moe_grouped_swiglu_fwd_mxfp8(xq, xs, offsets, w1q, w1s, w3q, w3s, w2q, w2s,
         _want(t, torch.uint8, (E, h, d // 32), n)
     _want(w2q, torch.uint8, (E, d, h), "w2q"); _want(w2s, torch.uint8, (E, d, h // 32), "w2s")
     for n, t in (("h1", h1), ("h3", h3), ("a", a)):
-        _want(t, torch.bfloat16, (R, h), n)
+        if t is not None or n != "a":             # a may be None: quantised a only
+            _want(t, torch.bfloat16, (R, h), n)
     _want(aq, torch.uint8, (R, h), "aq"); _want(as_, torch.uint8, (R, h // 32), "as")
     _want(yp, torch.bfloat16, (R, d), "yp")
     _ok("moe_grouped_swiglu_fwd_mxfp8", load().moe_grouped_swiglu_fwd_mxfp8(
