@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--workload", default="dense_e8")
     ap.add_argument("--compare", default="pool_e128",
                     help="second workload timed the same way (expert-count flatness); '' to skip")
+    ap.add_argument("--skew-workload", default="skew_e128",
+                    help="learned Zipf-biased router workload timed the same way (uneven experts); "
+                         "'' to skip")
     ap.add_argument("--mxfp8-workload", default="train_e128",
                     help="workload of the BF16 vs MXFP8-forward comparison; '' to skip")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -360,6 +363,14 @@ def run_ours(args):
         cmp_res["workload"] = w2.name
         del inp2
 
+    skew_res = None
+    if args.skew_workload:
+        w4 = wl.get_workload(args.skew_workload)
+        inp4 = wl.generate(w4, seed=args.seed + rank, with_backward=True)
+        skew_res = timed(w4, inp4, args.steps, args.warmup, with_e2e=False, sample_clocks=False)
+        skew_res["workload"] = w4.name
+        del inp4
+
     mx_res = None
     if args.mxfp8_workload:
         w3 = wl.get_workload(args.mxfp8_workload)
@@ -459,6 +470,15 @@ def run_ours(args):
                           "ms_per_step": cmp_res["ms_per_step"], "ratio_to_main": cv / value,
                           "kernels_ms": cmp_res["kernels_ms"], "gpu_launches": cmp_res["launches"],
                           "row_tile_overhead": cmp_res["row_tile_overhead"]}
+    if skew_res is not None:
+        sv = world * wl.get_workload(args.skew_workload).T / (skew_res["ms_per_step"] / 1e3)
+        out["skew"] = {"workload": skew_res["workload"], "value": sv, "unit": UNIT,
+                       "ms_per_step": skew_res["ms_per_step"], "ratio_to_main": sv / value,
+                       "kernels_ms": skew_res["kernels_ms"], "gpu_launches": skew_res["launches"],
+                       "row_tile_overhead": skew_res["row_tile_overhead"],
+                       "note": "learned router x W_r + b with a Zipf(1.2) expert bias (seed 0: 100 of 128 "
+                               "experts empty, the hottest holds a quarter of the routed rows); "
+                               "the step includes the fp32 router GEMM and its backward"}
     if mx_res is not None:
         w3, bf, mx, mxc, mxs = mx_res
         fl, _ = work_per_launch(w3)
