@@ -101,6 +101,19 @@ int moe_get_status(const void* ws, int32_t* host_status, moe_stream_t stream);
 int moe_router_logits(const moe_bf16_t* x, const float* W_r, const float* b,
                       int T, int d, int E, float* logits, moe_stream_t stream);
 
+/* The same logits on the tcgen05 tensor cores at fp32 accuracy.  W_r is split
+ * exactly into three bf16 parts (W_r = W0 + W1 + W2, each the bf16 rounding of
+ * what the earlier parts leave), written to the workspace scratch; the MMAs
+ * form x W0 + x W1 + x W2 with exact bf16 products and fp32 accumulation.  The
+ * router stays in high precision, as the page's DeepSeek-V3 paragraph asks
+ * (OLMo-core 3 tutorial, section "一个低精度格式，同时压三个地方").
+ * d % 8 == 0 (MOE_ERR_UNSUPPORTED otherwise); ws 16-byte aligned with at
+ * least moe_workspace_size(...) bytes (the split needs 256 + 6 E
+ * ceil(d/64)*64 bytes); a timed-out pipeline wait sets the status word. */
+int moe_router_logits_tc(const moe_bf16_t* x, const float* W_r, const float* b,
+                         int T, int d, int E, float* logits, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
 /* Top-k of each row of logits[T,E] (fp32): topk_idx[T,k] (int32) lists the k
  * largest logits in the total order (value descending, expert id ascending;
  * -0.0 == +0.0), and topk_gate[T,k] (fp32) = softmax over the k selected

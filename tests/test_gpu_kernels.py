@@ -83,6 +83,26 @@ def test_router_logits_and_backward(T, d, E, bias):
     assert_close(db, dbref, "db", rel_l2=1e-5, max_abs=1e-5)
 
 
+@pytest.mark.parametrize("T,d,E,bias", [(129, 256, 8, False), (300, 2048, 128, True), (64, 72, 5, True),
+                                        (1000, 512, 300, True), (16384, 2048, 128, True)])
+def test_router_logits_tensor_cores(T, d, E, bias):
+    # the tcgen05 router (W_r split into three bf16 parts, fp32 accumulation)
+    # against the fp64 oracle at the fp32 router tolerance: ragged rows (129,
+    # 300), a K tail (d = 72), expert tiles cut short (E = 5, 300), full size
+    w = wl.small_workload(T=T, d=d, E=E, k=1, h=64, routing="learned", zipf=bias)
+    inp = wl.generate(w, seed=7, with_backward=False)
+    x = bf16_tensor(inp["x"], DEV)
+    Wr = torch.from_numpy(inp["W_r"]).to(DEV)
+    b = torch.from_numpy(inp["b"]).to(DEV) if bias else None
+    z = torch.full((T, E), float("nan"), dtype=torch.float32, device=DEV)
+    ws = _ws(T, E, 1, d)
+    L.moe_reset_status(ws)
+    L.moe_router_logits_tc(x, Wr, b, z, ws)
+    assert L.moe_get_status(ws) == 0
+    zref = ol.router_logits(inp["x"], inp["W_r"], inp.get("b"), np.float64)
+    assert_close(z, zref, "logits", rel_l2=1e-5, max_abs=1e-5)
+
+
 @pytest.mark.parametrize("T,k,E", [(1, 1, 1), (5, 2, 3), (1000, 4, 8), (4096, 4, 128),
                                    (3000, 8, 1024), (257, 2, 700), (16384, 4, 128),
                                    # many chunk histograms per expert group of the scan

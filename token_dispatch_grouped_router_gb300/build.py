@@ -22,8 +22,8 @@ ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "lib", "libmoe.so")
 
-SOURCES = ["capi.cu", "router.cu", "route_map.cu", "permute.cu", "grouped_swiglu.cu", "mxfp8.cu",
-           "grouped_mxfp8.cu"]
+SOURCES = ["capi.cu", "router.cu", "router_tc.cu", "route_map.cu", "permute.cu",
+           "grouped_swiglu.cu", "mxfp8.cu", "grouped_mxfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -120,7 +120,7 @@ class MoELayer:
         if self.learned:
             if not self.logits_given:
                 mark("router_logits")
-                L.moe_router_logits(self.x, self.W_r, self.b, self.logits)
+                L.moe_router_logits_tc(self.x, self.W_r, self.b, self.logits, self.ws)
             mark("router_topk")
             L.moe_router_topk(self.logits, self.k, self.idx, self.gate)
         else:

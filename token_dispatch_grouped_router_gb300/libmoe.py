@@ -29,6 +29,7 @@ SIGNATURES = {
     "moe_reset_status": (_I, [_P, _P]),
     "moe_get_status": (_I, [_P, _P, _P]),
     "moe_router_logits": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_router_logits_tc": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_router_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_router_gates": (_I, [_P, _I, _I, _P, _P]),
     "moe_router_topk_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
@@ -143,6 +144,19 @@ def moe_router_logits(x, W_r, b, logits) -> None:
         _want(b, torch.float32, (E,), "b")
     _ok("moe_router_logits", load().moe_router_logits(
         _ptr(x), _ptr(W_r), _ptr(b), T, d, E, _ptr(logits), _stream()))
+
+
+def moe_router_logits_tc(x, W_r, b, logits, ws) -> None:
+    """moe_router_logits on the tensor cores (W_r split into three bf16 parts
+    in the workspace; fp32 accuracy)."""
+    T, d = x.shape
+    E = W_r.shape[1]
+    _want(x, torch.bfloat16, (T, d), "x"); _want(W_r, torch.float32, (d, E), "W_r")
+    _want(logits, torch.float32, (T, E), "logits")
+    if b is not None:
+        _want(b, torch.float32, (E,), "b")
+    _ok("moe_router_logits_tc", load().moe_router_logits_tc(
+        _ptr(x), _ptr(W_r), _ptr(b), T, d, E, _ptr(logits), _ptr(ws), _wsb(ws), _stream()))
 
 
 def moe_router_topk(logits, k: int, topk_idx, topk_gate) -> None:
