@@ -143,6 +143,24 @@ int moe_router_logits_bwd(const moe_bf16_t* x, const float* W_r,
                           moe_bf16_t* dx, float* dW_r, float* db,
                           void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The same backward when only the top-k logits carry gradient, as
+ * moe_router_topk_bwd leaves d_logits (the gates are a softmax over the
+ * selected logits, so every other entry is 0; this call reads only the
+ * selected ones):
+ *   dx[t] += sum_j d_logits[t, idx_tj] * W_r[:, idx_tj]   (bf16, one rounding)
+ *   dW_r[:, e] = sum over the rows routed to e of d_logits[t, e] * x[t]
+ *   db[e] = sum over the same rows of d_logits[t, e]         (db may be NULL)
+ * The sums over rows follow the route map (offsets[E+1] and slot_of_row[T*k]
+ * from moe_expert_offsets on topk_idx) in token order, in chunks of 256 rows
+ * added in chunk order: deterministic.  Results equal moe_router_logits_bwd's
+ * up to fp32 summation order.  d % 8 == 0 (MOE_ERR_UNSUPPORTED otherwise); ws
+ * needs moe_workspace_size(T, E, k, d, h) bytes. */
+int moe_router_logits_bwd_topk(const moe_bf16_t* x, const float* W_r, const float* d_logits,
+                               const int32_t* topk_idx, const int32_t* offsets,
+                               const int32_t* slot_of_row, int T, int d, int E, int k,
+                               moe_bf16_t* dx, float* dW_r, float* db, void* ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
 /* ------------------------------------------------------------- route map */
 
 /* Device-resident route map from topk_idx[T,k] (flattened slot s = t*k + j):

@@ -103,6 +103,50 @@ def test_router_logits_tensor_cores(T, d, E, bias):
     assert_close(z, zref, "logits", rel_l2=1e-5, max_abs=1e-5)
 
 
+@pytest.mark.parametrize("T,d,E,k,bias", [(129, 256, 8, 2, False), (300, 2048, 128, 4, True),
+                                          (64, 72, 5, 3, True), (3000, 128, 16, 8, False),
+                                          (16384, 2048, 128, 4, True)])
+def test_router_backward_through_topk(T, d, E, k, bias):
+    # backward of the router GEMM when only the selected logits carry gradient:
+    # against the fp64 oracle and against the dense call on the same d_logits;
+    # the Zipf bias leaves experts empty, whose dW_r columns and db must be 0
+    w = wl.small_workload(T=T, d=d, E=E, k=k, h=64, routing="learned", zipf=bias)
+    inp = wl.generate(w, seed=8, with_backward=False)
+    z = ol.router_logits(inp["x"], inp["W_r"], inp.get("b"))
+    idx = ol.topk(z, k)
+    g = ol.topk_gates(z, idx)
+    rng = np.random.default_rng(9)
+    dz = ol.router_topk_backward(g, rng.standard_normal((T, k)), idx, E).astype(np.float32)
+    counts, _, _, _ = ol.route_map(idx, E)
+    x = bf16_tensor(inp["x"], DEV)
+    Wr = torch.from_numpy(inp["W_r"]).to(DEV)
+    dzt = torch.from_numpy(dz).to(DEV)
+    it = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).to(DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    cnt, off = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    ros, sor = torch.empty(T * k, **i32), torch.empty(T * k, **i32)
+    ws = _ws(T, E, k, d)
+    L.moe_expert_offsets(it, E, cnt, off, ros, sor, ws)
+    dx0 = wl.bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    dx = bf16_tensor(dx0, DEV)
+    dWr = torch.full((d, E), float("nan"), dtype=torch.float32, device=DEV)
+    db = torch.full((E,), float("nan"), dtype=torch.float32, device=DEV)
+    L.moe_router_logits_bwd_topk(x, Wr, dzt, it, off, sor, dx, dWr, db, ws)
+    dxr, dWref, dbref = ol.router_logits_backward(inp["x"], inp["W_r"], dz)
+    assert_close(dx, ol.decode_bf16(dx0) + dxr, "dx")
+    assert_close(dWr, dWref, "dW_r", rel_l2=1e-5, max_abs=1e-5)
+    assert_close(db, dbref, "db", rel_l2=1e-5, max_abs=1e-5)
+    empty = np.flatnonzero(counts == 0)
+    assert torch.count_nonzero(dWr[:, torch.from_numpy(empty).to(DEV)]).item() == 0
+    assert torch.count_nonzero(db[torch.from_numpy(empty).to(DEV)]).item() == 0
+    # the dense call on the same (zero-padded) d_logits
+    dx2 = bf16_tensor(dx0, DEV)
+    dWr2 = torch.empty(d, E, dtype=torch.float32, device=DEV)
+    db2 = torch.empty(E, dtype=torch.float32, device=DEV)
+    L.moe_router_logits_bwd(x, Wr, dzt, dx2, dWr2, db2, _ws(T, E, k, d))
+    assert_close(dWr, dWr2.cpu().numpy(), "dW_r vs dense", rel_l2=1e-5, max_abs=1e-5)
+
+
 @pytest.mark.parametrize("T,k,E", [(1, 1, 1), (5, 2, 3), (1000, 4, 8), (4096, 4, 128),
                                    (3000, 8, 1024), (257, 2, 700), (16384, 4, 128),
                                    # many chunk histograms per expert group of the scan

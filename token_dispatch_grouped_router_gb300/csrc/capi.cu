@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "router_bwd.cuh"
 
 namespace moe {
 
@@ -53,7 +54,9 @@ uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_
 size_t moe_workspace_size(int T, int E, int k, int d, int h) {
   (void)h;
   if (T < 0 || E <= 0 || k <= 0 || d <= 0) return 0;
-  return moe::workspace_bytes(T, E, k, d);
+  const size_t a = moe::workspace_bytes(T, E, k, d);
+  const size_t b = moe::router_topk_scratch((long long)T * k, E, d).end;
+  return a > b ? a : b;
 }
 
 int moe_reset_status(void* ws, moe_stream_t stream) {

@@ -11,6 +11,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "router_bwd.cuh"
 
 namespace moe {
 namespace {
@@ -246,12 +247,223 @@ topk_bwd_kernel(const float* __restrict__ gate, const float* __restrict__ dgate,
   }
 }
 
+// ------------------------------------------- backward through the top-k only
+// The gates are a softmax over the k selected logits, so d_logits is zero
+// outside the selection (moe_router_topk_bwd writes it so) and the router
+// GEMMs' backward reduces to k rows of W_r^T per token (dx) and, per expert,
+// a sum over the rows routed to it (dW_r, db), taken in the route map's
+// token order so that the result does not depend on timing.
+
+// W [d][E] -> WT [E][d] through 32 x 32 shared-memory tiles
+__global__ void transpose_kernel(const float* __restrict__ W, int d, int E, float* __restrict__ WT) {
+  pdl_enter();
+  __shared__ float tile[32][33];
+  const int e0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int k = k0 + i, e = e0 + threadIdx.x;
+    tile[i][threadIdx.x] = (k < d && e < E) ? __ldg(W + (size_t)k * E + e) : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int e = e0 + i, k = k0 + threadIdx.x;
+    if (e < E && k < d) WT[(size_t)e * d + k] = tile[threadIdx.x][i];
+  }
+}
+
+// Chunks of at most kRouterChunk rows of every expert's segment, numbered
+// expert-major: units[u] = (expert, first row, rows); estart / ecount give
+// each expert's first chunk and chunk count; *total the number of chunks.
+// One block of 1024 threads, thread = expert.
+__global__ void __launch_bounds__(1024)
+router_units_kernel(const int32_t* __restrict__ offsets, int E, int R, int4* __restrict__ units,
+                    int* __restrict__ estart, int* __restrict__ ecount, int* __restrict__ total) {
+  pdl_enter();
+  __shared__ int wsum[32];
+  const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+  int lo = 0, hi = 0, n = 0;
+  if (e < E) {
+    lo = max(0, min(__ldg(offsets + e), R));
+    hi = max(lo, min(__ldg(offsets + e + 1), R));
+    n = (hi - lo + kRouterChunk - 1) / kRouterChunk;
+  }
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int v = wsum[lane];
+    int iv = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, iv, o);
+      if (lane >= o) iv += u;
+    }
+    wsum[lane] = iv - v;                 // exclusive prefix of the warp sums
+    if (lane == 31) *total = iv;
+  }
+  __syncthreads();
+  if (e < E) {
+    const int base = wsum[w] + incl - n;
+    estart[e] = base;
+    ecount[e] = n;
+    for (int c = 0; c < n; ++c)
+      units[base + c] = make_int4(e, lo + c * kRouterChunk, min(kRouterChunk, hi - lo - c * kRouterChunk), 0);
+  }
+}
+
+// Chunk u of expert e: part[u][:] = sum over its rows r (in order) of
+// dz[t_r, e] * x[t_r][:], pbias[u] = sum of those dz.  Thread = 8 columns.
+__global__ void __launch_bounds__(256)
+router_dw_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ dz,
+                         const int32_t* __restrict__ slot_of_row, const int4* __restrict__ units,
+                         const int* __restrict__ total, int d, int E, int k, float* __restrict__ part,
+                         float* __restrict__ pbias) {
+  pdl_enter();
+  const int u = blockIdx.x;
+  if (u >= __ldg(total)) return;
+  const int4 un = units[u];
+  const int e = un.x, r0 = un.y, rows = un.z;
+  for (int c0 = threadIdx.x * 8; c0 < d; c0 += 256 * 8) {
+    float acc[8] = {};
+    float gs = 0.f;
+#pragma unroll 4
+    for (int r = 0; r < rows; ++r) {
+      const int t = __ldg(slot_of_row + r0 + r) / k;
+      const float g = __ldg(dz + (size_t)t * E + e);
+      const uint4 v = ld_nc_v4(x + (size_t)t * d + c0);
+      acc[0] = fmaf(g, bf16_lo(v.x), acc[0]); acc[1] = fmaf(g, bf16_hi(v.x), acc[1]);
+      acc[2] = fmaf(g, bf16_lo(v.y), acc[2]); acc[3] = fmaf(g, bf16_hi(v.y), acc[3]);
+      acc[4] = fmaf(g, bf16_lo(v.z), acc[4]); acc[5] = fmaf(g, bf16_hi(v.z), acc[5]);
+      acc[6] = fmaf(g, bf16_lo(v.w), acc[6]); acc[7] = fmaf(g, bf16_hi(v.w), acc[7]);
+      gs += g;
+    }
+    float* p = part + (size_t)u * d + c0;
+    *reinterpret_cast<float4*>(p) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (c0 == 0) pbias[u] = gs;
+  }
+}
+
+// dW_r[n][e] = sum of expert e's chunk partials in chunk order (zero for an
+// empty expert); db[e] likewise.  Block = (256 columns, expert).
+__global__ void __launch_bounds__(256)
+router_dw_reduce_kernel(const float* __restrict__ part, const float* __restrict__ pbias,
+                        const int* __restrict__ estart, const int* __restrict__ ecount, int d, int E,
+                        float* __restrict__ dW, float* __restrict__ db) {
+  pdl_enter();
+  const int e = blockIdx.y, n = blockIdx.x * 256 + threadIdx.x;
+  const int s0 = __ldg(estart + e), cnt = __ldg(ecount + e);
+  if (n < d) {
+    float acc = 0.f;
+    for (int c = 0; c < cnt; ++c) acc += __ldg(part + (size_t)(s0 + c) * d + n);
+    dW[(size_t)n * E + e] = acc;
+  }
+  if (db && blockIdx.x == 0 && threadIdx.x == 0) {
+    float b = 0.f;
+    for (int c = 0; c < cnt; ++c) b += __ldg(pbias + s0 + c);
+    db[e] = b;
+  }
+}
+
+// dx[t] += sum_j dz[t, e_j] * WT[e_j] (j in slot order), rounded once to
+// bf16.  Warp per token, 8 columns per lane and step.
+__global__ void __launch_bounds__(256)
+router_dx_topk_kernel(const float* __restrict__ dz, const int32_t* __restrict__ idx,
+                      const float* __restrict__ WT, int T, int d, int E, int k,
+                      uint16_t* __restrict__ dx) {
+  pdl_enter();
+  const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int ee[kMaxTopK];
+  float gg[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    ee[j] = -1; gg[j] = 0.f;
+    if (j < k) {
+      const int e = __ldg(idx + (size_t)t * k + j);
+      if ((unsigned)e < (unsigned)E) { ee[j] = e; gg[j] = __ldg(dz + (size_t)t * E + e); }
+    }
+  }
+  for (int c0 = lane * 8; c0 < d; c0 += 256) {
+    float acc[8] = {};
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (ee[j] < 0) continue;
+      const float* w = WT + (size_t)ee[j] * d + c0;
+      const float4 a = __ldg(reinterpret_cast<const float4*>(w));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(w + 4));
+      acc[0] = fmaf(gg[j], a.x, acc[0]); acc[1] = fmaf(gg[j], a.y, acc[1]);
+      acc[2] = fmaf(gg[j], a.z, acc[2]); acc[3] = fmaf(gg[j], a.w, acc[3]);
+      acc[4] = fmaf(gg[j], b.x, acc[4]); acc[5] = fmaf(gg[j], b.y, acc[5]);
+      acc[6] = fmaf(gg[j], b.z, acc[6]); acc[7] = fmaf(gg[j], b.w, acc[7]);
+    }
+    uint4* p = reinterpret_cast<uint4*>(dx + (size_t)t * d + c0);
+    uint4 v = *p;
+    v.x = pack_bf16x2(bf16_lo(v.x) + acc[0], bf16_hi(v.x) + acc[1]);
+    v.y = pack_bf16x2(bf16_lo(v.y) + acc[2], bf16_hi(v.y) + acc[3]);
+    v.z = pack_bf16x2(bf16_lo(v.z) + acc[4], bf16_hi(v.z) + acc[5]);
+    v.w = pack_bf16x2(bf16_lo(v.w) + acc[6], bf16_hi(v.w) + acc[7]);
+    *p = v;
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" {
+
+int moe_router_logits_bwd_topk(const moe_bf16_t* x, const float* W_r, const float* d_logits,
+                               const int32_t* topk_idx, const int32_t* offsets,
+                               const int32_t* slot_of_row, int T, int d, int E, int k,
+                               moe_bf16_t* dx, float* dW_r, float* db, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && E > 0 && E <= kMaxExperts && k >= 1 && k <= kMaxTopK && k <= E);
+  if (d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_CHECK_PTR(W_r); MOE_CHECK_PTR(dW_r);
+  if (db && !aligned16(db)) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) {
+    if (cudaMemsetAsync(dW_r, 0, sizeof(float) * (size_t)d * E, s) != cudaSuccess ||
+        (db && cudaMemsetAsync(db, 0, sizeof(float) * (size_t)E, s) != cudaSuccess)) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  MOE_CHECK_PTR(x); MOE_CHECK_PTR(d_logits); MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(offsets);
+  MOE_CHECK_PTR(slot_of_row); MOE_CHECK_PTR(dx);
+  const long long R = (long long)T * k;
+  const RouterTopkScratch L = router_topk_scratch(R, E, d);
+  if (ws_bytes < L.end) return MOE_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* WT = reinterpret_cast<float*>(base + L.wt);
+  int4* units = reinterpret_cast<int4*>(base + L.units);
+  int* estart = reinterpret_cast<int*>(base + L.estart);
+  int* ecount = reinterpret_cast<int*>(base + L.ecount);
+  int* total = reinterpret_cast<int*>(base + L.total);
+  float* part = reinterpret_cast<float*>(base + L.part);
+  float* pbias = reinterpret_cast<float*>(base + L.pbias);
+  (void)launch_pdl(transpose_kernel, dim3((E + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, s, W_r, d, E, WT);
+  (void)launch_pdl(router_units_kernel, 1, 1024, 0, s, offsets, E, (int)R, units, estart, ecount, total);
+  (void)launch_pdl(router_dw_partial_kernel, (unsigned)L.max_units, 256, 0, s,
+                   reinterpret_cast<const uint16_t*>(x), d_logits, slot_of_row, units, total, d, E, k,
+                   part, pbias);
+  (void)launch_pdl(router_dw_reduce_kernel, dim3((d + 255) / 256, E), 256, 0, s, part, pbias, estart,
+                   ecount, d, E, dW_r, db);
+  (void)launch_pdl(router_dx_topk_kernel, (unsigned)((T + 7) / 8), 256, 0, s, d_logits, topk_idx, WT,
+                   T, d, E, k, reinterpret_cast<uint16_t*>(dx));
+  MOE_LAUNCH_CHECK(5);
+  return MOE_OK;
+}
 
 int moe_router_logits(const moe_bf16_t* x, const float* W_r, const float* b, int T, int d, int E,
                       float* logits, moe_stream_t stream) {

@@ -171,8 +171,8 @@ class MoELayer:
         L.moe_router_topk_bwd(self.gate, self.dgate, self.idx, self.E, self.dlogits)
         if self.learned:
             mark("router_logits_bwd")
-            L.moe_router_logits_bwd(self.x, self.W_r, self.dlogits, self.dX, self.dW_r,
-                                    self.db, self.ws)
+            L.moe_router_logits_bwd_topk(self.x, self.W_r, self.dlogits, self.idx, self.offsets,
+                                         self.slot_of_row, self.dX, self.dW_r, self.db, self.ws)
 
     # ------------------------------------------------------------- MXFP8
     def enable_mxfp8(self) -> None:

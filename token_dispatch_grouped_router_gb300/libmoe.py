@@ -34,6 +34,8 @@ SIGNATURES = {
     "moe_router_gates": (_I, [_P, _I, _I, _P, _P]),
     "moe_router_topk_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_router_logits_bwd": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_router_logits_bwd_topk": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                        _Z, _P]),
     "moe_expert_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_rows": (_I, [_P, _I, _I, _I, _P, _P, _P]),
@@ -190,6 +192,21 @@ def moe_router_logits_bwd(x, W_r, d_logits, dx, dW_r, db, ws) -> None:
     _ok("moe_router_logits_bwd", load().moe_router_logits_bwd(
         _ptr(x), _ptr(W_r), _ptr(d_logits), T, d, E, _ptr(dx), _ptr(dW_r), _ptr(db),
         _ptr(ws), ws.numel() * ws.element_size(), _stream()))
+
+
+def moe_router_logits_bwd_topk(x, W_r, d_logits, topk_idx, offsets, slot_of_row, dx, dW_r, db,
+                               ws) -> None:
+    """moe_router_logits_bwd for d_logits that is zero outside the top-k
+    selection (as moe_router_topk_bwd writes it), through the route map."""
+    T, d = x.shape
+    E = W_r.shape[1]
+    k = topk_idx.shape[1]
+    _want(d_logits, torch.float32, (T, E), "d_logits"); _want(dx, torch.bfloat16, (T, d), "dx")
+    _want(dW_r, torch.float32, (d, E), "dW_r"); _want(topk_idx, torch.int32, (T, k), "topk_idx")
+    _want(offsets, torch.int32, (E + 1,), "offsets"); _want(slot_of_row, torch.int32, (T * k,), "slot_of_row")
+    _ok("moe_router_logits_bwd_topk", load().moe_router_logits_bwd_topk(
+        _ptr(x), _ptr(W_r), _ptr(d_logits), _ptr(topk_idx), _ptr(offsets), _ptr(slot_of_row),
+        T, d, E, k, _ptr(dx), _ptr(dW_r), _ptr(db), _ptr(ws), _wsb(ws), _stream()))
 
 
 # ------------------------------------------------------------- route map
