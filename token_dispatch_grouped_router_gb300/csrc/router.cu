@@ -316,35 +316,54 @@ router_units_kernel(const int32_t* __restrict__ offsets, int E, int R, int4* __r
 }
 
 // Chunk u of expert e: part[u][:] = sum over its rows r (in order) of
-// dz[t_r, e] * x[t_r][:], pbias[u] = sum of those dz.  Thread = 8 columns.
+// dz[t_r, e] * x[t_r][:], pbias[u] = sum of those dz.  The chunk's token ids
+// and gradients are staged in shared memory first, so the x rows are loaded
+// without a chain of dependent reads in front of each.  Thread = 8 columns.
 __global__ void __launch_bounds__(256)
 router_dw_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ dz,
                          const int32_t* __restrict__ slot_of_row, const int4* __restrict__ units,
                          const int* __restrict__ total, int d, int E, int k, float* __restrict__ part,
                          float* __restrict__ pbias) {
   pdl_enter();
+  __shared__ int s_t[kRouterChunk];
+  __shared__ float s_g[kRouterChunk];
   const int u = blockIdx.x;
   if (u >= __ldg(total)) return;
   const int4 un = units[u];
   const int e = un.x, r0 = un.y, rows = un.z;
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    const int t = __ldg(slot_of_row + r0 + i) / k;
+    s_t[i] = t;
+    s_g[i] = __ldg(dz + (size_t)t * E + e);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float gs = 0.f;
+    for (int r = 0; r < rows; ++r) gs += s_g[r];
+    pbias[u] = gs;
+  }
   for (int c0 = threadIdx.x * 8; c0 < d; c0 += 256 * 8) {
     float acc[8] = {};
-    float gs = 0.f;
-#pragma unroll 4
-    for (int r = 0; r < rows; ++r) {
-      const int t = __ldg(slot_of_row + r0 + r) / k;
-      const float g = __ldg(dz + (size_t)t * E + e);
-      const uint4 v = ld_nc_v4(x + (size_t)t * d + c0);
-      acc[0] = fmaf(g, bf16_lo(v.x), acc[0]); acc[1] = fmaf(g, bf16_hi(v.x), acc[1]);
-      acc[2] = fmaf(g, bf16_lo(v.y), acc[2]); acc[3] = fmaf(g, bf16_hi(v.y), acc[3]);
-      acc[4] = fmaf(g, bf16_lo(v.z), acc[4]); acc[5] = fmaf(g, bf16_hi(v.z), acc[5]);
-      acc[6] = fmaf(g, bf16_lo(v.w), acc[6]); acc[7] = fmaf(g, bf16_hi(v.w), acc[7]);
-      gs += g;
+    // groups of 8 rows: the 8 row loads are issued before their 64 FMAs
+    for (int r0g = 0; r0g < rows; r0g += 8) {
+      const int n = min(8, rows - r0g);
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[i] = i < n ? ld_nc_v4(x + (size_t)s_t[r0g + i] * d + c0) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i >= n) break;
+        const float g = s_g[r0g + i];
+        acc[0] = fmaf(g, bf16_lo(v[i].x), acc[0]); acc[1] = fmaf(g, bf16_hi(v[i].x), acc[1]);
+        acc[2] = fmaf(g, bf16_lo(v[i].y), acc[2]); acc[3] = fmaf(g, bf16_hi(v[i].y), acc[3]);
+        acc[4] = fmaf(g, bf16_lo(v[i].z), acc[4]); acc[5] = fmaf(g, bf16_hi(v[i].z), acc[5]);
+        acc[6] = fmaf(g, bf16_lo(v[i].w), acc[6]); acc[7] = fmaf(g, bf16_hi(v[i].w), acc[7]);
+      }
     }
     float* p = part + (size_t)u * d + c0;
     *reinterpret_cast<float4*>(p) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     *reinterpret_cast<float4*>(p + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    if (c0 == 0) pbias[u] = gs;
   }
 }
 
