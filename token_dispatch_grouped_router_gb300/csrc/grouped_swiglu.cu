@@ -504,6 +504,8 @@ constexpr int kRingSlotBytes = 2 * kRingChunk;
 template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_STAGES; }
 template <int MODE> __host__ __device__ constexpr int pair_ring_bytes() { return MODE == kDA ? kRingSlots * kRingSlotBytes : 0; }
 template <int MODE> __host__ __device__ constexpr int pair_stage_bytes() { return MODE == kDA ? 0 : kEpiWarps * kStageBytes; }
+// WG: a 32 x 32 bf16 box of zeros, the source of every store of an empty expert's dW tiles
+template <int MODE> __host__ __device__ constexpr int pair_zero_bytes() { return MODE == kWG ? 2048 : 0; }
 template <int MODE> using PairSharedT = PipeShared<pair_stages<MODE>()>;
 constexpr int kPairThreads = kThreads + 32;           // + DA's ring loader warp
 
@@ -676,6 +678,27 @@ __device__ __forceinline__ bool epilogue_da_ring(const Tile& tl, uint32_t tacc, 
   return true;
 }
 
+// A whole dW tile of an expert with no rows: this warp's 32 rows x 4 chunks of
+// 32 columns are TMA-stored from a shared box of zeros (no accumulator, no
+// staging); lane 0 issues the stores as one bulk group.
+__device__ __forceinline__ void epilogue_zero_tile(const Tile& tl, int lane_q, int half, int lane,
+                                                   const uint8_t* zero, const GemmArgs& a,
+                                                   const OutMaps& om) {
+  const int M = tl.which == 2 ? a.h : a.d;
+  const int N = tl.which == 2 ? a.d : a.h;
+  const int r0 = tl.m0 + lane_q * 32;
+  if (lane == 0 && r0 < M) {
+    const CUtensorMap* map = tl.which == 0 ? om.o0 : (tl.which == 1 ? om.o1 : om.o2);
+#pragma unroll 1
+    for (int c = half * 4; c < half * 4 + 4; ++c) {
+      const int col = tl.n0 + c * 32;
+      if (col < N) tma_store_3d(map, smem_u32(zero), col, r0, tl.e);
+    }
+    bulk_commit();
+  }
+  __syncwarp();
+}
+
 // A K-chunk of a split wgrad tile: this CTA's 128 rows x 256 columns of the
 // fp32 accumulator (zeros for an empty chunk) to partial slot tl.part; each
 // lane writes its row's 32 values of a chunk as 128 contiguous bytes.
@@ -738,7 +761,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   uint8_t* sB = smem + PS * P_HALF;
   uint8_t* ring = sB + PS * P_HALF;                          // DA only
   uint8_t* sStage = ring + pair_ring_bytes<MODE>();                 // not DA
-  PairShared* sh = reinterpret_cast<PairShared*>(sStage + pair_stage_bytes<MODE>());
+  uint8_t* sZero = sStage + pair_stage_bytes<MODE>();               // WG only
+  PairShared* sh = reinterpret_cast<PairShared*>(sZero + pair_zero_bytes<MODE>());
   int* s_off = reinterpret_cast<int*>(sh + 1);
   int* s_ts = s_off + (args.E + 1);
 
@@ -748,6 +772,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = __ldg(args.offsets + i);
+  if constexpr (MODE == kWG) {
+    for (int i = threadIdx.x; i < pair_zero_bytes<MODE>() / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(sZero)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();              // the zeros are read by TMA stores
+  }
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < PS; ++s) {
@@ -849,6 +878,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
       bool ok = true, issued_any = false;
       for (int t = pair; t < total && ok; t += npairs) {
         const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+        if constexpr (MODE == kWG) {
+          if (tl.part < 0 && tl.nkb == 0) continue;     // empty expert: no accumulator (epilogue stores zeros)
+        }
         if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tf = smem_u32(&sh->tfull[acc]);
@@ -904,6 +936,10 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
       // this CTA's rows of the output tile
       if constexpr (MODE == kWG) {
         tl.m0 += 128 * (int)rank;
+        if (tl.part < 0 && tl.nkb == 0) {          // empty expert: dW tile of zeros, no accumulator
+          epilogue_zero_tile(tl, lane_q, half, lane, sZero, args, om);
+          continue;
+        }
       } else {
         tl.row0 += 128 * (int)rank;
         tl.rows = max(0, min(128, tl.rows - 128 * (int)rank));
@@ -1025,7 +1061,8 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
 template <int MODE>
 constexpr size_t pair_smem_bytes(int E) {
   return 1024 + (size_t)pair_stages<MODE>() * 2 * P_HALF + pair_ring_bytes<MODE>() +
-         (size_t)pair_stage_bytes<MODE>() + sizeof(PairSharedT<MODE>) + 2 * (size_t)(E + 1) * 4;
+         (size_t)pair_stage_bytes<MODE>() + pair_zero_bytes<MODE>() + sizeof(PairSharedT<MODE>) +
+         2 * (size_t)(E + 1) * 4;
 }
 // the largest expert count whose tile table still fits beside the pipeline
 // in the 227 KB of shared memory a block may opt in to
