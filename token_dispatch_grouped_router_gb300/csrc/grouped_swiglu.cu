@@ -78,34 +78,19 @@ struct Tile {
 
 using Shared = PipeShared<STAGES>;
 
+// Row tiles of the single-CTA kernel (the weight-gradient GEMM runs on CTA
+// pairs only, decode_pair_tile below).
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int* s_off,
                                             const int* s_ts) {
+  static_assert(MODE != kWG, "the weight-gradient GEMM runs on CTA pairs only");
   Tile tl{};
-  if constexpr (MODE == kWG) {
-    const int per = 2 * a.wg_t1 + a.wg_t2;
-    tl.e = t / per;
-    int l = t - tl.e * per;
-    int mt;
-    if (l < a.wg_t1) { tl.which = 0; mt = a.wg_mt1; }
-    else if (l < 2 * a.wg_t1) { tl.which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
-    else { tl.which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
-    tl.m0 = (l % mt) * BM;
-    tl.n0 = (l / mt) * BN;
-    int lo = s_off[tl.e], hi = s_off[tl.e + 1];
-    lo = max(0, min(lo, a.R));
-    hi = max(lo, min(hi, a.R));
-    tl.krow0 = lo;
-    tl.krows = hi - lo;
-    tl.nkb = (tl.krows + BK - 1) / BK;
-  } else {
-    const RowTile r = decode_row_tile(t, a.E, a.R, s_off, s_ts);
-    tl.e = r.e;
-    tl.row0 = r.row0;
-    tl.rows = r.rows;
-    tl.n0 = r.n_idx * (MODE == kUp ? BN / 2 : BN);
-    tl.nkb = a.kb_total;
-  }
+  const RowTile r = decode_row_tile(t, a.E, a.R, s_off, s_ts);
+  tl.e = r.e;
+  tl.row0 = r.row0;
+  tl.rows = r.rows;
+  tl.n0 = r.n_idx * (MODE == kUp ? BN / 2 : BN);
+  tl.nkb = a.kb_total;
   return tl;
 }
 
@@ -136,20 +121,12 @@ __device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa,
   } else if constexpr (MODE == kDA) {
     tma_load_2d(sa, a0, bar, kb * BK, tl.row0);
     tma_load_3d(sb, b0, bar, kb * BK, tl.n0, tl.e);
-  } else if constexpr (MODE == kDX) {
+  } else {  // kDX
+    static_assert(MODE == kDX, "the weight-gradient GEMM runs on CTA pairs only");
     const bool second = kb >= a.kb_split;
     const int kk = (second ? kb - a.kb_split : kb) * BK;
     tma_load_2d(sa, second ? a1 : a0, bar, kk, tl.row0);
     tma_load_3d(sb, second ? b1 : b0, bar, kk, tl.n0, tl.e);
-  } else {  // kWG: the expert's own descriptors (rows past its end read as 0)
-    const int y = tl.krow0 + kb * BK;
-    const CUtensorMap* em = a.wg_maps + (size_t)tl.e * kWgradMaps;
-    const CUtensorMap* am = em + (tl.which == 2 ? 1 : 0);
-    const CUtensorMap* bm = em + 2 + tl.which;
-    tma_load_2d(sa, am, bar, tl.m0, y);
-    tma_load_2d(sa + SUB, am, bar, tl.m0 + 64, y);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * SUB, bm, bar, tl.n0 + 64 * c, y);
   }
 }
 
@@ -325,13 +302,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     fence_mbar_init();
   }
   __syncthreads();
-  if constexpr (MODE == kWG) {
-    if (threadIdx.x == 0) sh->total_tiles = args.E * (2 * args.wg_t1 + args.wg_t2);
-  } else {
-    if (warp == 0) {
-      const int n = build_row_tile_table(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
-      if (lane == 0) sh->total_tiles = n;
-    }
+  if (warp == 0) {
+    const int n = build_row_tile_table(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
+    if (lane == 0) sh->total_tiles = n;
   }
   __syncthreads();
   const int total = sh->total_tiles;
@@ -356,23 +329,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     // the whole warp walks the schedule (converged); lane 0 issues the copies
     int stage = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
-    int wg_e = -1;                          // WG: expert of the descriptors acquired
-    uint32_t wg_seen = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
-      if constexpr (MODE == kWG) {
-        // the descriptors were written by an earlier kernel through the
-        // generic proxy; make them visible to the tensormap proxy, once per
-        // descriptor (a CTA meets the experts in increasing order)
-        if (lane == 0 && tl.nkb > 0) {
-          if (tl.e != wg_e) { wg_e = tl.e; wg_seen = 0; }
-          const CUtensorMap* em = args.wg_maps + (size_t)tl.e * kWgradMaps;
-          const int oa = tl.which == 2 ? 1 : 0, ob = 2 + tl.which;
-          if (!(wg_seen & (1u << oa))) { tensormap_acquire(em + oa); wg_seen |= 1u << oa; }
-          if (!(wg_seen & (1u << ob))) { tensormap_acquire(em + ob); wg_seen |= 1u << ob; }
-        }
-      }
       for (int kb = 0; kb < tl.nkb; ++kb) {
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
@@ -395,9 +354,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    constexpr bool a_mn = (MODE == kWG);
-    constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kWG);
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, a_mn, b_mn);
+    constexpr bool b_mn = (MODE == kUp || MODE == kDown);   // A (rows) is always K-major
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, b_mn);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
@@ -410,8 +368,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         if (lane == 0) mbar_arrive(smem_u32(&sh->tfull[acc]));
       } else {
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          int nkk = BK / 16;
-          if constexpr (MODE == kWG) nkk = wg_groups(tl, kb);
+          constexpr int nkk = BK / 16;
           if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) {
             ok = false;
             break;
@@ -421,9 +378,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
           const uint32_t sb = smem_u32(sB + stage * B_STAGE);
           if (lane == 0) {
             for (int kk = 0; kk < nkk; ++kk) {
-              uint64_t ad, bd;
-              if constexpr (a_mn) ad = sdesc_sw128(sa + kk * 2048, SUB, 1024);
-              else ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              uint64_t bd;
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
               if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
               else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
               mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
