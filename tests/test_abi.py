@@ -108,3 +108,32 @@ def test_wgrad_workspace_holds_the_per_expert_descriptors(lib):
     assert lib.moe_grouped_swiglu_bwd_wgrad(*args(fake, 256 + 640 * 127)) == -3
     # descriptors must sit on 128-byte boundaries
     assert lib.moe_grouped_swiglu_bwd_wgrad(*args(ctypes.c_void_p(0x1010), need)) == -1
+
+
+def test_router_and_mxfp8_additions_check_arguments_on_the_host(lib):
+    NULL = None
+    fake = ctypes.c_void_p(0x1000)
+    big = 1 << 30
+    # tensor-core router: d must give 16-byte rows of x; a workspace is required
+    assert lib.moe_router_logits_tc(fake, fake, NULL, 64, 12, 8, fake, fake, big, NULL) == -2
+    assert lib.moe_router_logits_tc(fake, fake, NULL, 64, 16, 8, fake, NULL, 0, NULL) == -3
+    assert lib.moe_router_logits_tc(fake, fake, NULL, 64, 16, 2000, fake, fake, big, NULL) == -1
+    # ... and the scratch for the three bf16 parts of W_r (6 E ceil(d/64)*64 bytes)
+    assert lib.moe_router_logits_tc(fake, fake, NULL, 64, 2048, 128, fake, fake,
+                                    256 + 6 * 128 * 2048 - 1, NULL) == -3
+    # router backward through the top-k: d % 8, k <= E, workspace size
+    assert lib.moe_router_logits_bwd_topk(fake, fake, fake, fake, fake, fake, 64, 12, 8, 2,
+                                          fake, fake, NULL, fake, big, NULL) == -2
+    assert lib.moe_router_logits_bwd_topk(fake, fake, fake, fake, fake, fake, 64, 16, 4, 8,
+                                          fake, fake, NULL, fake, big, NULL) == -1
+    assert lib.moe_router_logits_bwd_topk(fake, fake, fake, fake, fake, fake, 64, 16, 8, 2,
+                                          fake, fake, NULL, fake, 300, NULL) == -3
+    # MXFP8: dequantise needs K % 32, the fp32-master quantiser N % 128
+    assert lib.moe_mxfp8_dequantize_rows(fake, fake, 4, 48, fake, NULL) == -2
+    assert lib.moe_mxfp8_dequantize_rows(fake, NULL, 4, 64, fake, NULL) == -1
+    assert lib.moe_mxfp8_quantize_weights_f32(fake, 2, 64, 96, fake, fake, NULL) == -2
+    # T = 0 / rows = 0 launch nothing
+    before = lib.moe_launch_count()
+    assert lib.moe_router_logits_tc(NULL, NULL, NULL, 0, 16, 8, NULL, fake, big, NULL) == 0
+    assert lib.moe_mxfp8_dequantize_rows(NULL, NULL, 0, 64, NULL, NULL) == 0
+    assert lib.moe_launch_count() == before
