@@ -203,6 +203,18 @@ class ClockSampler:
                 "samples": len(inside), "which": how, "interval_ms": 50}
 
 
+def capacity_stats(counts, T: int, k: int, E: int, factor: float = 1.25):
+    """What a layer padded to one capacity per expert would do with these
+    per-expert row counts: capacity ceil(factor*T*k/E), every expert keeping
+    at most that many rows.  Host arithmetic on the device's counts."""
+    import math
+    C = int(math.ceil(factor * T * k / E))
+    R = T * k
+    dropped = int(sum(max(0, int(c) - C) for c in counts))
+    return {"capacity_factor": factor, "capacity": C, "dropped_rows": dropped,
+            "dropped_fraction": dropped / R, "padded_over_routed_rows": E * C / R}
+
+
 # ----------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -299,9 +311,12 @@ def run_ours(args):
     def tile_overhead(layer):
         """Rows the row-grouped GEMMs multiply beyond the T*k routed rows: each
         expert's last tile of 256 (CTA pairs) or 128 rows (single CTAs) is only
-        partly filled.  Read from the device counts after the timed steps."""
+        partly filled.  Read from the device counts after the timed steps,
+        with what a capacity-padded layer would drop from the same counts."""
         c = layer.counts.cpu().numpy().astype(np.int64)
-        return {f"tiles_{t}": float((-(-c // t) * t).sum() / layer.R - 1.0) for t in (256, 128)}
+        out = {f"tiles_{t}": float((-(-c // t) * t).sum() / layer.R - 1.0) for t in (256, 128)}
+        out["capacity_padding"] = capacity_stats(c, layer.T, layer.k, layer.E)
+        return out
 
     def timed(w, inp, K, W, with_e2e, sample_clocks=True):
         layer = make_layer(w, inp)

@@ -27,3 +27,15 @@ def test_mxfp8_saved_activations_keep_codes_and_scales():
     assert b["saved"] - b["mxfp8_saved"] == (2 * R * d - (R * d + R * d // 32)) + \
         (2 * R * h - (R * h + R * h // 32))
     assert b["recompute"] < b["mxfp8_saved"] < b["saved"]
+
+
+def test_bench_capacity_stats_by_hand():
+    # 3 experts, T*k = 12 routed rows, capacity ceil(1.25 * 12 / 3) = 5:
+    # loads 9, 3, 0 drop 4 rows; the padded layer multiplies 15 rows for 12
+    import bench
+    st = bench.capacity_stats([9, 3, 0], T=6, k=2, E=3)
+    assert st["capacity"] == 5 and st["dropped_rows"] == 4
+    assert abs(st["dropped_fraction"] - 4 / 12) < 1e-12
+    assert abs(st["padded_over_routed_rows"] - 15 / 12) < 1e-12
+    # enough capacity: nothing dropped
+    assert bench.capacity_stats([4, 4, 4], T=6, k=2, E=3)["dropped_rows"] == 0
