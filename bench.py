@@ -427,13 +427,20 @@ def run_ours(args):
             traffic = prof["dram_bytes_per_launch"]
     except (OSError, ValueError):
         pass
+    # The timed region is tens of milliseconds at full SM clock (see "clocks"),
+    # so the tensor-bound kernels are measured against the burst cuBLAS peak;
+    # the sustained one (seconds-long loop under the power cap, lower clock)
+    # is reported beside it.
+    sm_mhz = (main.get("clocks") or {}).get("sm_mhz")
+    burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
     if dom in flops:
         ach = flops[dom] / (km[dom] / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": traffic,
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": burst, "unit": "TFLOP/s",
+                "frac": ach / burst, "traffic": traffic,
                 "algorithmic_flops_per_launch": flops[dom],
-                "peak_note": f"{peaks['source']} cuBLAS bf16, sustained"}
+                "frac_of_sustained": ach / sustained, "sm_mhz_median": sm_mhz,
+                "peak_note": f"{peaks['source']} cuBLAS bf16, burst (sustained {sustained:.1f} "
+                             f"TFLOP/s reported as frac_of_sustained)"}
     else:
         ach = bytes_[dom] / (km[dom] / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -457,12 +464,13 @@ def run_ours(args):
                    "l2": "flushed between timed steps (256 MB write, twice the L2)",
                    "parallelism": f"{world} replica(s), token-sharded, no data-path collective"},
         "roofline": roof,
-        "gemm": {"tflops": gemm_tflops, "frac_of_peak": gemm_tflops / peaks["bf16_tflops_sustained"],
-                 "ms": gemm_ms,
-                 # each grouped GEMM against the same sustained bf16 peak
+        "gemm": {"tflops": gemm_tflops, "frac_of_peak": gemm_tflops / burst,
+                 "frac_of_sustained": gemm_tflops / sustained, "ms": gemm_ms,
+                 "peak": burst, "peak_note": "burst cuBLAS bf16", "sm_mhz_median": sm_mhz,
+                 # each grouped GEMM against the same burst bf16 peak
                  "per_kernel": {k: {"ms": km[k], "tflops": flops[k] / (km[k] / 1e3) / 1e12,
-                                    "frac_of_peak": flops[k] / (km[k] / 1e3) / 1e12
-                                    / peaks["bf16_tflops_sustained"]} for k in gemm_labels}},
+                                    "frac_of_peak": flops[k] / (km[k] / 1e3) / 1e12 / burst}
+                                for k in gemm_labels}},
         "dispatch_gbs": rows.get("dispatch", {}).get("GB_s"),
         "row_kernels": rows,
         "kernels_ms": km,
@@ -519,10 +527,10 @@ def run_ours(args):
             "step_speedup": bf["ms_per_step"] / mx["ms_per_step"],
             "step_speedup_cached_weights": bf["ms_per_step"] / mxc["ms_per_step"],
             "fwd_gemm_speedup": bf_fwd / mx_fwd,
-            # the fp8 dense peak taken as twice the measured sustained bf16 one
-            # (the nominal fp8 / bf16 ratio of the part)
-            "fwd_gemm_frac_of_fp8_peak": fwd_flops / (mx_fwd / 1e3) / 1e12
-                                         / (2 * peaks["bf16_tflops_sustained"]),
+            # the fp8 dense peak taken as twice the measured burst bf16 one
+            # (the nominal fp8 / bf16 ratio of the part, 4.5 / 2.25 PFLOP/s)
+            "fwd_gemm_frac_of_fp8_peak": fwd_flops / (mx_fwd / 1e3) / 1e12 / (2 * burst),
+            "fp8_peak": 2 * burst,
             "unit": UNIT, "units_note": "fp8 GEMM TFLOP/s compare to a 2x higher tensor peak than bf16",
             "kernels_ms_mxfp8": mx["kernels_ms"],
         }

@@ -170,7 +170,8 @@ int moe_router_logits_bwd_topk(const moe_bf16_t* x, const float* W_r, const floa
  *                   offsets[e] + number of slots s' < s routed to e (stable)
  *   slot_of_row[R]  inverse permutation
  * No host synchronisation.  An expert id outside [0, E) sets
- * MOE_DEV_BAD_EXPERT_ID in the workspace status word. */
+ * MOE_DEV_BAD_EXPERT_ID in the workspace status word; that slot gets
+ * row_of_slot = -1 and takes no row (offsets[E] is then below T*k). */
 int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E,
                        int32_t* counts, int32_t* offsets,
                        int32_t* row_of_slot, int32_t* slot_of_row,
@@ -192,6 +193,9 @@ int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E,
  *    Clear it yourself before the call if you read it.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    The address is looked up again when the device's context has changed
+ *    since (after cudaDeviceReset the array lives at a new address), so the
+ *    first call after a reset must also come before any capture.
  *  - All calls share the one array and no call clears it (every entry a call
  *    reads is written earlier in that call): calls that can overlap on the
  *    GPU (different streams, or concurrent host threads) race and must be
@@ -205,7 +209,10 @@ int moe_expert_offsets_noalloc(const int32_t* topk_idx, int T, int k, int E,
 /* ------------------------------------------------------- dispatch/combine */
 
 /* Rowwise dispatch: xp[row_of_slot[t*k+j], :] = x[t, :] for all t, j.
- * x[T,d] bf16 -> xp[T*k, d] bf16 (expert-contiguous).  Exact copy. */
+ * x[T,d] bf16 -> xp[T*k, d] bf16 (expert-contiguous).  Exact copy.
+ * Here and in every call below that reads row_of_slot, an entry outside
+ * [0, T*k) (the -1 of a slot with a bad expert id) is skipped: no row is
+ * written through it, a combine adds nothing for it, and its dgate is 0. */
 int moe_dispatch_rows(const moe_bf16_t* x, int T, int d, int k,
                       const int32_t* row_of_slot, moe_bf16_t* xp,
                       moe_stream_t stream);

@@ -199,8 +199,8 @@ def test_bad_expert_id_sets_device_status_without_faulting():
     idx[17, 1] = E + 3
     counts = torch.empty(E, dtype=torch.int32, device=DEV)
     offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
-    ros = torch.full((T * k,), -1, dtype=torch.int32, device=DEV)
-    sor = torch.full((T * k,), -1, dtype=torch.int32, device=DEV)
+    ros = torch.full((T * k,), -7, dtype=torch.int32, device=DEV)
+    sor = torch.full((T * k,), -7, dtype=torch.int32, device=DEV)
     ws = _ws(T, E, k)
     L.moe_reset_status(ws)
     L.moe_expert_offsets(torch.from_numpy(idx).to(DEV), E, counts, offs, ros, sor, ws)
@@ -208,6 +208,52 @@ def test_bad_expert_id_sets_device_status_without_faulting():
     assert i32(counts).sum() == T * k - 1
     torch.cuda.synchronize()                     # the context is still healthy
     L.moe_reset_status(ws)
+    assert L.moe_get_status(ws) == 0
+    # the bad slot takes no row; every valid slot keeps its oracle row
+    bad = 17 * k + 1
+    rows = i32(ros)
+    assert rows[bad] == -1
+    good = np.ones(T * k, bool); good[bad] = False
+    # the valid slots in slot order form a route map of their own (k = 1)
+    flat = idx.reshape(-1)
+    _, _, expect, _ = ol.route_map(flat[good].reshape(-1, 1), E)
+    assert np.array_equal(rows[good], expect)
+    # the row kernels run on the map with the -1 entry and stay inside their
+    # buffers (guard bands of sentinel rows on both sides)
+    d, G = 64, 4
+    rng = np.random.default_rng(6)
+    x = bf16_tensor(wl.bf16_bits(rng.standard_normal((T, d)).astype(np.float32)), DEV)
+    g = torch.from_numpy(rng.random((T, k)).astype(np.float32)).to(DEV)
+    sent = torch.full(((T * k + 2 * G), d), 7.0, dtype=torch.bfloat16, device=DEV)
+    xp = sent[G:G + T * k]
+    L.moe_dispatch_rows(x, ros, k, xp)
+    yp_full = torch.full(((T * k + 2 * G), d), 7.0, dtype=torch.bfloat16, device=DEV)
+    yp = yp_full[G:G + T * k]
+    yp.copy_(xp)
+    out_full = torch.full((T + 2 * G, d), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = out_full[G:G + T]
+    L.moe_combine(yp, ros, g, k, out)
+    dyp_full = torch.full(((T * k + 2 * G), d), 7.0, dtype=torch.bfloat16, device=DEV)
+    dyp = dyp_full[G:G + T * k]
+    dg = torch.full((T, k), 5.0, dtype=torch.float32, device=DEV)
+    L.moe_combine_bwd(x, yp, ros, g, k, dyp, dg)
+    xq_full = torch.full(((T * k + 2 * G), d), 9, dtype=torch.uint8, device=DEV)
+    xs_full = torch.full(((T * k + 2 * G), d // 32), 9, dtype=torch.uint8, device=DEV)
+    L.moe_dispatch_rows_mxfp8(x, ros, k, xq_full[G:G + T * k], xs_full[G:G + T * k])
+    torch.cuda.synchronize()
+    for name, full, n in (("xp", sent, T * k), ("out", out_full, T), ("dyp", dyp_full, T * k)):
+        f = as_f64(full)
+        assert np.all(f[:G] == 7.0) and np.all(f[G + n:] == 7.0), name
+    for name, full in (("xq", xq_full), ("xs", xs_full)):
+        f = full.cpu().numpy()
+        assert np.all(f[:G] == 9) and np.all(f[G + T * k:] == 9), name
+    # valid slots: exact copies and sums of the oracle's; the bad slot adds 0
+    xf = as_f64(x)
+    assert np.array_equal(as_f64(xp)[rows[good]], np.repeat(xf, k, axis=0)[good])
+    gg = as_f64(g).copy(); gg[17, 1] = 0.0
+    ref_out = ol.combine(as_f64(yp), rows.clip(0), gg, k)
+    assert_close(out, ref_out, "combine with a skipped slot")
+    assert as_f64(dg)[17, 1] == 0.0
     assert L.moe_get_status(ws) == 0
 
 

@@ -186,6 +186,9 @@ def test_recompute_backward_matches_saved_bitwise(T, E):
     assert L.moe_get_status(layer.ws) == 0
     for n, v in saved.items():
         assert torch.equal(getattr(layer, n), v), n
+    # and the recomputed step against the fp64 oracle, tensor by tensor (the
+    # recomputed Xp, H1, H3, A included)
+    compare_full(layer, w, inp)
 
 
 @pytest.mark.parametrize("T,E", [(333, 5), (1400, 2)])    # single-CTA / CTA-pair row GEMMs
@@ -263,6 +266,10 @@ def _sampled_reference(inp, w, idx, g, ros, toks, hs, experts):
             out_t += g[t, j] * f["Yp"][0]
             dX_t += b["dXp"][0]
             dg_t[j] = float(dY[t] @ f["Yp"][0])
+        if "W_r" in inp:
+            # learned router: dX also carries dz W_r^T through the top-k softmax
+            dz = ol.router_topk_backward(g[t:t + 1], dg_t[None], idx[t:t + 1], w.E)
+            dX_t += ol.router_logits_backward(x[t:t + 1], inp["W_r"], dz)[0][0]
         res["out"].append(out_t); res["dX"].append(dX_t); res["dgate"].append(dg_t)
     # weight gradients of sampled experts, restricted to hidden units hs
     wg = {}
@@ -327,8 +334,7 @@ def test_full_size_sampled(key):
     assert_close(layer.out[tk], np.array(res["out"]), "out")
     assert_close(layer.dxp[rows], np.array(res["dxp"]), "dxp")
     assert_close(layer.dgate[tk], np.array(res["dgate"]), "dgate")
-    if w.routing == "uniform":
-        assert_close(layer.dX[tk], np.array(res["dX"]), "dX")
+    assert_close(layer.dX[tk], np.array(res["dX"]), "dX")
     hst = torch.tensor(hs, device=DEV, dtype=torch.long)
     for e, v in wg.items():
         if v is None:

@@ -172,7 +172,7 @@ def _mx_layer(w, inp):
     (2600, 512, 4, 2, 256, (1,)),
     (700, 128, 1, 1, 128, ()),
 ])
-def test_grouped_forward_mxfp8_small(T, d, E, k, h, empty):
+def test_grouped_forward_mxfp8_small(T, d, E, k, h, empty, record_property):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
     inp = wl.generate(w, seed=2, with_backward=False)
     if empty:
@@ -192,7 +192,15 @@ def test_grouped_forward_mxfp8_small(T, d, E, k, h, empty):
     assert_close(t["yp"], ref["Yp"], "yp", rel_l2=MX_REL_L2, max_abs=0.1)
     exact = ol.expert_ffn_forward(Xp, off, inp["W1"], inp["W3"], inp["W2"])["Yp"]
     rel = np.linalg.norm(as_f64(t["yp"]) - exact) / np.linalg.norm(exact)
-    assert rel < 0.12                       # E4M3 precision against the unquantised layer
+    # the MXFP8 output against the unquantised fp64 layer: reported (pytest -s
+    # prints it; junit XML carries it as a property) and bounded by what E4M3's
+    # 3 mantissa bits allow through two quantised GEMMs and a quantised A
+    rel_q = np.linalg.norm(as_f64(t["yp"]) - ref["Yp"]) / np.linalg.norm(ref["Yp"])
+    record_property("yp_rel_l2_vs_unquantised", float(rel))
+    record_property("yp_rel_l2_vs_quantised", float(rel_q))
+    print(f"\nMXFP8 yp T={T} d={d} E={E} k={k} h={h}: rel-L2 {rel:.4f} vs the unquantised "
+          f"layer, {rel_q:.2e} vs the quantise-dequantise oracle")
+    assert 0.02 < rel < 0.12
     for e in empty:
         assert c[e] == 0
 

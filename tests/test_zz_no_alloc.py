@@ -1,4 +1,5 @@
-"""The allocation-free route map agrees with the workspace version.
+"""The allocation-free route map agrees with the workspace version and with
+the oracle.
 
 moe_expert_offsets_noalloc serves callers that cannot allocate device memory
 (stream capture, engines that hand over only their own arena's tensors,
@@ -11,6 +12,8 @@ run every other test; it also passes alone in a fresh process.
 import ctypes
 
 import numpy as np
+
+import oracle.layer as ol
 import pytest
 import torch
 
@@ -48,8 +51,12 @@ def test_no_alloc_route_map_equals_workspace_route_map(T, k, E):
         L.moe_expert_offsets(idx, E, *ref, ws)
         L.moe_expert_offsets_noalloc(idx, E, *got, status)
         torch.cuda.synchronize()
-        for a, b, name in zip(got, ref, ("counts", "offsets", "row_of_slot", "slot_of_row")):
+        names = ("counts", "offsets", "row_of_slot", "slot_of_row")
+        for a, b, name in zip(got, ref, names):
             assert torch.equal(a, b), (call, name)
+        # bit-exact against the plain definition as well (expert 1 is empty)
+        for a, o, name in zip(got, ol.route_map(idx.cpu().numpy(), E), names):
+            assert np.array_equal(a.cpu().numpy(), o), (call, name, "oracle")
         assert int(status.item()) == 0
         assert L.moe_get_status(ws) == 0
 
@@ -70,4 +77,10 @@ def test_no_alloc_reports_bad_ids_and_rejects_oversize():
     fake = ctypes.c_void_p(out[0].data_ptr())
     rc = lib.moe_expert_offsets_noalloc(fake, 262145, 1, 8, fake, fake, fake, fake, None, None)
     assert rc == -2                          # MOE_ERR_UNSUPPORTED
+    assert L.moe_launch_count() == before
+    # the binding checks the optional status word like every other output
+    for bad in (torch.zeros(1, dtype=torch.int32), torch.zeros(1, dtype=torch.int64, device=DEV),
+                torch.zeros(0, dtype=torch.int32, device=DEV)):
+        with pytest.raises(ValueError):
+            L.moe_expert_offsets_noalloc(idx, E, *out, bad)
     assert L.moe_launch_count() == before

@@ -136,6 +136,11 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// A row index read from a route map is used only inside [0, R): slots whose
+// expert id was out of range carry row -1 (and a caller-built map may hold
+// anything), so the row kernels skip such rows instead of writing through them.
+__device__ __forceinline__ bool row_ok(int row, int R) { return (unsigned)row < (unsigned)R; }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -172,7 +172,8 @@ dispatch_mxfp8_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
   if (t >= T) return;
   int rows[kMaxTopK];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
+  for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : -1;
+  const int R = T * k;
   const uint16_t* src = x + (size_t)t * d;
   // 8 elements per lane, 256 per warp and step; all lanes take every step so
   // the shuffles below always see the full warp (d is a multiple of 32, so a
@@ -197,7 +198,7 @@ dispatch_mxfp8_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
     o.y = e4m3x4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
+      if (row_ok(rows[j], R)) {
         const size_t r = (size_t)rows[j];
         *reinterpret_cast<uint2*>(xq + r * d + c0) = o;
         if ((lane & 3) == 0) xs[r * (d / 32) + c0 / 32] = (uint8_t)(e + 127);

@@ -24,13 +24,14 @@ __global__ void __launch_bounds__(kThreads)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
                 const int32_t* __restrict__ row_of_slot, uint16_t* __restrict__ xp) {
   pdl_enter();
+  const int R = T * k;
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const int nvec = d >> 3;
   int rows[kMaxTopK];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
+  for (int j = 0; j < kMaxTopK; ++j) rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : -1;
   const uint16_t* src = x + (size_t)t * d;
   for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
     uint4 val[U];
@@ -41,7 +42,7 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
     }
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
+      if (row_ok(rows[j], R)) {
         uint16_t* dst = xp + (size_t)rows[j] * d;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -74,9 +75,10 @@ combine_kernel(const uint16_t* __restrict__ yp, const int32_t* __restrict__ row_
   float g[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
-    rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : 0;
+    rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : -1;
     g[j] = (j < k) ? (gate ? __ldg(gate + (size_t)t * k + j) : 1.f) : 0.f;
   }
+  const int R = T * k;
   uint16_t* dst = out + (size_t)t * d;
   for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
     float acc[U][8];
@@ -86,7 +88,7 @@ combine_kernel(const uint16_t* __restrict__ yp, const int32_t* __restrict__ row_
       for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
+      if (row_ok(rows[j], R)) {
         const uint16_t* src = yp + (size_t)rows[j] * d;
         uint4 val[U];
 #pragma unroll
@@ -149,9 +151,12 @@ combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict
   const int nvec = d >> 3;
   int rows[K];
   float g[K], dot[K];
+  bool ok[K];
 #pragma unroll
   for (int j = 0; j < K; ++j) {
     rows[j] = __ldg(row_of_slot + (size_t)t * K + j);
+    ok[j] = row_ok(rows[j], T * K);
+    if (!ok[j]) rows[j] = 0;                   // read a valid row; store and dot skipped
     g[j] = __ldg(gate + (size_t)t * K + j);
     dot[j] = 0.f;
   }
@@ -178,7 +183,7 @@ combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + 32 * u;
-        if (v < nvec) {
+        if (v < nvec && ok[j]) {
           dot[j] = dot8(dv[u], yv[j][u], dot[j]);
           st_v4(dr + (size_t)v * 8, scale8(dv[u], g[j]));
         }

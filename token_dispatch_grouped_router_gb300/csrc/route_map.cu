@@ -171,7 +171,10 @@ __global__ void route_place_kernel(const int32_t* __restrict__ idx, int R, int E
   int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= R) return;
   int e = __ldg(idx + s);
-  if (e < 0 || e >= E) return;                 // reported by route_count
+  if (e < 0 || e >= E) {                       // reported by route_count
+    row_of_slot[s] = -1;                       // the row kernels skip it
+    return;
+  }
   int b = s / kRouteChunk;
   int row = __ldg(offsets + e) + __ldg(chunk_base + (size_t)b * E + e) + __ldg(local_rank + s);
   row_of_slot[s] = row;
@@ -243,21 +246,58 @@ static __device__ __align__(256) int32_t
     g_route_scratch[kNoAllocDummyInts + kNoAllocChunkInts + kNoAllocMaxSlots];
 
 std::mutex g_noalloc_mu;
-int32_t* g_noalloc_base[64] = {nullptr};
+struct NoAllocSlot { unsigned long long ctx_id; int32_t* base; };
+NoAllocSlot g_noalloc[64] = {};
 
-// Device address of g_route_scratch on the current device (looked up once per
-// device; the host-side symbol itself is not a device address).
+// Unique id of the calling thread's current context (never reused within a
+// process), through the driver entry points the runtime exposes; 0 if there
+// is none yet or the driver lacks the query.
+unsigned long long current_ctx_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+    (void)cudaGetLastError();
+    looked = true;
+  }
+  if (!get_current || !get_id) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Device address of g_route_scratch in the current context (the host-side
+// symbol itself is not a device address).  It is looked up on the first call
+// on a device and again whenever that device's context has changed since
+// (after a cudaDeviceReset the module, and with it the array, is loaded
+// afresh at another address).
 int32_t* noalloc_scratch(int dev) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_base[dev] == nullptr) {
+  NoAllocSlot& slot = g_noalloc[dev];
+  const unsigned long long id = current_ctx_id();
+  if (slot.base == nullptr || id == 0 || slot.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) {
       (void)cudaGetLastError();
+      slot.base = nullptr;
       return nullptr;
     }
-    g_noalloc_base[dev] = static_cast<int32_t*>(p);
+    slot.base = static_cast<int32_t*>(p);
+    slot.ctx_id = current_ctx_id();        // the lookup may have created the context
   }
-  return g_noalloc_base[dev];
+  return slot.base;
 }
 
 }  // namespace

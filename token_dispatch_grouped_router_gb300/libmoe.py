@@ -231,6 +231,10 @@ def moe_expert_offsets_noalloc(topk_idx, E: int, counts, offsets, row_of_slot, s
     _want(offsets, torch.int32, (E + 1,), "offsets")
     _want(row_of_slot, torch.int32, (T * k,), "row_of_slot")
     _want(slot_of_row, torch.int32, (T * k,), "slot_of_row")
+    if status is not None:
+        _want(status, torch.int32, (1,), "status")
+        if status.device != topk_idx.device:
+            raise ValueError(f"status: expected a tensor on {topk_idx.device}, got {status.device}")
     _ok("moe_expert_offsets_noalloc", load().moe_expert_offsets_noalloc(
         _ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(row_of_slot),
         _ptr(slot_of_row), _ptr(status), _stream()))
