@@ -146,3 +146,80 @@ def test_mxfp8_forward_error_matches_format_precision():
     h1x = Xp[off[0]:off[1]] @ W1[0]
     rel1 = np.linalg.norm(h1 - h1x) / np.linalg.norm(h1x)
     assert 0.015 < rel1 < 0.06
+
+
+def _padded_case(seed, T=12, d=5, E=3, k=2, h=4):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, d))
+    W1 = rng.standard_normal((E, d, h)) / 2; W3 = rng.standard_normal((E, d, h)) / 2
+    W2 = rng.standard_normal((E, h, d)) / 2
+    W_r = rng.standard_normal((d, E))
+    dOut = rng.standard_normal((T, d))
+    return x, W1, W3, W2, W_r, dOut
+
+
+def test_padded_backward_finite_differences_with_drops():
+    # learned router, capacity below the hottest expert's load: the central
+    # differences of <dOut, out> must match every gradient the backward returns
+    T, d, E, k, h = 12, 5, 3, 2, 4
+    x, W1, W3, W2, W_r, dOut = _padded_case(11, T, d, E, k, h)
+    idx = ol.topk(x @ W_r, k)
+    C = 6
+    counts = np.bincount(idx.reshape(-1), minlength=E)
+    assert counts.max() > C                      # some slots are dropped
+
+    def loss(x_, W1_, W3_, W2_, W_r_):
+        g = ol.topk_gates(x_ @ W_r_, idx)
+        return float((dOut * pd.padded_forward(x_, idx, g, W1_, W3_, W2_, E, C)["out"]).sum())
+
+    g = ol.topk_gates(x @ W_r, idx)
+    b = pd.padded_backward(x, idx, g, W1, W3, W2, dOut, E, C, W_r=W_r)
+    args = [x, W1, W3, W2, W_r]
+    eps = 1e-6
+    for which, grad in ((0, b["dX"]), (1, b["dW1"]), (2, b["dW3"]), (3, b["dW2"]), (4, b["dW_r"])):
+        num = np.zeros_like(args[which])
+        for i in np.ndindex(args[which].shape):
+            plus = [a.copy() for a in args]; minus = [a.copy() for a in args]
+            plus[which][i] += eps; minus[which][i] -= eps
+            num[i] = (loss(*plus) - loss(*minus)) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-5, atol=1e-6)
+    # a dropped slot has no gate gradient; a kept one does
+    p = pd.padded_forward(x, idx, g, W1, W3, W2, E, C)
+    assert np.all(b["dg"][~p["kept"]] == 0) and np.all(b["dg"][p["kept"]] != 0)
+
+
+def test_padded_backward_with_enough_capacity_equals_unpadded():
+    T, d, E, k, h = 30, 8, 4, 2, 6
+    rng = np.random.default_rng(12)
+    inp = dict(x=rng.standard_normal((T, d)), W1=rng.standard_normal((E, d, h)),
+               W3=rng.standard_normal((E, d, h)), W2=rng.standard_normal((E, h, d)),
+               idx=np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32),
+               glogit=rng.standard_normal((T, k)), dY=rng.standard_normal((T, d)))
+    ref = ol.layer_forward(inp, k, E)
+    refb = ol.layer_backward(inp, ref, k, E)
+    C = int(ref["counts"].max()) + 3               # zero rows in every batch
+    b = pd.padded_backward(inp["x"], inp["idx"], ref["g"], inp["W1"], inp["W3"], inp["W2"],
+                           inp["dY"], E, C)
+    for n, m in (("dX", "dX"), ("dg", "dg"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2"),
+                 ("dz", "dz")):
+        np.testing.assert_allclose(b[n], refb[m], rtol=1e-11, atol=1e-11)
+
+
+def test_padded_backward_drop_by_hand():
+    # T=4, k=1, E=2, capacity 2: token 2 is dropped at expert 0, so it gets no
+    # gradient, and expert 0's weight gradient comes from tokens 0 and 1 only
+    T, d, E, h = 4, 3, 2, 2
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((T, d))
+    W1 = rng.standard_normal((E, d, h)); W3 = rng.standard_normal((E, d, h))
+    W2 = rng.standard_normal((E, h, d))
+    dOut = rng.standard_normal((T, d))
+    idx = np.array([[0], [0], [0], [1]])
+    g = np.ones((T, 1))
+    b = pd.padded_backward(x, idx, g, W1, W3, W2, dOut, E, 2)
+    assert np.all(b["dX"][2] == 0) and b["dg"][2, 0] == 0
+    kept = ol.expert_ffn_forward(x[:2], [0, 2], W1[:1], W3[:1], W2[:1])
+    kb = ol.expert_ffn_backward(x[:2], [0, 2], W1[:1], W3[:1], W2[:1], kept["H1"], kept["H3"],
+                                kept["A"], dOut[:2])
+    for n in ("dW1", "dW3", "dW2"):
+        np.testing.assert_allclose(b[n][0], kb[n][0], rtol=1e-12, atol=1e-12)
