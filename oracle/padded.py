@@ -22,11 +22,37 @@ import numpy as np
 
 from .layer import _f64, _sigmoid, router_topk_backward, silu, route_map
 
-__all__ = ["capacity", "padded_forward", "padded_backward"]
+__all__ = ["capacity", "capacity_route_map", "padded_forward", "padded_backward"]
 
 
 def capacity(T: int, k: int, E: int, factor: float = 1.25) -> int:
     return int(math.ceil(factor * T * k / E))
+
+
+def capacity_route_map(idx: np.ndarray, E: int, C: int):
+    """Route map of the padded layer: expert e owns rows [e*C, (e+1)*C).
+
+    Returns counts[E] (rows kept, min(routed, C)), offsets[E+1] (e*C),
+    row_of_slot[T*k] (e*C + the slot's rank among the slots routed to e in
+    slot order when that rank is below C, else -1 for a dropped slot),
+    slot_of_row[E*C] (the slot a row holds, -1 for a zero row) and routed[E]
+    (rows routed before the cut), all int32.
+    """
+    idx = np.asarray(idx, np.int64)
+    flat = idx.reshape(-1)
+    routed = np.zeros(E, np.int64)
+    row_of_slot = np.full(flat.size, -1, np.int64)
+    slot_of_row = np.full(E * C, -1, np.int64)
+    for s, e in enumerate(flat):                 # slots in order: rank = earlier slots of e
+        rank = routed[e]
+        routed[e] += 1
+        if rank < C:
+            row_of_slot[s] = e * C + rank
+            slot_of_row[e * C + rank] = s
+    counts = np.minimum(routed, C)
+    offsets = np.arange(E + 1, dtype=np.int64) * C
+    i32 = lambda a: a.astype(np.int32)  # noqa: E731
+    return i32(counts), i32(offsets), i32(row_of_slot), i32(slot_of_row), i32(routed)
 
 
 def padded_forward(x, idx, g, W1, W3, W2, E: int, C: int) -> Dict:

@@ -223,3 +223,30 @@ def test_padded_backward_drop_by_hand():
                                 kept["A"], dOut[:2])
     for n in ("dW1", "dW3", "dW2"):
         np.testing.assert_allclose(b[n][0], kb[n][0], rtol=1e-12, atol=1e-12)
+
+
+def test_capacity_route_map_by_hand_and_against_the_kept_mask():
+    # T=4, k=1, E=2, C=2: expert 0 keeps tokens 0, 1 (rows 0, 1) and drops
+    # token 2; expert 1 holds token 3 in row 2 and leaves row 3 empty
+    idx = np.array([[0], [0], [0], [1]])
+    c, o, ros, sor, routed = pd.capacity_route_map(idx, 2, 2)
+    assert list(c) == [2, 1] and list(o) == [0, 2, 4] and list(routed) == [3, 1]
+    assert list(ros) == [0, 1, -1, 2] and list(sor) == [0, 1, 3, -1]
+    # larger: the kept slots are exactly padded_forward's, every kept row maps back
+    T, d, E, k, h = 40, 4, 5, 3, 4
+    rng = np.random.default_rng(14)
+    idx = np.stack([rng.choice(E, k, replace=False, p=[.5, .2, .1, .1, .1]) for _ in range(T)])
+    C = 18
+    c, o, ros, sor, routed = pd.capacity_route_map(idx, E, C)
+    x = rng.standard_normal((T, d))
+    W = rng.standard_normal((E, d, h)); W2 = rng.standard_normal((E, h, d))
+    p = pd.padded_forward(x, idx, np.ones((T, k)), W, W, W2, E, C)
+    assert np.array_equal(ros >= 0, p["kept"].reshape(-1))
+    assert np.array_equal(routed, np.bincount(idx.reshape(-1), minlength=E))
+    kept = np.nonzero(ros >= 0)[0]
+    assert np.array_equal(sor[ros[kept]], kept)
+    assert (sor >= 0).sum() == kept.size == c.sum()
+    for e in range(E):                           # kept rows fill the front of each block
+        blk = sor[e * C:(e + 1) * C]
+        assert np.all(blk[:c[e]] >= 0) and np.all(blk[c[e]:] == -1)
+        assert np.all(np.diff(blk[:c[e]]) > 0)   # in slot order
