@@ -59,6 +59,9 @@ def parse_args():
                          "'' to skip")
     ap.add_argument("--mxfp8-workload", default="train_e128",
                     help="workload of the BF16 vs MXFP8-forward comparison; '' to skip")
+    ap.add_argument("--capacity-factor", type=float, default=1.25,
+                    help="capacity factor of the padded layer timed beside each workload "
+                         "(C = ceil(f*T*k/E)); 0 to skip")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -248,8 +251,9 @@ def run_ours(args):
         if dist:
             dist.barrier()
 
-    def make_layer(w, inp, mxfp8=False):
-        layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=(w.routing == "learned"), device=dev)
+    def make_layer(w, inp, mxfp8=False, capacity_factor=None):
+        layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=(w.routing == "learned"), device=dev,
+                         capacity_factor=capacity_factor)
         layer.load_inputs(inp)
         if mxfp8:
             layer.enable_mxfp8()
@@ -332,7 +336,31 @@ def run_ours(args):
             layer.recompute = False
         del layer
         torch.cuda.empty_cache()
+        if args.capacity_factor > 0:
+            res["padded"] = timed_padded(w, inp, K, W, res["ms_per_step"])
         return res
+
+    def timed_padded(w, inp, K, W, unpadded_ms):
+        """The capacity-padded layer on the same inputs, timed the same way:
+        every expert multiplies C rows (first C routed in token order, then
+        zero rows), later slots are dropped."""
+        layer = make_layer(w, inp, capacity_factor=args.capacity_factor)
+        res = timed_layer(layer, K, W)
+        routed = layer.routed.cpu().numpy().astype(np.int64)
+        R = layer.T * layer.k
+        dropped = int(np.maximum(routed - layer.C, 0).sum())
+        out = {"capacity_factor": args.capacity_factor, "capacity": layer.C,
+               "value": throughput(w.T, world, res["ms_per_step"]), "unit": UNIT,
+               "ms_per_step": res["ms_per_step"],
+               "padded_time_over_unpadded": res["ms_per_step"] / unpadded_ms,
+               "dropped_rows": dropped, "dropped_fraction": dropped / R,
+               "gemm_rows_over_routed": layer.R / R,
+               "kernels_ms": res["kernels_ms"], "gpu_launches": res["launches"],
+               "note": "every expert padded to C rows with zero rows, overflow dropped; same "
+                       "grouped GEMM kernels on E*C rows"}
+        del layer
+        torch.cuda.empty_cache()
+        return out
 
     def e2e(layer, inp, K):
         """Same step through the public API with host inputs: every step copies
@@ -479,6 +507,8 @@ def run_ours(args):
         "clocks": main["clocks"],
         "row_tile_overhead": main["row_tile_overhead"],
     }
+    if "padded" in main:
+        out["padded"] = main["padded"]
     rec = main["recompute"]
     out["recompute"] = {
         "value": throughput(w.T, world, rec["ms_per_step"]), "unit": UNIT,
@@ -492,13 +522,15 @@ def run_ours(args):
         out["compare"] = {"workload": cmp_res["workload"], "value": cv, "unit": UNIT,
                           "ms_per_step": cmp_res["ms_per_step"], "ratio_to_main": cv / value,
                           "kernels_ms": cmp_res["kernels_ms"], "gpu_launches": cmp_res["launches"],
-                          "row_tile_overhead": cmp_res["row_tile_overhead"]}
+                          "row_tile_overhead": cmp_res["row_tile_overhead"],
+                          "padded": cmp_res.get("padded")}
     if skew_res is not None:
         sv = world * wl.get_workload(args.skew_workload).T / (skew_res["ms_per_step"] / 1e3)
         out["skew"] = {"workload": skew_res["workload"], "value": sv, "unit": UNIT,
                        "ms_per_step": skew_res["ms_per_step"], "ratio_to_main": sv / value,
                        "kernels_ms": skew_res["kernels_ms"], "gpu_launches": skew_res["launches"],
                        "row_tile_overhead": skew_res["row_tile_overhead"],
+                       "padded": skew_res.get("padded"),
                        "note": "learned router x W_r + b with a Zipf(1.2) expert bias (seed 0: 100 of 128 "
                                "experts empty, the hottest holds a quarter of the routed rows); "
                                "the step includes the fp32 router GEMM and its backward"}

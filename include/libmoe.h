@@ -309,6 +309,58 @@ int moe_grouped_swiglu_bwd_wgrad(const moe_bf16_t* xp, const int32_t* offsets, i
                                  moe_bf16_t* dW3, moe_bf16_t* dW2, void* ws,
                                  size_t ws_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------ capacity-padded layer */
+/* The alternative the unpadded layer replaces, built on the same kernels so
+ * the two can be timed side by side ("OLMo-core 3：MoE 训练栈让专家池越大、吞吐
+ * 不再越慢", section "另外两处税：主机同步与 padding": without the device route
+ * map every expert batch is padded to one common capacity; the page gives no
+ * capacity formula, so C is the caller's).  Every expert owns exactly C rows
+ * of the expert-sorted buffers, rows [e*C, (e+1)*C): its first C routed slots
+ * in token order (slot order) fill the front of that block, the remaining
+ * rows are zero, and slots beyond the first C are dropped (they contribute
+ * nothing to the output and the other gates are not renormalised).  The
+ * grouped SwiGLU calls run on these buffers unchanged with R = E*C and
+ * offsets[e] = e*C, so they multiply E*C rows however the tokens were
+ * routed. */
+
+/* Capacity-padded route map from topk_idx[T,k]:
+ *   counts[E]        rows kept per expert, min(routed, C)
+ *   offsets[E+1]     e*C (offsets[E] = E*C)
+ *   row_of_slot[T*k] e*C + rank of the slot among expert e's slots in slot
+ *                    order if that rank is below C, else -1 (dropped)
+ *   slot_of_row[E*C] the slot a row holds, -1 for a zero row
+ *   routed[E]        (optional, may be NULL) rows routed to e before the cut
+ * C >= 1 and E*C must fit in int32; ws as for moe_expert_offsets (status
+ * word, route-map scratch and 2 E int32).  A bad expert id sets
+ * MOE_DEV_BAD_EXPERT_ID and its slot is dropped. */
+int moe_expert_offsets_capacity(const int32_t* topk_idx, int T, int k, int E, int C,
+                                int32_t* counts, int32_t* offsets,
+                                int32_t* row_of_slot, int32_t* slot_of_row,
+                                int32_t* routed, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/* Padded dispatch: xp[E*C, d] gets x[t] in row row_of_slot[t*k+j] for every
+ * kept slot and zeros in every row e*C + j with j >= counts[e] (counts from
+ * moe_expert_offsets_capacity).  Two launches (copy, zero rows). */
+int moe_dispatch_rows_capacity(const moe_bf16_t* x, int T, int d, int k,
+                               const int32_t* row_of_slot, const int32_t* counts,
+                               int E, int C, moe_bf16_t* xp, moe_stream_t stream);
+
+/* moe_combine over a padded yp[E*C, d]: out[t] = sum over the kept slots of
+ * gate[t,j] * yp[row(t,j)] (gate == NULL: unit gates, the unpermute-sum). */
+int moe_combine_capacity(const moe_bf16_t* yp, int E, int C, const int32_t* row_of_slot,
+                         const float* gate, int T, int k, int d, moe_bf16_t* out,
+                         moe_stream_t stream);
+
+/* moe_combine_bwd over padded buffers: dyp[row(t,j)] = bf16(gate[t,j] dout[t])
+ * for the kept slots, zeros in the zero rows (as moe_dispatch_rows_capacity),
+ * dgate[t,j] = <dout[t], yp[row(t,j)]> for a kept slot and 0 for a dropped
+ * one. */
+int moe_combine_bwd_capacity(const moe_bf16_t* dout, const moe_bf16_t* yp, int E, int C,
+                             const int32_t* row_of_slot, const int32_t* counts,
+                             const float* gate, int T, int k, int d, moe_bf16_t* dyp,
+                             float* dgate, moe_stream_t stream);
+
 /* ----------------------------------------------------------------- MXFP8 */
 /* MXFP8 = E4M3 codes (uint8) with one E8M0 scale byte (2^(byte-127)) per 32
  * consecutive elements along a GEMM's reduction dimension ("OLMo-core 3：MoE

@@ -137,3 +137,35 @@ def test_router_and_mxfp8_additions_check_arguments_on_the_host(lib):
     assert lib.moe_router_logits_tc(NULL, NULL, NULL, 0, 16, 8, NULL, fake, big, NULL) == 0
     assert lib.moe_mxfp8_dequantize_rows(NULL, NULL, 0, 64, NULL, NULL) == 0
     assert lib.moe_launch_count() == before
+
+
+def test_capacity_calls_check_arguments_on_the_host(lib):
+    NULL = None
+    fake = ctypes.c_void_p(0x1000)
+    big = 1 << 30
+    before = lib.moe_launch_count()
+    # capacity below 1, E*C beyond int32, missing outputs, short workspace
+    assert lib.moe_expert_offsets_capacity(fake, 64, 2, 8, 0, fake, fake, fake, fake, NULL,
+                                           fake, big, NULL) == -1
+    assert lib.moe_expert_offsets_capacity(fake, 64, 2, 8, 1 << 29, fake, fake, fake, fake, NULL,
+                                           fake, big, NULL) == -1
+    assert lib.moe_expert_offsets_capacity(fake, 64, 2, 8, 20, fake, fake, fake, NULL, NULL,
+                                           fake, big, NULL) == -1
+    assert lib.moe_expert_offsets_capacity(fake, 64, 2, 8, 20, fake, fake, fake, fake,
+                                           ctypes.c_void_p(0x1004), fake, big, NULL) == -1
+    assert lib.moe_expert_offsets_capacity(fake, 64, 2, 8, 20, fake, fake, fake, fake, NULL,
+                                           NULL, 0, NULL) == -3
+    assert lib.moe_expert_offsets_capacity(fake, 64, 2, 8, 20, fake, fake, fake, fake, NULL,
+                                           fake, 300, NULL) == -3
+    # padded dispatch / combine / combine backward: sizes and pointers
+    assert lib.moe_dispatch_rows_capacity(fake, 4, 12, 2, fake, fake, 8, 4, fake, NULL) == -1
+    assert lib.moe_dispatch_rows_capacity(fake, 4, 16, 2, fake, NULL, 8, 4, fake, NULL) == -1
+    assert lib.moe_dispatch_rows_capacity(fake, 4, 16, 2, fake, fake, 8, 0, fake, NULL) == -1
+    assert lib.moe_combine_capacity(fake, 8, 0, fake, NULL, 4, 2, 16, fake, NULL) == -1
+    assert lib.moe_combine_capacity(fake, 8, 4, fake, ctypes.c_void_p(0x1004), 4, 2, 16, fake,
+                                    NULL) == -1
+    assert lib.moe_combine_bwd_capacity(fake, fake, 8, 4, fake, NULL, fake, 4, 2, 16, fake, fake,
+                                        NULL) == -1
+    # T = 0: the padded combine does nothing
+    assert lib.moe_combine_capacity(NULL, 8, 4, NULL, NULL, 0, 2, 16, NULL, NULL) == 0
+    assert lib.moe_launch_count() == before

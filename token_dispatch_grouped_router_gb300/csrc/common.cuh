@@ -62,6 +62,19 @@ inline RouteScratch route_scratch(long long R, int E) {
   return L;
 }
 
+// moe_expert_offsets_capacity: the route-map scratch, then the routed
+// (pre-capacity) counts and their offsets.
+struct CapacityScratch { RouteScratch route; size_t routed_counts, routed_offsets, end; };
+
+inline CapacityScratch capacity_scratch(long long R, int E) {
+  CapacityScratch c;
+  c.route = route_scratch(R, E);
+  c.routed_counts = c.route.end;
+  c.routed_offsets = round_up(c.routed_counts + (size_t)E * 4, 256);
+  c.end = round_up(c.routed_offsets + (size_t)(E + 1) * 4, 256);
+  return c;
+}
+
 inline size_t router_scratch_end(int E, int d) {
   return round_up(kStatusBytes + (size_t)kRouterSplits * d * E * 4, 256);
 }
@@ -75,7 +88,7 @@ inline size_t wgrad_parts_end(int E) {
 }
 
 inline size_t workspace_bytes(long long T, int E, int k, int d) {
-  size_t a = route_scratch(T * (long long)k, E).end;
+  size_t a = capacity_scratch(T * (long long)k, E).end;
   size_t b = router_scratch_end(E, d);
   size_t c = wgrad_parts_end(E);
   a = a > b ? a : b;

@@ -22,9 +22,8 @@ constexpr int kWarps = kThreads / 32;
 template <int U>
 __global__ void __launch_bounds__(kThreads)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int d, int k,
-                const int32_t* __restrict__ row_of_slot, uint16_t* __restrict__ xp) {
+                const int32_t* __restrict__ row_of_slot, int R, uint16_t* __restrict__ xp) {
   pdl_enter();
-  const int R = T * k;
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -64,7 +63,7 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float g, uint4 v) {
 // out[t] = sum_j g[t,j] * yp[row(t,j)] in slot order, fp32, one rounding.
 template <int U>
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const uint16_t* __restrict__ yp, const int32_t* __restrict__ row_of_slot,
+combine_kernel(const uint16_t* __restrict__ yp, int R, const int32_t* __restrict__ row_of_slot,
                const float* __restrict__ gate, int T, int k, int d, uint16_t* __restrict__ out) {
   pdl_enter();
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
@@ -78,7 +77,6 @@ combine_kernel(const uint16_t* __restrict__ yp, const int32_t* __restrict__ row_
     rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : -1;
     g[j] = (j < k) ? (gate ? __ldg(gate + (size_t)t * k + j) : 1.f) : 0.f;
   }
-  const int R = T * k;
   uint16_t* dst = out + (size_t)t * d;
   for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
     float acc[U][8];
@@ -141,7 +139,7 @@ __device__ __forceinline__ uint4 scale8(uint4 a, float g) {
 // slot's loads after the previous slot's stores).
 template <int K, int U>
 __global__ void __launch_bounds__(kThreads)
-combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ yp,
+combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ yp, int R,
                    const int32_t* __restrict__ row_of_slot, const float* __restrict__ gate,
                    int T, int d, uint16_t* __restrict__ dyp, float* __restrict__ dgate) {
   pdl_enter();
@@ -155,7 +153,7 @@ combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict
 #pragma unroll
   for (int j = 0; j < K; ++j) {
     rows[j] = __ldg(row_of_slot + (size_t)t * K + j);
-    ok[j] = row_ok(rows[j], T * K);
+    ok[j] = row_ok(rows[j], R);
     if (!ok[j]) rows[j] = 0;                   // read a valid row; store and dot skipped
     g[j] = __ldg(gate + (size_t)t * K + j);
     dot[j] = 0.f;
@@ -198,12 +196,50 @@ combine_bwd_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict
 }
 
 template <int K>
-void launch_combine_bwd(dim3 grid, cudaStream_t s, const uint16_t* dout, const uint16_t* yp,
+void launch_combine_bwd(dim3 grid, cudaStream_t s, const uint16_t* dout, const uint16_t* yp, int R,
                         const int32_t* row_of_slot, const float* gate, int T, int d, uint16_t* dyp,
                         float* dgate) {
   // 8 to 16 row vectors of 16 bytes in flight a lane
   constexpr int U = K <= 2 ? 8 : (K <= 4 ? 4 : 2);
-  (void)launch_pdl(combine_bwd_kernel<K, U>, grid, kThreads, 0, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate);
+  (void)launch_pdl(combine_bwd_kernel<K, U>, grid, kThreads, 0, s, dout, yp, R, row_of_slot, gate, T, d, dyp,
+                   dgate);
+}
+
+// Zero the rows of a capacity-padded buffer [E*C][d] that hold no routed
+// row: rows [e*C + counts[e], (e+1)*C) of every expert.  Warp per row.
+__global__ void __launch_bounds__(kThreads)
+zero_pad_rows_kernel(const int32_t* __restrict__ counts, int E, int C, int d, uint16_t* __restrict__ buf) {
+  pdl_enter();
+  const long long r = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= (long long)E * C) return;
+  const int e = (int)(r / C), j = (int)(r - (long long)e * C);
+  if (j < __ldg(counts + e)) return;
+  uint16_t* p = buf + (size_t)r * d;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int v = lane; v < (d >> 3); v += 32) st_v4(p + (size_t)v * 8, z);
+}
+
+int launch_zero_pad_rows(const int32_t* counts, int E, int C, int d, uint16_t* buf, cudaStream_t s) {
+  const long long rows = (long long)E * C;
+  (void)launch_pdl(zero_pad_rows_kernel, (unsigned)((rows + kWarps - 1) / kWarps), kThreads, 0, s, counts, E,
+                   C, d, buf);
+  return 1;
+}
+
+void combine_bwd_switch(dim3 grid, cudaStream_t s, const moe_bf16_t* dout, const moe_bf16_t* yp, int R,
+                        const int32_t* row_of_slot, const float* gate, int T, int k, int d, moe_bf16_t* dyp,
+                        float* dgate) {
+  switch (k) {
+    case 1: launch_combine_bwd<1>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 2: launch_combine_bwd<2>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 3: launch_combine_bwd<3>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 4: launch_combine_bwd<4>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 5: launch_combine_bwd<5>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 6: launch_combine_bwd<6>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    case 7: launch_combine_bwd<7>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+    default: launch_combine_bwd<8>(grid, s, dout, yp, R, row_of_slot, gate, T, d, dyp, dgate); break;
+  }
 }
 
 }  // namespace
@@ -219,7 +255,8 @@ int moe_dispatch_rows(const moe_bf16_t* x, int T, int d, int k, const int32_t* r
   if (T == 0) return MOE_OK;
   MOE_CHECK_PTR(x); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(xp);
   dim3 grid((T + kWarps - 1) / kWarps);
-  (void)launch_pdl(dispatch_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, x, T, d, k, row_of_slot, xp);
+  (void)launch_pdl(dispatch_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, x, T, d, k, row_of_slot, T * k,
+                   xp);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -234,7 +271,8 @@ int moe_combine(const moe_bf16_t* yp, const int32_t* row_of_slot, const float* g
   // 8 vectors a lane: a 2048-wide row in one pass.  (A copy specialised on k
   // issues all k x 8 loads up front, needs 136 registers and runs 1.8x slower
   // at one block per SM; this one stays at 127 and two blocks.)
-  (void)launch_pdl(combine_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, yp, row_of_slot, gate, T, k, d, out);
+  (void)launch_pdl(combine_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, yp, T * k, row_of_slot, gate, T,
+                   k, d, out);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -248,17 +286,62 @@ int moe_combine_bwd(const moe_bf16_t* dout, const moe_bf16_t* yp, const int32_t*
   MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dgate);
   dim3 grid((T + kWarps - 1) / kWarps);
   const cudaStream_t s = (cudaStream_t)stream;
-  switch (k) {
-    case 1: launch_combine_bwd<1>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    case 2: launch_combine_bwd<2>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    case 3: launch_combine_bwd<3>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    case 4: launch_combine_bwd<4>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    case 5: launch_combine_bwd<5>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    case 6: launch_combine_bwd<6>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    case 7: launch_combine_bwd<7>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-    default: launch_combine_bwd<8>(grid, s, dout, yp, row_of_slot, gate, T, d, dyp, dgate); break;
-  }
+  combine_bwd_switch(grid, s, dout, yp, T * k, row_of_slot, gate, T, k, d, dyp, dgate);
   MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+// ------------------------------------------------- capacity-padded layer
+
+int moe_dispatch_rows_capacity(const moe_bf16_t* x, int T, int d, int k, const int32_t* row_of_slot,
+                               const int32_t* counts, int E, int C, moe_bf16_t* xp,
+                               moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && d % 8 == 0 && k >= 1 && k <= kMaxTopK && E >= 1 && C >= 1);
+  MOE_CHECK_ARG((long long)E * C <= 0x7fffffffLL && (long long)T * k <= 0x7fffffffLL);
+  MOE_CHECK_PTR(counts); MOE_CHECK_PTR(xp);
+  const cudaStream_t s = (cudaStream_t)stream;
+  int n = 0;
+  if (T > 0) {
+    MOE_CHECK_PTR(x); MOE_CHECK_PTR(row_of_slot);
+    (void)launch_pdl(dispatch_kernel<8>, dim3((T + kWarps - 1) / kWarps), kThreads, 0, s, x, T, d, k,
+                     row_of_slot, E * C, xp);
+    n = 1;
+  }
+  n += launch_zero_pad_rows(counts, E, C, d, xp, s);
+  MOE_LAUNCH_CHECK(n);
+  return MOE_OK;
+}
+
+int moe_combine_capacity(const moe_bf16_t* yp, int E, int C, const int32_t* row_of_slot, const float* gate,
+                         int T, int k, int d, moe_bf16_t* out, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && d % 8 == 0 && k >= 1 && k <= kMaxTopK && E >= 1 && C >= 1);
+  MOE_CHECK_ARG((long long)E * C <= 0x7fffffffLL);
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(out);
+  if (gate && !aligned16(gate)) return MOE_ERR_INVALID_ARG;
+  (void)launch_pdl(combine_kernel<8>, dim3((T + kWarps - 1) / kWarps), kThreads, 0, (cudaStream_t)stream, yp,
+                   E * C, row_of_slot, gate, T, k, d, out);
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+int moe_combine_bwd_capacity(const moe_bf16_t* dout, const moe_bf16_t* yp, int E, int C,
+                             const int32_t* row_of_slot, const int32_t* counts, const float* gate,
+                             int T, int k, int d, moe_bf16_t* dyp, float* dgate, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && d > 0 && d % 8 == 0 && k >= 1 && k <= kMaxTopK && E >= 1 && C >= 1);
+  MOE_CHECK_ARG((long long)E * C <= 0x7fffffffLL);
+  MOE_CHECK_PTR(counts); MOE_CHECK_PTR(dyp);
+  const cudaStream_t s = (cudaStream_t)stream;
+  int n = 0;
+  if (T > 0) {
+    MOE_CHECK_PTR(dout); MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(gate);
+    MOE_CHECK_PTR(dgate);
+    combine_bwd_switch(dim3((T + kWarps - 1) / kWarps), s, dout, yp, E * C, row_of_slot, gate, T, k, d, dyp,
+                       dgate);
+    n = 1;
+  }
+  n += launch_zero_pad_rows(counts, E, C, d, dyp, s);
+  MOE_LAUNCH_CHECK(n);
   return MOE_OK;
 }
 

@@ -181,6 +181,46 @@ __global__ void route_place_kernel(const int32_t* __restrict__ idx, int R, int E
   slot_of_row[row] = s;
 }
 
+// Capacity-padded map: expert e owns rows [e*C, (e+1)*C); its first C routed
+// slots in slot order keep their stable rank as the row inside that block,
+// later ones are dropped (row -1).  Rows of a block past the expert's kept
+// count hold no slot (slot_of_row -1).  One thread per index of the largest
+// of the three ranges (slots, padded rows, experts).
+__global__ void route_place_capacity_kernel(const int32_t* __restrict__ idx, int R, int E, int C,
+                                            const int32_t* __restrict__ chunk_base,
+                                            const int32_t* __restrict__ local_rank,
+                                            const int32_t* __restrict__ routed_counts,
+                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ routed,
+                                            int32_t* __restrict__ row_of_slot,
+                                            int32_t* __restrict__ slot_of_row) {
+  pdl_enter();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long EC = (long long)E * C;
+  if (i < R) {
+    const int s = (int)i;
+    const int e = __ldg(idx + s);
+    int row = -1;
+    if (e >= 0 && e < E) {
+      const int rank = __ldg(chunk_base + (size_t)(s / kRouteChunk) * E + e) + __ldg(local_rank + s);
+      if (rank < C) row = e * C + rank;
+    }
+    row_of_slot[s] = row;
+    if (row >= 0) slot_of_row[row] = s;
+  }
+  if (i < EC) {
+    const int e = (int)(i / C), j = (int)(i - (long long)e * C);
+    if (j >= __ldg(routed_counts + e)) slot_of_row[i] = -1;     // a zero row
+  }
+  if (i < E) {
+    const int n = __ldg(routed_counts + i);
+    counts[i] = min(n, C);
+    offsets[i] = (int)i * C;
+    if (routed) routed[i] = n;
+  }
+  if (i == 0) offsets[E] = (int)EC;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -219,6 +259,46 @@ extern "C" int moe_expert_offsets(const int32_t* topk_idx, int T, int k, int E, 
                                                              local_rank, offsets, row_of_slot,
                                                              slot_of_row);
   MOE_LAUNCH_CHECK(3);
+  return MOE_OK;
+}
+
+extern "C" int moe_expert_offsets_capacity(const int32_t* topk_idx, int T, int k, int E, int C,
+                                           int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                                           int32_t* slot_of_row, int32_t* routed, void* ws,
+                                           size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && k >= 1 && k <= kMaxTopK && E >= 1 && E <= kMaxExperts && k <= E && C >= 1);
+  MOE_CHECK_ARG((long long)T * k <= 0x7fffffffLL && (long long)E * C <= 0x7fffffffLL);
+  MOE_CHECK_PTR(counts); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(slot_of_row);
+  if (routed && !aligned16(routed)) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  const long long R = (long long)T * k;
+  if (R > 0) { MOE_CHECK_PTR(topk_idx); MOE_CHECK_PTR(row_of_slot); }
+  const CapacityScratch L = capacity_scratch(R, E);
+  if (ws_bytes < L.end) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* wsb = reinterpret_cast<char*>(ws);
+  int32_t* chunk_counts = reinterpret_cast<int32_t*>(wsb + L.route.chunk_counts);
+  int32_t* local_rank = reinterpret_cast<int32_t*>(wsb + L.route.local_rank);
+  int32_t* rcounts = reinterpret_cast<int32_t*>(wsb + L.routed_counts);
+  int32_t* roffsets = reinterpret_cast<int32_t*>(wsb + L.routed_offsets);
+  int* status = reinterpret_cast<int*>(ws);
+  const long long EC = (long long)E * C;
+  int launches = 0;
+  if (R > 0) {
+    const int nchunks = (int)((R + kRouteChunk - 1) / kRouteChunk);
+    (void)launch_pdl(route_count_kernel, nchunks, kRCThreads, sizeof(int32_t) * kRCWarps * E, s, topk_idx,
+                     (int)R, E, chunk_counts, local_rank, status);
+    (void)launch_pdl(route_scan_kernel, 1, 1024, 0, s, chunk_counts, nchunks, E, rcounts, roffsets);
+    launches = 2;
+  } else if (cudaMemsetAsync(rcounts, 0, sizeof(int32_t) * E, s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  long long n = R > EC ? R : EC;
+  if (n < E + 1) n = E + 1;
+  (void)launch_pdl(route_place_capacity_kernel, (unsigned)((n + 255) / 256), 256, 0, s, topk_idx, (int)R, E, C,
+                   chunk_counts, local_rank, rcounts, counts, offsets, routed, row_of_slot, slot_of_row);
+  MOE_LAUNCH_CHECK(launches + 1);
   return MOE_OK;
 }
 

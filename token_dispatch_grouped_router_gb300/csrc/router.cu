@@ -322,8 +322,8 @@ router_units_kernel(const int32_t* __restrict__ offsets, int E, int R, int4* __r
 __global__ void __launch_bounds__(256)
 router_dw_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ dz,
                          const int32_t* __restrict__ slot_of_row, const int4* __restrict__ units,
-                         const int* __restrict__ total, int d, int E, int k, float* __restrict__ part,
-                         float* __restrict__ pbias) {
+                         const int* __restrict__ total, int d, int E, int k, int R,
+                         float* __restrict__ part, float* __restrict__ pbias) {
   pdl_enter();
   __shared__ int s_t[kRouterChunk];
   __shared__ float s_g[kRouterChunk];
@@ -332,9 +332,12 @@ router_dw_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict
   const int4 un = units[u];
   const int e = un.x, r0 = un.y, rows = un.z;
   for (int i = threadIdx.x; i < rows; i += blockDim.x) {
-    const int t = __ldg(slot_of_row + r0 + i) / k;
+    // a slot outside [0, T*k) (a row that holds no slot) adds nothing
+    const int sl = __ldg(slot_of_row + r0 + i);
+    const bool ok = row_ok(sl, R);
+    const int t = ok ? sl / k : 0;
     s_t[i] = t;
-    s_g[i] = __ldg(dz + (size_t)t * E + e);
+    s_g[i] = ok ? __ldg(dz + (size_t)t * E + e) : 0.f;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -475,7 +478,7 @@ int moe_router_logits_bwd_topk(const moe_bf16_t* x, const float* W_r, const floa
   (void)launch_pdl(router_units_kernel, 1, 1024, 0, s, offsets, E, (int)R, units, estart, ecount, total);
   (void)launch_pdl(router_dw_partial_kernel, (unsigned)L.max_units, 256, 0, s,
                    reinterpret_cast<const uint16_t*>(x), d_logits, slot_of_row, units, total, d, E, k,
-                   part, pbias);
+                   (int)R, part, pbias);
   (void)launch_pdl(router_dw_reduce_kernel, dim3((d + 255) / 256, E), 256, 0, s, part, pbias, estart,
                    ecount, d, E, dW_r, db);
   (void)launch_pdl(router_dx_topk_kernel, (unsigned)((T + 7) / 8), 256, 0, s, d_logits, topk_idx, WT,

@@ -15,10 +15,17 @@ SwiGLU intermediates H1, H3, A left by the forward: it gathers the rows again
 from x and recomputes H1, H3, A from them, so that only x, the routing and Yp
 (for the gate gradient) have to live from the forward to the backward.
 
+With ``capacity_factor=f`` the layer is the capacity-padded alternative the
+device route map replaces: every expert gets C = ceil(f * T * k / E) rows of
+the expert-sorted buffers (its first C routed slots in token order, then zero
+rows), later slots are dropped, and the same grouped GEMMs run on all E * C
+rows (the ``_capacity`` route-map, dispatch and combine calls).
+
 Nothing is copied back to the host and nothing waits on the host.
 """
 from __future__ import annotations
 
+import math
 from typing import Dict, Optional
 
 import numpy as np
@@ -46,12 +53,17 @@ class MoELayer:
     """Buffers and call sequence of one MoE layer step on one GPU."""
 
     def __init__(self, T: int, d: int, E: int, k: int, h: int, learned: bool,
-                 device="cuda", with_backward: bool = True, recompute: bool = False):
+                 device="cuda", with_backward: bool = True, recompute: bool = False,
+                 capacity_factor: Optional[float] = None):
         self.T, self.d, self.E, self.k, self.h = T, d, E, k, h
-        self.R = T * k
         self.learned = learned
         self.with_backward = with_backward
         self.recompute = recompute
+        # capacity-padded layer: E * C rows in every expert-sorted buffer
+        self.C = int(math.ceil(capacity_factor * T * k / E)) if capacity_factor else None
+        if self.C is not None and T > 0:
+            self.C = max(self.C, 1)
+        self.R = T * k if self.C is None else E * self.C
         dev = torch.device(device)
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
         e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
@@ -69,8 +81,15 @@ class MoELayer:
         self.gate = e(T, k, dt=f32)
         self.counts = e(E, dt=i32)
         self.offsets = e(E + 1, dt=i32)
-        self.row_of_slot = e(R, dt=i32)
+        self.row_of_slot = e(T * k, dt=i32)
         self.slot_of_row = e(R, dt=i32)
+        if self.C is not None:
+            self.routed = e(E, dt=i32)          # rows routed before the capacity cut
+            if learned and with_backward:
+                # the router backward sums over every routed slot, dropped ones
+                # included: it reads the unpadded route map
+                self.u_counts = e(E, dt=i32); self.u_offsets = e(E + 1, dt=i32)
+                self.u_row_of_slot = e(T * k, dt=i32); self.u_slot_of_row = e(T * k, dt=i32)
         self.xp = e(R, d)
         self.h1 = e(R, h); self.h3 = e(R, h); self.a = e(R, h)
         self.yp = e(R, d)
@@ -127,26 +146,42 @@ class MoELayer:
             mark("router_gates")
             L.moe_router_gates(self.glogit, self.gate)
         mark("expert_offsets")
-        L.moe_expert_offsets(self.idx, self.E, self.counts, self.offsets, self.row_of_slot,
-                             self.slot_of_row, self.ws)
+        if self.C is not None:
+            L.moe_expert_offsets_capacity(self.idx, self.E, self.C, self.counts, self.offsets,
+                                          self.row_of_slot, self.slot_of_row, self.ws, self.routed)
+        else:
+            L.moe_expert_offsets(self.idx, self.E, self.counts, self.offsets, self.row_of_slot,
+                                 self.slot_of_row, self.ws)
+
+    def _combine(self, rows, gate, out) -> None:
+        if self.C is not None:
+            L.moe_combine_capacity(rows, self.E, self.C, self.row_of_slot, gate, self.k, out)
+        else:
+            L.moe_combine(rows, self.row_of_slot, gate, self.k, out)
 
     def forward(self, mark=None) -> torch.Tensor:
         mark = mark or _nomark
         self.route(mark)
         mark("dispatch")
-        L.moe_dispatch_rows(self.x, self.row_of_slot, self.k, self.xp)
+        if self.C is not None:
+            L.moe_dispatch_rows_capacity(self.x, self.row_of_slot, self.counts, self.k, self.C,
+                                         self.xp)
+        else:
+            L.moe_dispatch_rows(self.x, self.row_of_slot, self.k, self.xp)
         mark("gemm_up")
         L.moe_grouped_swiglu_fwd_up(self.xp, self.offsets, self.W1, self.W3, self.h1, self.h3,
                                     self.a, self.ws)
         mark("gemm_down")
         L.moe_grouped_swiglu_fwd_down(self.a, self.offsets, self.W2, self.yp, self.ws)
         mark("combine")
-        L.moe_combine(self.yp, self.row_of_slot, self.gate, self.k, self.out)
+        self._combine(self.yp, self.gate, self.out)
         return self.out
 
     # ----------------------------------------------------------- backward
     def backward(self, mark=None) -> None:
         mark = mark or _nomark
+        if self.recompute and self.C is not None:
+            raise ValueError("the recompute policy is not combined with capacity padding")
         if self.recompute:
             mark("dispatch_recompute")
             L.moe_dispatch_rows(self.x, self.row_of_slot, self.k, self.xp)
@@ -154,8 +189,12 @@ class MoELayer:
             L.moe_grouped_swiglu_fwd_up(self.xp, self.offsets, self.W1, self.W3, self.h1,
                                         self.h3, self.a, self.ws)
         mark("combine_bwd")
-        L.moe_combine_bwd(self.dY, self.yp, self.row_of_slot, self.gate, self.k,
-                          self.dyp, self.dgate)
+        if self.C is not None:
+            L.moe_combine_bwd_capacity(self.dY, self.yp, self.C, self.row_of_slot, self.counts,
+                                       self.gate, self.k, self.dyp, self.dgate)
+        else:
+            L.moe_combine_bwd(self.dY, self.yp, self.row_of_slot, self.gate, self.k,
+                              self.dyp, self.dgate)
         mark("gemm_dact")
         L.moe_grouped_swiglu_bwd_dact(self.offsets, self.W2, self.h1, self.h3, self.dyp,
                                       self.dh1, self.dh3, self.ws)
@@ -166,18 +205,26 @@ class MoELayer:
         L.moe_grouped_swiglu_bwd_wgrad(self.xp, self.offsets, self.a, self.dyp, self.dh1,
                                        self.dh3, self.dW1, self.dW3, self.dW2, self.ws)
         mark("unpermute")
-        L.moe_combine(self.dxp, self.row_of_slot, None, self.k, self.dX)
+        self._combine(self.dxp, None, self.dX)
         mark("router_bwd")
         L.moe_router_topk_bwd(self.gate, self.dgate, self.idx, self.E, self.dlogits)
         if self.learned:
+            offsets, slot_of_row = self.offsets, self.slot_of_row
+            if self.C is not None:
+                mark("expert_offsets_unpadded")
+                L.moe_expert_offsets(self.idx, self.E, self.u_counts, self.u_offsets,
+                                     self.u_row_of_slot, self.u_slot_of_row, self.ws)
+                offsets, slot_of_row = self.u_offsets, self.u_slot_of_row
             mark("router_logits_bwd")
-            L.moe_router_logits_bwd_topk(self.x, self.W_r, self.dlogits, self.idx, self.offsets,
-                                         self.slot_of_row, self.dX, self.dW_r, self.db, self.ws)
+            L.moe_router_logits_bwd_topk(self.x, self.W_r, self.dlogits, self.idx, offsets,
+                                         slot_of_row, self.dX, self.dW_r, self.db, self.ws)
 
     # ------------------------------------------------------------- MXFP8
     def enable_mxfp8(self) -> None:
         """Allocate the MXFP8 buffers: K-major E4M3 weight copies with their
         E8M0 scales, quantised expert rows and quantised activations."""
+        if self.C is not None:
+            raise ValueError("the MXFP8 path is not combined with capacity padding")
         E, d, h, R = self.E, self.d, self.h, self.R
         dev = self.x.device
         u = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)  # noqa: E731

@@ -38,6 +38,10 @@ SIGNATURES = {
                                         _Z, _P]),
     "moe_expert_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_offsets_capacity": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_dispatch_rows_capacity": (_I, [_P, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
+    "moe_combine_capacity": (_I, [_P, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_combine_bwd_capacity": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_rows": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
@@ -238,6 +242,52 @@ def moe_expert_offsets_noalloc(topk_idx, E: int, counts, offsets, row_of_slot, s
     _ok("moe_expert_offsets_noalloc", load().moe_expert_offsets_noalloc(
         _ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(row_of_slot),
         _ptr(slot_of_row), _ptr(status), _stream()))
+
+
+# ------------------------------------------------ capacity-padded layer
+
+def moe_expert_offsets_capacity(topk_idx, E: int, C: int, counts, offsets, row_of_slot,
+                                slot_of_row, ws, routed=None) -> None:
+    T, k = topk_idx.shape
+    _want(topk_idx, torch.int32, (T, k), "topk_idx"); _want(counts, torch.int32, (E,), "counts")
+    _want(offsets, torch.int32, (E + 1,), "offsets")
+    _want(row_of_slot, torch.int32, (T * k,), "row_of_slot")
+    _want(slot_of_row, torch.int32, (E * C,), "slot_of_row")
+    if routed is not None:
+        _want(routed, torch.int32, (E,), "routed")
+    _ok("moe_expert_offsets_capacity", load().moe_expert_offsets_capacity(
+        _ptr(topk_idx), T, k, E, C, _ptr(counts), _ptr(offsets), _ptr(row_of_slot),
+        _ptr(slot_of_row), _ptr(routed), _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_dispatch_rows_capacity(x, row_of_slot, counts, k: int, C: int, xp) -> None:
+    T, d = x.shape
+    E = counts.shape[0]
+    _want(x, torch.bfloat16, (T, d), "x"); _want(xp, torch.bfloat16, (E * C, d), "xp")
+    _want(row_of_slot, torch.int32, (T * k,), "row_of_slot"); _want(counts, torch.int32, (E,), "counts")
+    _ok("moe_dispatch_rows_capacity", load().moe_dispatch_rows_capacity(
+        _ptr(x), T, d, k, _ptr(row_of_slot), _ptr(counts), E, C, _ptr(xp), _stream()))
+
+
+def moe_combine_capacity(yp, E: int, C: int, row_of_slot, gate, k: int, out) -> None:
+    T, d = out.shape
+    _want(yp, torch.bfloat16, (E * C, d), "yp"); _want(out, torch.bfloat16, (T, d), "out")
+    _want(row_of_slot, torch.int32, (T * k,), "row_of_slot")
+    if gate is not None:
+        _want(gate, torch.float32, (T, k), "gate")
+    _ok("moe_combine_capacity", load().moe_combine_capacity(
+        _ptr(yp), E, C, _ptr(row_of_slot), _ptr(gate), T, k, d, _ptr(out), _stream()))
+
+
+def moe_combine_bwd_capacity(dout, yp, C: int, row_of_slot, counts, gate, k: int, dyp, dgate) -> None:
+    T, d = dout.shape
+    E = counts.shape[0]
+    _want(yp, torch.bfloat16, (E * C, d), "yp"); _want(dyp, torch.bfloat16, (E * C, d), "dyp")
+    _want(row_of_slot, torch.int32, (T * k,), "row_of_slot"); _want(counts, torch.int32, (E,), "counts")
+    _want(gate, torch.float32, (T, k), "gate"); _want(dgate, torch.float32, (T, k), "dgate")
+    _ok("moe_combine_bwd_capacity", load().moe_combine_bwd_capacity(
+        _ptr(dout), _ptr(yp), E, C, _ptr(row_of_slot), _ptr(counts), _ptr(gate), T, k, d,
+        _ptr(dyp), _ptr(dgate), _stream()))
 
 
 # ------------------------------------------------------- dispatch/combine
