@@ -406,21 +406,46 @@ int moe_dispatch_rows_mxfp8(const moe_bf16_t* x, int T, int d, int k,
                             const int32_t* row_of_slot, uint8_t* xq, uint8_t* xs,
                             moe_bf16_t* xp, moe_stream_t stream);
 
+/* Bytes of the scale atoms moe_mxfp8_weight_scale_atoms writes for E experts
+ * (0 unless d and h are multiples of 128). */
+size_t moe_mxfp8_weight_atom_bytes(int E, int d, int h);
+
+/* The weight scales in the order the block-scaled GEMM's tiles read them.
+ * The tensor cores take E8M0 scales from tensor memory, filled from 512-byte
+ * shared-memory atoms (32 rows of 16 bytes; byte 4j + q of row r is the scale
+ * of output column 32j + r of a 128-column group for the q-th 32-element block
+ * of a 128-deep k-block); the GEMM fetches whole atoms by TMA.  From the
+ * row-major tables of moe_mxfp8_quantize_weights (w1s/w3s [E][h][d/32], w2s
+ * [E][d][h/32]) this writes, per expert, column tile and k-block, two atoms:
+ * the up-projection's tiles are 96 rows of W1 followed by the same 96 rows of
+ * W3 (ceil(h/96) tiles, K = d), then the down-projection's 192 rows of W2
+ * (ceil(d/192) tiles, K = h); columns past the matrix hold 0.  Call it with
+ * the weight quantisation, once per optimizer step.  d, h multiples of 128;
+ * scale tables 4-byte aligned, atoms 16-byte aligned with
+ * moe_mxfp8_weight_atom_bytes(E, d, h) bytes.  Two launches. */
+int moe_mxfp8_weight_scale_atoms(const uint8_t* w1s, const uint8_t* w3s, const uint8_t* w2s,
+                                 int E, int d, int h, uint8_t* atoms, moe_stream_t stream);
+
 /* Forward of the grouped SwiGLU FFN with MXFP8 GEMM operands and fp32
  * accumulation (block-scaled tcgen05 MMA): h1 = Xq_e W1q[e], h3 = Xq_e W3q[e],
  * a = silu(h1) * h3 (bf16 h1, h3, a for the bf16 backward), a quantised along
  * h into aq[R][h] / as[R][h/32], yp = Aq_e W2q[e] (bf16).  a may be NULL:
  * then only its quantised form is written (a caller that keeps the saved
  * activation in MXFP8 and dequantises it for the backward).  Weights come from
- * moe_mxfp8_quantize_weights (w1q/w3q [E][h][d], w2q [E][d][h]).  d and h
- * must be multiples of 128 and E <= 768 (MOE_ERR_UNSUPPORTED otherwise: the
- * kernels keep an E-sized tile table beside 128 x 256 operand tiles in shared
- * memory). */
+ * moe_mxfp8_quantize_weights (w1q/w3q [E][h][d], w2q [E][d][h]) and their
+ * scales from moe_mxfp8_weight_scale_atoms (w_atoms); xs and as are row-major
+ * [R][K/32] tables, which the call lays out as atoms in the workspace
+ * ((ceil(R/128) + E) (d + h) * 4 bytes after the status word; every expert's
+ * rows start a fresh 128-row block there).  With at least 512 rows per expert
+ * on average the GEMMs run on 2-CTA clusters (256 x 192 tiles), otherwise on
+ * single CTAs (128 x 192).  d and h must be multiples of 128 and E <= 768
+ * (MOE_ERR_UNSUPPORTED otherwise: the kernels keep an E-sized tile table
+ * beside their operand stages in shared memory); ws needs
+ * moe_workspace_size(T, E, k, d, h) bytes (MOE_ERR_WORKSPACE). */
 int moe_grouped_swiglu_fwd_mxfp8(const uint8_t* xq, const uint8_t* xs,
                                  const int32_t* offsets, int R, int E, int d, int h,
-                                 const uint8_t* w1q, const uint8_t* w1s,
-                                 const uint8_t* w3q, const uint8_t* w3s,
-                                 const uint8_t* w2q, const uint8_t* w2s,
+                                 const uint8_t* w1q, const uint8_t* w3q, const uint8_t* w2q,
+                                 const uint8_t* w_atoms,
                                  moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a,
                                  uint8_t* aq, uint8_t* as, moe_bf16_t* yp,
                                  void* ws, size_t ws_bytes, moe_stream_t stream);

@@ -88,6 +88,47 @@ def test_quantize_weights_from_fp32_masters_bit_exact(E, K, N):
         assert np.array_equal(gq[e], qr.T), e
 
 
+def _atoms_of(scales, cols, K, second=None):
+    """Expected atom bytes of row-major scales [E][N][K/32] for column tiles of
+    `cols` (96: rows of `scales` then the same rows of `second`; 192: rows of
+    `scales`): per (expert, tile, 128-deep k-block) two 512-byte atoms, byte
+    (c % 32) * 16 + ((c % 128) // 32) * 4 + q of atom c // 128 = the scale of
+    tile column c for 32-block q of the k-block."""
+    E, N, _ = scales.shape
+    KB = K // 128
+    NT = -(-N // cols)
+    out = np.zeros((E, NT, KB, 2, 32, 4, 4), np.uint8)   # [..][atom][r][j][q]
+    for c in range(192):
+        for nt in range(NT):
+            if cols == 96:
+                tab, n = (scales, nt * 96 + c) if c < 96 else (second, nt * 96 + c - 96)
+            else:
+                tab, n = scales, nt * 192 + c
+            if n >= N:
+                continue
+            blk = tab[:, n, :].reshape(E, KB, 4)             # [e][kb][q]
+            out[:, nt, :, c // 128, c % 32, (c % 128) // 32, :] = blk
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("E,d,h", [(2, 128, 128), (3, 256, 384), (2, 512, 256)])
+def test_weight_scale_atoms_layout(E, d, h):
+    # the GEMM's atom order of the weight scales, byte for byte
+    rng = np.random.default_rng(E + d + h)
+    w1s = rng.integers(0, 255, (E, h, d // 32), dtype=np.uint8)
+    w3s = rng.integers(0, 255, (E, h, d // 32), dtype=np.uint8)
+    w2s = rng.integers(0, 255, (E, d, h // 32), dtype=np.uint8)
+    n = L.moe_mxfp8_weight_atom_bytes(E, d, h)
+    atoms = torch.full((n,), 7, dtype=torch.uint8, device=DEV)
+    L.moe_mxfp8_weight_scale_atoms(*(torch.from_numpy(a).to(DEV) for a in (w1s, w3s, w2s)), atoms)
+    up = _atoms_of(w1s, 96, d, second=w3s)
+    dn = _atoms_of(w2s, 192, h)
+    assert n == up.size + dn.size
+    got = u8(atoms)
+    assert np.array_equal(got[:up.size], up)
+    assert np.array_equal(got[up.size:], dn)
+
+
 @pytest.mark.parametrize("rows,K", [(1, 32), (37, 96), (513, 2048)])
 def test_dequantize_rows_bit_exact(rows, K):
     # codes and scales from the oracle's quantiser, including tiny and huge
@@ -141,6 +182,8 @@ def _mx_layer(w, inp):
     L.moe_mxfp8_quantize_weights(t["W1"], t["w1q"], t["w1s"])
     L.moe_mxfp8_quantize_weights(t["W3"], t["w3q"], t["w3s"])
     L.moe_mxfp8_quantize_weights(t["W2"], t["w2q"], t["w2s"])
+    t["w_atoms"] = u(L.moe_mxfp8_weight_atom_bytes(E, d, h))
+    L.moe_mxfp8_weight_scale_atoms(t["w1s"], t["w3s"], t["w2s"], t["w_atoms"])
     idx = torch.from_numpy(np.ascontiguousarray(inp["idx"])).to(dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
@@ -153,8 +196,8 @@ def _mx_layer(w, inp):
     t["h1"], t["h3"], t["a"], t["yp"] = b(R, h), b(R, h), b(R, h), b(R, d)
     t["aq"], t["as"] = u(R, h), u(R, h // 32)
     L.moe_reset_status(ws)
-    L.moe_grouped_swiglu_fwd_mxfp8(t["xq"], t["xs"], offs, t["w1q"], t["w1s"], t["w3q"], t["w3s"],
-                                   t["w2q"], t["w2s"], t["h1"], t["h3"], t["a"], t["aq"], t["as"],
+    L.moe_grouped_swiglu_fwd_mxfp8(t["xq"], t["xs"], offs, t["w1q"], t["w3q"], t["w2q"],
+                                   t["w_atoms"], t["h1"], t["h3"], t["a"], t["aq"], t["as"],
                                    t["yp"], ws)
     torch.cuda.synchronize()
     assert L.moe_get_status(ws) == 0
@@ -171,6 +214,11 @@ def _mx_layer(w, inp):
     (1500, 256, 2, 1, 384, ()),
     (2600, 512, 4, 2, 256, (1,)),
     (700, 128, 1, 1, 128, ()),
+    # CTA pairs whose last 256-row tile leaves the odd CTA without rows
+    (1100, 128, 1, 1, 128, ()),
+    # CTA pairs, experts whose rows start off a 128-row boundary, d not a
+    # multiple of the 192-column tile
+    (3100, 640, 3, 2, 384, ()),
 ])
 def test_grouped_forward_mxfp8_small(T, d, E, k, h, empty, record_property):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)

@@ -52,11 +52,15 @@ int moe_version(void) { return 100; }
 uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
 
 size_t moe_workspace_size(int T, int E, int k, int d, int h) {
-  (void)h;
   if (T < 0 || E <= 0 || k <= 0 || d <= 0) return 0;
   const size_t a = moe::workspace_bytes(T, E, k, d);
   const size_t b = moe::router_topk_scratch((long long)T * k, E, d).end;
-  return a > b ? a : b;
+  size_t r = a > b ? a : b;
+  if (h > 0 && d % 128 == 0 && h % 128 == 0) {       // the MXFP8 forward's scale atoms
+    const size_t c = moe::mx_scratch_end((long long)T * k, E, d, h);
+    r = r > c ? r : c;
+  }
+  return r;
 }
 
 int moe_reset_status(void* ws, moe_stream_t stream) {

@@ -22,14 +22,24 @@
 // fp32 accumulators (at TMEM columns 0 and 256) leave room for the scale
 // factors, so the epilogue of one tile overlaps the next tile's mainloop
 // (a 256-column tile would fit only one accumulator).
-// Scale factors: per stage 512-byte atoms, byte (r, 4j + k) = scale of row
-// (or column) 32j + r of the atom for the stage's k-th 32-element block, one
-// for A and two for B (columns 0-127 and 128-191), gathered by the producer
-// warp with zero-filling cp.async (row-major scales in HBM) and moved to
-// tensor memory with tcgen05.cp .32x128b.warpx4 (which replicates an atom
-// into the four lane quarters).  The MMA then reads row m's A scale at lane
-// m, column base + m/32, and column n's B scale at lane n%32 of the issuing
-// quarter, column base + n/32, byte = the MMA's scale-factor id (0..3).
+// Scale factors: the E8M0 scales come in 512-byte atoms, the layout in which
+// tcgen05.cp .32x128b.warpx4 moves them to tensor memory (see mx_common.cuh:
+// byte (r, 4j + q) of an atom is the scale of row or column 32j + r of a
+// 128-row block for the q-th 32-block of a 128-deep k-block).  The atoms are
+// kept in HBM in the order the tiles read them, so each stage's scales arrive
+// by TMA on the same barrier as its operands: one atom for the A rows, two for
+// the 192 B columns.  The MMA then reads row m's A scale at lane m, column
+// base + m/32, and column n's B scale at lane n%32 of the issuing quarter,
+// column base + n/32, byte = the MMA's scale-factor id (0..3).
+//
+// Two kernel forms.  Single CTA: 128 x 192 tiles, 4 stages.  CTA pairs
+// (2-CTA clusters, cta_group::2): 256 x 192 tiles, each CTA stages its own
+// 128 A rows, half of the B columns (UP8: the even CTA the 96 W1 columns, the
+// odd CTA the same 96 W3 columns) and the scale atoms its half of the MMA
+// reads (its own A atom, both B atoms); all of a stage's copies, of both
+// CTAs, complete on the even CTA's barrier, whose MMA lane also copies both
+// CTAs' atoms into their tensor memory (tcgen05.cp.cta_group::2).  Per MMA a
+// CTA then moves 7 KB through shared memory instead of 10 KB on one CTA.
 #include "gemm_common.cuh"
 #include "mx_common.cuh"
 
@@ -41,45 +51,49 @@ using namespace gemm;
 
 enum Mode8 : int { kUp8 = 0, kDown8 = 1 };
 
-constexpr int BM = 128, BN = 192, BK = 128, STAGES = 4;
-constexpr int A_STAGE = BM * BK;                // 16 KB of E4M3
-constexpr int B_STAGE = BN * BK;                // 24 KB
-constexpr int SF_STAGE = 1536;                  // A atom + two B atoms
-constexpr int kAccStride = 256;                 // accumulators at TMEM columns 0 and 256
-constexpr int kSfCol0 = 448;                    // stage s: A at +12s, B at +12s+4 (8 columns)
+constexpr int BN = 192, BK = 128;               // MMA N, k-block (fp8 bytes)
+constexpr int A_STAGE = 128 * BK;               // 16 KB: one CTA's 128 A rows
+constexpr int SF_STAGE = 3 * mx::kAtomBytes;    // A atom + two B atoms
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts8 = 768;               // shared-memory tile table bound
+
+// Per form: rows a tile covers, B rows a CTA stages, pipeline stages, and the
+// tensor-memory columns of the second accumulator and of stage s's scales
+// (A at sf_col(s), B at sf_col(s) + 4, 12 columns a stage).
+template <bool PAIR> struct Form;
+template <> struct Form<false> {
+  static constexpr int TM = 128, BROWS = 192, STAGES = 4, THREADS = kThreads;
+  __device__ static uint32_t acc_col(int acc) { return (uint32_t)acc * 256; }
+  __device__ static uint32_t sf_col(int s) { return 448 + 12 * s; }
+};
+template <> struct Form<true> {
+  static constexpr int TM = 256, BROWS = 96, STAGES = 6, THREADS = kThreads;
+  __device__ static uint32_t acc_col(int acc) { return (uint32_t)acc * 256; }
+  // the 64 columns after each 192-column accumulator hold five stages' scales
+  __device__ static uint32_t sf_col(int s) { return s < 5 ? 192 + 12 * s : 448 + 12 * (s - 5); }
+};
+template <bool PAIR> constexpr int b_stage() { return Form<PAIR>::BROWS * BK; }
+template <bool PAIR> constexpr int stage_bytes() { return A_STAGE + b_stage<PAIR>() + SF_STAGE; }
 
 struct Args8 {
   const int32_t* offsets;
   int E, R, d, h;
-  int n_tiles;
+  int n_tiles;                  // column tiles per expert
   int kb_total;                 // K / 128
-  int K;                        // reduction length of this GEMM
-  const uint8_t* sfa;           // activation scales [R][K/32]
-  const uint8_t* sfb0;          // weight scales [E][N][K/32] (UP8: W1)
-  const uint8_t* sfb1;          // UP8: W3 scales
   int N;                        // rows of one weight matrix (UP8: h, DOWN8: d)
   uint16_t* out0;               // UP8: h1 / DOWN8: yp
   uint16_t* out1;               // UP8: h3
   uint16_t* out2;               // UP8: a
   uint8_t* aq;                  // UP8: quantised a [R][h]
-  uint8_t* as;                  // UP8: scales of a [R][h/32]
+  uint8_t* as;                  // UP8: scales of a [R][h/32], row-major
   int* status;
 };
 
-using Shared = PipeShared<STAGES>;
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 4 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ void tmem_cp_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tmem_cp_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
@@ -88,6 +102,16 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
@@ -119,7 +143,8 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
                                           const CUtensorMap* o2) {
   const uint32_t tbase = tacc + ((uint32_t)(lane_q * 32) << 16);
   const int nrows = min(32, rt.rows - lane_q * 32);
-  const size_t r0 = (size_t)rt.row0 + (nrows > 0 ? lane_q * 32 : 0);
+  if (nrows <= 0) return;                         // warp-uniform: no rows of this quarter
+  const size_t r0 = (size_t)rt.row0 + lane_q * 32;
   const bool whole = nrows == 32;
   if constexpr (MODE == kUp8) {
     // columns 0..95: h1[:, n0..n0+95]; 96..191: h3[:, n0..n0+95]; three
@@ -185,160 +210,193 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
   }
 }
 
-template <int MODE>
+// One persistent kernel per mode and form.  Warp 0 loads operands and scale
+// atoms by TMA, warp 1 allocates tensor memory and one lane (of the even CTA,
+// on pairs) copies the atoms to tensor memory and issues the MMAs, warps 2-9
+// drain the other accumulator.
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSA,
+                     const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmO0,
                      const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
                      const Args8 args) {
+  using F = Form<PAIR>;
+  constexpr int S = F::STAGES, TM = F::TM;
+  constexpr int B_STAGE = b_stage<PAIR>();
+  using Shared = PipeShared<S>;
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = sA + STAGES * A_STAGE;
-  uint8_t* sSF = sB + STAGES * B_STAGE;                      // STAGES x 1 KB
-  uint8_t* sStage = sSF + STAGES * SF_STAGE;                 // kEpiWarps x kStageBytes
+  uint8_t* sB = sA + S * A_STAGE;
+  uint8_t* sSF = sB + S * B_STAGE;                           // S x 1.5 KB
+  uint8_t* sStage = sSF + S * SF_STAGE;                      // kEpiWarps x kStageBytes
   Shared* sh = reinterpret_cast<Shared*>(sStage + kEpiWarps * kStageBytes);
   int* s_off = reinterpret_cast<int*>(sh + 1);
   int* s_ts = s_off + (args.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;      // pair or CTA
+  const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   for (int i = threadIdx.x; i <= args.E; i += kThreads) s_off[i] = __ldg(args.offsets + i);
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1 + 32);     // TMA arrival + one cp.async arrival per lane
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
       mbar_init(smem_u32(&sh->empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) { mbar_init(smem_u32(&sh->tfull[s]), 1); mbar_init(smem_u32(&sh->tempty[s]), kEpiWarps); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sh->tfull[s]), 1);
+      mbar_init(smem_u32(&sh->tempty[s]), (PAIR ? 2 : 1) * kEpiWarps);
+    }
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
   if (warp == 0) {
-    const int n = build_row_tile_table(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
+    const int n = build_row_tile_table<TM>(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
     if (lane == 0) sh->total_tiles = n;
   }
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();      // both CTAs' barriers exist before either signals
+  else __syncthreads();
   const int total = sh->total_tiles;
-  if ((int)blockIdx.x >= total) return;
+  if (unit >= total) return;               // uniform across a pair; no TMEM taken
 
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) { tmem_alloc_pair(smem_u32(&sh->tmem_base), kTmemCols); tmem_relinquish_pair(); }
+    else { tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols); tmem_relinquish(); }
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmSA); prefetch_tmap(&tmSB);
     prefetch_tmap(&tmO0); prefetch_tmap(&tmO1); prefetch_tmap(&tmO2);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-  const int ksf = args.K / 32;                               // scale bytes per row
+  const int KB = args.kb_total;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const RowTile rt = decode_row_tile(t, args.E, args.R, s_off, s_ts);
+    for (int t = unit; t < total && ok; t += nunits) {
+      const RowTile rt = decode_row_tile<TM>(t, args.E, args.R, s_off, s_ts);
       const int n0 = rt.n_idx * (MODE == kUp8 ? BN / 2 : BN);
-      for (int kb = 0; kb < args.kb_total; ++kb) {
+      // this CTA's 128 rows start a 128-row block of the expert's scale rows
+      const int e_off = max(0, min(s_off[rt.e], args.R));
+      const int blk = mx::act_block0(e_off, rt.e) + (rt.row0 - e_off) / 128 + (int)rank;
+      const int wat = (rt.e * args.n_tiles + rt.n_idx) * KB;
+      for (int kb = 0; kb < KB; ++kb) {
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
-        const uint32_t fb = smem_u32(&sh->full[stage]);
-        const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
-          tma_load_2d(sa, &tmA, fb, kb * BK, rt.row0);
-          if constexpr (MODE == kUp8) {
-            // 96 rows of W1 then the same 96 rows of W3
-            tma_load_3d(sb, &tmB0, fb, kb * BK, n0, rt.e);
-            tma_load_3d(sb + 96 * BK, &tmB1, fb, kb * BK, n0, rt.e);
-          } else {
-            tma_load_3d(sb, &tmB0, fb, kb * BK, n0, rt.e);
-          }
-        }
-        // scale atoms: this lane gathers rows 32j + lane (j = 0..3) of A and
-        // columns 128hb + 32j + lane (< 192) of B
-        const uint32_t sfa_s = smem_u32(sSF + stage * SF_STAGE);
-        const uint32_t sfb_s = sfa_s + 512;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int row = rt.row0 + 32 * j + lane;
-          const bool v = row < args.R;
-          cp_async4(sfa_s + 16 * lane + 4 * j,
-                    args.sfa + (size_t)(v ? row : 0) * ksf + kb * 4, v);
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const int c = 128 * hb + 32 * j + lane;               // tile column
-            const uint8_t* tab = args.sfb0;
-            int n = n0 + c;
+          const uint32_t fb_local = smem_u32(&sh->full[stage]);
+          const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
+          const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
+          const int arow = rt.row0 + 128 * (int)rank;
+          if constexpr (PAIR) {
+            const uint32_t fb = mapa_shared(fb_local, 0);
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * (A_STAGE + B_STAGE + SF_STAGE));
+            tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
             if constexpr (MODE == kUp8) {
-              if (c >= BN / 2) { tab = args.sfb1; n -= BN / 2; }  // W3 half
+              // the even CTA stages the 96 W1 rows, the odd CTA the same W3 rows
+              tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, fb, kb * BK, n0, rt.e);
+            } else {
+              tma_load_3d_pair(sb, &tmB0, fb, kb * BK, n0 + 96 * (int)rank, rt.e);
             }
-            const bool bv = c < BN && n < args.N;
-            cp_async4(sfb_s + 512 * hb + 16 * lane + 4 * j,
-                      tab + ((size_t)rt.e * args.N + (bv ? n : 0)) * ksf + kb * 4, bv);
+            tma_load_2d_pair(ss, &tmSA, fb, 0, blk * KB + kb);
+            tma_load_2d_pair(ss + mx::kAtomBytes, &tmSB, fb, 0, (wat + kb) * 2);
+          } else {
+            mbar_arrive_expect_tx(fb_local, A_STAGE + B_STAGE + SF_STAGE);
+            tma_load_2d(sa, &tmA, fb_local, kb * BK, arow);
+            if constexpr (MODE == kUp8) {
+              // 96 rows of W1 then the same 96 rows of W3
+              tma_load_3d(sb, &tmB0, fb_local, kb * BK, n0, rt.e);
+              tma_load_3d(sb + 96 * BK, &tmB1, fb_local, kb * BK, n0, rt.e);
+            } else {
+              tma_load_3d(sb, &tmB0, fb_local, kb * BK, n0, rt.e);
+            }
+            tma_load_2d(ss, &tmSA, fb_local, 0, blk * KB + kb);
+            tma_load_2d(ss + mx::kAtomBytes, &tmSB, fb_local, 0, (wat + kb) * 2);
           }
         }
-        cp_async_arrive_noinc(fb);
         __syncwarp();
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
-    if (!ok && lane == 0) {
-      for (int s = 0; s < STAGES; ++s)
+    if (!ok && leader && lane == 0) {
+      // the (even CTA's) full barriers count every copy of the stage
+      for (int s = 0; s < S; ++s)
         if (issued & (1u << s)) drain_wait(smem_u32(&sh->full[s]), (last_par >> s) & 1u);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0;
-    bool ok = true, issued_any = false;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t dt = tmem + (uint32_t)(acc * kAccStride);
-      for (int kb = 0; kb < args.kb_total; ++kb) {
-        if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+    if (leader) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, issued_any = false;
+      for (int t = unit; t < total && ok; t += nunits) {
+        if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          // the scale bytes were written by cp.async (generic proxy); make them
-          // visible to the tensor core's async proxy before tcgen05.cp reads them
-          fence_proxy_async_smem();
-          const uint32_t sfa_t = tmem + kSfCol0 + 12 * stage, sfb_t = sfa_t + 4;
-          const uint32_t sf_s = smem_u32(sSF + stage * SF_STAGE);
-          tmem_cp_warpx4(sfa_t, sdesc_atom(sf_s));
-          tmem_cp_warpx4(sfb_t, sdesc_atom(sf_s + 512));          // B columns 0..127
-          tmem_cp_warpx4(sfb_t + 4, sdesc_atom(sf_s + 1024));     // B columns 128..191
-          const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
+        const uint32_t dt = tmem + F::acc_col(acc);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sfa_t = tmem + F::sf_col(stage), sfb_t = sfa_t + 4;
+            const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
+            const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
+            if constexpr (PAIR) {
+              tmem_cp_warpx4_pair(sfa_t, sdesc_atom(ss));
+              tmem_cp_warpx4_pair(sfb_t, sdesc_atom(ss + 512));        // B columns 0..127
+              tmem_cp_warpx4_pair(sfb_t + 4, sdesc_atom(ss + 1024));   // B columns 128..191
+            } else {
+              tmem_cp_warpx4(sfa_t, sdesc_atom(ss));
+              tmem_cp_warpx4(sfb_t, sdesc_atom(ss + 512));
+              tmem_cp_warpx4(sfb_t + 4, sdesc_atom(ss + 1024));
+            }
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-            mma_mxf8(dt, ad, bd, idesc_mxf8(BM, BN, kk), sfa_t, sfb_t, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 32; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+              const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+              if constexpr (PAIR) mma_mxf8_pair(dt, ad, bd, idesc_mxf8(256, BN, kk), sfa_t, sfb_t, accum);
+              else mma_mxf8(dt, ad, bd, idesc_mxf8(128, BN, kk), sfa_t, sfb_t, accum);
+            }
+            const uint32_t eb = smem_u32(&sh->empty[stage]);
+            if constexpr (PAIR) { mma_commit_pair(mapa_shared(eb, 0)); mma_commit_pair(mapa_shared(eb, 1)); }
+            else mma_commit(eb);
           }
-          mma_commit(smem_u32(&sh->empty[stage]));
+          issued_any = true;
+          __syncwarp();
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
-        issued_any = true;
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t tf = smem_u32(&sh->tfull[acc]);
+          if constexpr (PAIR) { mma_commit_pair(mapa_shared(tf, 0)); mma_commit_pair(mapa_shared(tf, 1)); }
+          else mma_commit(tf);
+        }
         __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(&sh->tfull[acc]));
-      __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (!ok && issued_any && lane == 0) {
+        if constexpr (PAIR) mma_commit_pair(mapa_shared(smem_u32(&sh->drain), 0));
+        else mma_commit(smem_u32(&sh->drain));
+        drain_wait(smem_u32(&sh->drain), 0);
+      }
     }
-    if (!ok && issued_any && lane == 0) {
-      mma_commit(smem_u32(&sh->drain));
-      drain_wait(smem_u32(&sh->drain), 0);
-    }
+    // the odd CTA's MMA warp only holds its half of the TMEM allocation
   } else {
     // ------------------------------------------------------------ epilogue
     const int lane_q = warp & 3;
@@ -346,44 +404,144 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     uint8_t* stg = sStage + (warp - 2) * kStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const RowTile rt = decode_row_tile(t, args.E, args.R, s_off, s_ts);
+    for (int t = unit; t < total; t += nunits) {
+      RowTile rt = decode_row_tile<TM>(t, args.E, args.R, s_off, s_ts);
       const int n0 = rt.n_idx * (MODE == kUp8 ? BN / 2 : BN);
+      if constexpr (PAIR) {                       // this CTA's 128 rows of the tile
+        rt.row0 += 128 * (int)rank;
+        rt.rows = max(0, min(128, rt.rows - 128 * (int)rank));
+      }
       if (!bounded_wait(smem_u32(&sh->tfull[acc]), acc_phase, &sh->abort_flag, args.status)) break;
       tc_fence_after();
-      epilogue8<MODE>(rt, n0, tmem + (uint32_t)(acc * kAccStride), lane_q, half, lane, stg, args,
-                      &tmO0, &tmO1, &tmO2);
+      epilogue8<MODE>(rt, n0, tmem + F::acc_col(acc), lane_q, half, lane, stg, args, &tmO0, &tmO1, &tmO2);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&sh->tempty[acc]), 0));
+        else mbar_arrive(smem_u32(&sh->tempty[acc]));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     stg_finish(lane);
   }
 
   tc_fence_before();
-  __syncthreads();
+  // no CTA leaves (or frees TMEM) while its peer may still signal it
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-constexpr size_t smem_bytes8(int E) {
-  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE + SF_STAGE) + (size_t)kEpiWarps * kStageBytes +
-         sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
+// Row-major activation scales [R][K/32] -> atoms (layout in mx_common.cuh).
+// Thread per (row, k-block): the row's four scale bytes of the k-block, one
+// 32-bit word of an atom.  Offsets are clamped to [0, R] as the GEMM reads
+// them, so every word lands inside the (ceil(R/128) + E) K/128 atoms.
+__global__ void __launch_bounds__(256)
+act_atoms_kernel(const uint8_t* __restrict__ s, const int32_t* __restrict__ offsets, int E, int R, int K,
+                 uint32_t* __restrict__ atoms) {
+  pdl_enter();
+  const int KB = K / 128;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)R * KB) return;
+  const int row = (int)(i / KB), kb = (int)(i - (long long)row * KB);
+  int lo = 0, hi = E;                 // the expert whose segment holds the row
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(offsets + mid) <= row) lo = mid; else hi = mid;
+  }
+  const int off = max(0, min(__ldg(offsets + lo), row));
+  const int srow = row - off + 128 * mx::act_block0(off, lo);
+  const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(s + (size_t)row * (K / 32)) + kb);
+  atoms[((size_t)(srow >> 7) * KB + kb) * 128 + (srow & 31) * 4 + ((srow >> 5) & 3)] = v;
 }
 
-template <int MODE>
-int launch8(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& o0,
-            const CUtensorMap& o1, const CUtensorMap& o2, const Args8& args, int grid, cudaStream_t s) {
-  auto kern = grouped_mxfp8_kernel<MODE>;
+// Row-major weight scales [E][N][K/32] -> the atoms of the GEMM's column
+// tiles (cols = 96: 96 rows of s0 then the same rows of s1; cols = 192: 192
+// rows of s0).  Thread per (tile k-block, column 0..255); columns 192-255 and
+// rows past N are zero.
+__global__ void __launch_bounds__(256)
+weight_atoms_kernel(const uint8_t* __restrict__ s0, const uint8_t* __restrict__ s1, int E, int N, int K,
+                    int cols, int NT, uint32_t* __restrict__ atoms) {
+  pdl_enter();
+  const int KB = K / 128;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)E * NT * KB * 256) return;
+  const int c = (int)(i & 255);
+  const long long p = i >> 8;                     // ((e * NT + nt) * KB + kb)
+  const int kb = (int)(p % KB), nt = (int)((p / KB) % NT), e = (int)(p / ((long long)KB * NT));
+  const uint8_t* tab = s0;
+  int n = nt * cols + c;
+  if (cols == mx::kUpCols && c >= mx::kUpCols) { tab = s1; n -= mx::kUpCols; }
+  uint32_t v = 0;
+  if (c < BN && n < N)
+    v = __ldg(reinterpret_cast<const uint32_t*>(tab + ((size_t)e * N + n) * (K / 32)) + kb);
+  atoms[(p * 2 + (c >> 7)) * 128 + (c & 31) * 4 + ((c >> 5) & 3)] = v;
+}
+
+// 2-D map over 512-byte atoms (32-bit elements, box = `count` whole atoms)
+inline bool map_atoms(CUtensorMap* m, const void* ptr, uint64_t n_atoms, uint32_t count) {
+  auto fn = encode_fn();
+  if (!fn || n_atoms == 0) return false;
+  cuuint64_t dims[2] = {128, n_atoms};
+  cuuint64_t strides[1] = {mx::kAtomBytes};
+  cuuint32_t box[2] = {128, count};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool PAIR>
+constexpr size_t smem_bytes8(int E) {
+  return 1024 + (size_t)Form<PAIR>::STAGES * stage_bytes<PAIR>() + (size_t)kEpiWarps * kStageBytes +
+         sizeof(PipeShared<Form<PAIR>::STAGES>) + 2 * (size_t)(E + 1) * 4;
+}
+static_assert(smem_bytes8<true>(kMaxExperts8) <= 227 * 1024, "pair MXFP8 kernel fits in shared memory");
+static_assert(smem_bytes8<false>(kMaxExperts8) <= 227 * 1024, "MXFP8 kernel fits in shared memory");
+
+struct Maps8 { CUtensorMap a, b0, b1, sa, sb, o0, o1, o2; };
+
+template <int MODE, bool PAIR>
+int launch8(const Maps8& m, const Args8& args, long long tiles_upper, cudaStream_t s) {
+  auto kern = grouped_mxfp8_kernel<MODE, PAIR>;
   static bool attr_done[64] = {false};
-  if (ensure_smem_attr(kern, smem_bytes8(kMaxExperts8), attr_done) != MOE_OK) return MOE_ERR_CUDA;
-  (void)launch_pdl(kern, grid, kThreads, smem_bytes8(args.E), s, a, b0, b1, o0, o1, o2, args);
+  if (ensure_smem_attr(kern, smem_bytes8<PAIR>(kMaxExperts8), attr_done) != MOE_OK) return MOE_ERR_CUDA;
+  const long long ub = tiles_upper > 0 ? tiles_upper : 1;
+  if constexpr (PAIR) {
+    const long long half_sms = sm_count() / 2;
+    const long long npairs = ub < half_sms ? ub : half_sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (npairs > 0 ? npairs : 1)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes8<PAIR>(args.E);
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, m.a, m.b0, m.b1, m.sa, m.sb, m.o0, m.o1, m.o2, args) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  } else {
+    const long long g = ub < sm_count() ? ub : sm_count();
+    (void)launch_pdl(kern, (unsigned)g, kThreads, smem_bytes8<PAIR>(args.E), s, m.a, m.b0, m.b1, m.sa, m.sb,
+                     m.o0, m.o1, m.o2, args);
+  }
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
+
+// CTA pairs once the experts average at least this many rows (the 256-row
+// tiles waste less than they gain); single CTAs below.
+constexpr long long kPairMinRows8 = 512;
 
 }  // namespace
 }  // namespace moe
@@ -391,46 +549,92 @@ int launch8(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, 
 using namespace moe;
 using namespace moe::gemm;
 
+extern "C" size_t moe_mxfp8_weight_atom_bytes(int E, int d, int h) {
+  if (E < 1 || d <= 0 || h <= 0 || d % 128 != 0 || h % 128 != 0) return 0;
+  return (size_t)mx::weight_atom_bytes(E, d, h);
+}
+
+extern "C" int moe_mxfp8_weight_scale_atoms(const uint8_t* w1s, const uint8_t* w3s, const uint8_t* w2s,
+                                            int E, int d, int h, uint8_t* atoms, moe_stream_t stream) {
+  if (E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || h % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  auto al4 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!al4(w1s) || !al4(w3s) || !al4(w2s)) return MOE_ERR_INVALID_ARG;
+  MOE_CHECK_PTR(atoms);
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* up = reinterpret_cast<uint32_t*>(atoms);
+  uint32_t* dn = up + mx::up_atom_count(E, d, h) * 128;
+  const int ntu = mx::up_tiles(h), ntd = mx::down_tiles(d);
+  const long long nu = (long long)E * ntu * (d / 128) * 256, nd = (long long)E * ntd * (h / 128) * 256;
+  (void)launch_pdl(weight_atoms_kernel, (unsigned)((nu + 255) / 256), 256, 0, s, w1s, w3s, E, h, d,
+                   mx::kUpCols, ntu, up);
+  (void)launch_pdl(weight_atoms_kernel, (unsigned)((nd + 255) / 256), 256, 0, s, w2s, w2s, E, d, h,
+                   mx::kDownCols, ntd, dn);
+  MOE_LAUNCH_CHECK(2);
+  return MOE_OK;
+}
+
 extern "C" int moe_grouped_swiglu_fwd_mxfp8(
     const uint8_t* xq, const uint8_t* xs, const int32_t* offsets, int R, int E, int d, int h,
-    const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w3q, const uint8_t* w3s,
-    const uint8_t* w2q, const uint8_t* w2s, moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a,
-    uint8_t* aq, uint8_t* as, moe_bf16_t* yp, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const uint8_t* w1q, const uint8_t* w3q, const uint8_t* w2q, const uint8_t* w_atoms,
+    moe_bf16_t* h1, moe_bf16_t* h3, moe_bf16_t* a, uint8_t* aq, uint8_t* as, moe_bf16_t* yp,
+    void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (R < 0 || E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
   if (d % 128 != 0 || h % 128 != 0 || E > kMaxExperts8) return MOE_ERR_UNSUPPORTED;
-  if (ws == nullptr || ws_bytes < kStatusBytes) return MOE_ERR_WORKSPACE;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
   if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const size_t need = mx_scratch_end(R, E, d, h);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (R == 0) return MOE_OK;
   MOE_CHECK_PTR(xq); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(w1q); MOE_CHECK_PTR(w3q);
-  MOE_CHECK_PTR(w2q); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(aq);
+  MOE_CHECK_PTR(w2q); MOE_CHECK_PTR(w_atoms); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3); MOE_CHECK_PTR(aq);
   MOE_CHECK_PTR(yp);
   if (a != nullptr && !aligned16(a)) return MOE_ERR_INVALID_ARG;      // a may be NULL
-  // scale tables are read 4 bytes at a time
+  // the row-major scale tables are read 4 bytes at a time
   auto al4 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
-  if (!al4(xs) || !al4(w1s) || !al4(w3s) || !al4(w2s) || as == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!al4(xs) || !al4(as)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint32_t* xatoms = reinterpret_cast<uint32_t*>(wsb + mx_scratch_x(R, E, d, h));
+  uint32_t* aatoms = reinterpret_cast<uint32_t*>(wsb + mx_scratch_a(R, E, d, h));
+  const long long nbx = mx::act_atom_blocks(R, E) * (d / 128), nba = mx::act_atom_blocks(R, E) * (h / 128);
+  const uint8_t* up_atoms = w_atoms;
+  const uint8_t* dn_atoms = w_atoms + mx::up_atom_count(E, d, h) * mx::kAtomBytes;
+  const long long n_up_atoms = mx::up_atom_count(E, d, h);
+  const long long n_dn_atoms = (long long)E * mx::down_tiles(d) * (h / 128) * 2;
+  const bool pair = (long long)R >= kPairMinRows8 * E;
+  const int TM = pair ? 256 : 128;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  CUtensorMap mx, mw1, mw3, ma, mw2;
-  if (!map2d(&mx, xq, d, R, BK, BM, U8, 1) || !map3d(&mw1, w1q, d, h, E, BK, BN / 2, U8, 1) ||
-      !map3d(&mw3, w3q, d, h, E, BK, BN / 2, U8, 1) || !map2d(&ma, aq, h, R, BK, BM, U8, 1) ||
-      !map3d(&mw2, w2q, h, d, E, BK, BN, U8, 1))
+  const uint32_t brows = pair ? 96 : 192;
+  Maps8 mu{}, md{};
+  if (!map2d(&mu.a, xq, d, R, BK, 128, U8, 1) || !map3d(&mu.b0, w1q, d, h, E, BK, 96, U8, 1) ||
+      !map3d(&mu.b1, w3q, d, h, E, BK, 96, U8, 1) || !map_atoms(&mu.sa, xatoms, nbx, 1) ||
+      !map_atoms(&mu.sb, up_atoms, n_up_atoms, 2) ||
+      !map2d(&md.a, aq, h, R, BK, 128, U8, 1) || !map3d(&md.b0, w2q, h, d, E, BK, brows, U8, 1) ||
+      !map_atoms(&md.sa, aatoms, nba, 1) || !map_atoms(&md.sb, dn_atoms, n_dn_atoms, 2))
     return MOE_ERR_CUDA;
+  md.b1 = md.b0;
+  if (!map2d_out(&mu.o0, h1, h, R, h) || !map2d_out(&mu.o1, h3, h, R, h) ||
+      !map2d_out(&mu.o2, a ? a : h1, h, R, h) || !map2d_out(&md.o0, yp, d, R, d))
+    return MOE_ERR_CUDA;
+  md.o1 = md.o0; md.o2 = md.o0;
   Args8 g{};
   g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
   // up-projection: K = d, 96 columns of W1 and of W3 per tile
-  g.K = d; g.kb_total = d / BK; g.n_tiles = (h + BN / 2 - 1) / (BN / 2); g.N = h;
-  g.sfa = xs; g.sfb0 = w1s; g.sfb1 = w3s;
+  g.kb_total = d / BK; g.n_tiles = mx::up_tiles(h); g.N = h;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.aq = aq; g.as = as;
-  CUtensorMap mo_h1, mo_h3, mo_a, mo_yp;
-  if (!map2d_out(&mo_h1, h1, h, R, h) || !map2d_out(&mo_h3, h3, h, R, h) ||
-      !map2d_out(&mo_a, a ? a : h1, h, R, h) || !map2d_out(&mo_yp, yp, d, R, d))
-    return MOE_ERR_CUDA;
-  int st = launch8<kUp8>(mx, mw1, mw3, mo_h1, mo_h3, mo_a, g, row_grid_upper(R, E, g.n_tiles), s);
+  const long long lx = (long long)R * (d / 128), la = (long long)R * (h / 128);
+  (void)launch_pdl(act_atoms_kernel, (unsigned)((lx + 255) / 256), 256, 0, s, xs, offsets, E, R, d, xatoms);
+  MOE_LAUNCH_CHECK(1);
+  int st = pair ? launch8<kUp8, true>(mu, g, row_tiles_upper(R, E, g.n_tiles, TM), s)
+                : launch8<kUp8, false>(mu, g, row_tiles_upper(R, E, g.n_tiles, TM), s);
   if (st != MOE_OK) return st;
   // down-projection: K = h
   Args8 g2 = g;
-  g2.K = h; g2.kb_total = h / BK; g2.n_tiles = (d + BN - 1) / BN; g2.N = d;
-  g2.sfa = as; g2.sfb0 = w2s; g2.sfb1 = w2s;
+  g2.kb_total = h / BK; g2.n_tiles = mx::down_tiles(d); g2.N = d;
   g2.out0 = yp; g2.out1 = nullptr; g2.out2 = nullptr; g2.aq = nullptr; g2.as = nullptr;
-  return launch8<kDown8>(ma, mw2, mw2, mo_yp, mo_yp, mo_yp, g2, row_grid_upper(R, E, g2.n_tiles), s);
+  (void)launch_pdl(act_atoms_kernel, (unsigned)((la + 255) / 256), 256, 0, s, as, offsets, E, R, h, aatoms);
+  MOE_LAUNCH_CHECK(1);
+  return pair ? launch8<kDown8, true>(md, g2, row_tiles_upper(R, E, g2.n_tiles, TM), s)
+              : launch8<kDown8, false>(md, g2, row_tiles_upper(R, E, g2.n_tiles, TM), s);
 }

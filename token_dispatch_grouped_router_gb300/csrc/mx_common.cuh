@@ -34,5 +34,42 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
+// ------------------------------------------------------------ scale atoms
+// The block-scaled MMA reads its E8M0 scale factors from tensor memory, where
+// tcgen05.cp (.32x128b.warpx4) puts them from 512-byte shared-memory atoms:
+// 32 rows of 16 bytes, byte 4j + q of row r holding the scale of row (or
+// output column) 32j + r of a 128-row block for the q-th 32-element block of
+// a 128-deep k-block.  The GEMMs fetch whole atoms by TMA, so the scales they
+// read are kept in HBM in atom order (GEMM scratch, rebuilt from the
+// row-major tables):
+//  * activations [R][K] in expert-sorted rows: every expert starts a fresh
+//    128-row block.  Row r of expert e is scale row
+//      s = r - offsets[e] + 128 * (ceil(offsets[e] / 128) + e)
+//    (segments cannot overlap: s < offsets[e+1] + 128 (e + 1) - 1 <= the next
+//    expert's first scale row), and (block s / 128, k-block kb) is atom
+//    (s / 128) * (K / 128) + kb; (ceil(R / 128) + E) * K / 128 atoms.
+//  * weights, per expert, column tile and k-block two atoms (tile columns
+//    0-127 and 128-191): the up-projection's tiles are 96 rows of W1 then the
+//    same 96 rows of W3 (ceil(h / 96) tiles, K = d), the down-projection's
+//    192 rows of W2 (ceil(d / 192) tiles, K = h); columns past N hold 0.
+constexpr int kAtomBytes = 512;
+constexpr int kUpCols = 96, kDownCols = 192;
+
+__host__ __device__ inline long long act_atom_blocks(long long R, int E) { return (R + 127) / 128 + E; }
+__host__ __device__ inline long long act_atom_bytes(long long R, int E, int K) {
+  return act_atom_blocks(R, E) * (K / 128) * kAtomBytes;
+}
+__host__ __device__ inline int up_tiles(int h) { return (h + kUpCols - 1) / kUpCols; }
+__host__ __device__ inline int down_tiles(int d) { return (d + kDownCols - 1) / kDownCols; }
+// weight atoms: the up-projection's, then the down-projection's
+__host__ __device__ inline long long up_atom_count(int E, int d, int h) {
+  return (long long)E * up_tiles(h) * (d / 128) * 2;
+}
+__host__ __device__ inline long long weight_atom_bytes(int E, int d, int h) {
+  return (up_atom_count(E, d, h) + (long long)E * down_tiles(d) * (h / 128) * 2) * kAtomBytes;
+}
+// first 128-row block of expert e's scale rows
+__host__ __device__ inline int act_block0(int offset_e, int e) { return (offset_e + 127) / 128 + e; }
+
 }  // namespace mx
 }  // namespace moe

@@ -231,6 +231,7 @@ class MoELayer:
         self.w1q, self.w1s = u(E, h, d), u(E, h, d // 32)
         self.w3q, self.w3s = u(E, h, d), u(E, h, d // 32)
         self.w2q, self.w2s = u(E, d, h), u(E, d, h // 32)
+        self.w_atoms = u(L.moe_mxfp8_weight_atom_bytes(E, d, h))
         self.xq, self.xs = u(R, d), u(R, d // 32)
         self.aq, self.as_ = u(R, h), u(R, h // 32)
 
@@ -241,6 +242,7 @@ class MoELayer:
         L.moe_mxfp8_quantize_weights(self.W1, self.w1q, self.w1s)
         L.moe_mxfp8_quantize_weights(self.W3, self.w3q, self.w3s)
         L.moe_mxfp8_quantize_weights(self.W2, self.w2q, self.w2s)
+        L.moe_mxfp8_weight_scale_atoms(self.w1s, self.w3s, self.w2s, self.w_atoms)
 
     def quantize_weights_from_masters(self, W1m: torch.Tensor, W3m: torch.Tensor,
                                       W2m: torch.Tensor) -> None:
@@ -249,6 +251,7 @@ class MoELayer:
         L.moe_mxfp8_quantize_weights_f32(W1m, self.w1q, self.w1s)
         L.moe_mxfp8_quantize_weights_f32(W3m, self.w3q, self.w3s)
         L.moe_mxfp8_quantize_weights_f32(W2m, self.w2q, self.w2s)
+        L.moe_mxfp8_weight_scale_atoms(self.w1s, self.w3s, self.w2s, self.w_atoms)
 
     def forward_mxfp8(self, mark=None, saved: str = "bf16") -> torch.Tensor:
         """Forward with MXFP8 GEMM operands.  saved="bf16": h1, h3, a and xp
@@ -264,8 +267,8 @@ class MoELayer:
         L.moe_dispatch_rows_mxfp8(self.x, self.row_of_slot, self.k, self.xq, self.xs,
                                   self.xp if keep_bf16 else None)
         mark("gemm_fwd_mxfp8")
-        L.moe_grouped_swiglu_fwd_mxfp8(self.xq, self.xs, self.offsets, self.w1q, self.w1s,
-                                       self.w3q, self.w3s, self.w2q, self.w2s, self.h1, self.h3,
+        L.moe_grouped_swiglu_fwd_mxfp8(self.xq, self.xs, self.offsets, self.w1q, self.w3q,
+                                       self.w2q, self.w_atoms, self.h1, self.h3,
                                        self.a if keep_bf16 else None, self.aq, self.as_, self.yp,
                                        self.ws)
         mark("combine")

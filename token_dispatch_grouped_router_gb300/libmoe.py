@@ -54,8 +54,10 @@ SIGNATURES = {
     "moe_mxfp8_quantize_weights_f32": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_mxfp8_dequantize_rows": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_dispatch_rows_mxfp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_mxfp8_weight_atom_bytes": (_Z, [_I, _I, _I]),
+    "moe_mxfp8_weight_scale_atoms": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
-                                          _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+                                          _P, _P, _P, _P, _P, _Z, _P]),
     "moe_grouped_swiglu_fwd_up": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_grouped_swiglu_fwd_down": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_grouped_swiglu_bwd_dact": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
@@ -447,22 +449,37 @@ def moe_dispatch_rows_mxfp8(x, row_of_slot, k: int, xq, xs, xp=None) -> None:
         _ptr(x), T, d, k, _ptr(row_of_slot), _ptr(xq), _ptr(xs), _ptr(xp), _stream()))
 
 
-def moe_grouped_swiglu_fwd_mxfp8(xq, xs, offsets, w1q, w1s, w3q, w3s, w2q, w2s,
+def moe_mxfp8_weight_atom_bytes(E: int, d: int, h: int) -> int:
+    return int(load().moe_mxfp8_weight_atom_bytes(E, d, h))
+
+
+def moe_mxfp8_weight_scale_atoms(w1s, w3s, w2s, atoms) -> None:
+    """The row-major weight scales in the atom order of the block-scaled GEMM's
+    tiles (see include/libmoe.h)."""
+    E, h, kd = w1s.shape
+    d = kd * 32
+    _want(w1s, torch.uint8, (E, h, d // 32), "w1s"); _want(w3s, torch.uint8, (E, h, d // 32), "w3s")
+    _want(w2s, torch.uint8, (E, d, h // 32), "w2s")
+    _want(atoms, torch.uint8, (moe_mxfp8_weight_atom_bytes(E, d, h),), "atoms")
+    _ok("moe_mxfp8_weight_scale_atoms", load().moe_mxfp8_weight_scale_atoms(
+        _ptr(w1s), _ptr(w3s), _ptr(w2s), E, d, h, _ptr(atoms), _stream()))
+
+
+def moe_grouped_swiglu_fwd_mxfp8(xq, xs, offsets, w1q, w3q, w2q, w_atoms,
                                  h1, h3, a, aq, as_, yp, ws) -> None:
     R, d = xq.shape
     E, h, _ = w1q.shape
     _want(xs, torch.uint8, (R, d // 32), "xs")
     for n, t in (("w1q", w1q), ("w3q", w3q)):
         _want(t, torch.uint8, (E, h, d), n)
-    for n, t in (("w1s", w1s), ("w3s", w3s)):
-        _want(t, torch.uint8, (E, h, d // 32), n)
-    _want(w2q, torch.uint8, (E, d, h), "w2q"); _want(w2s, torch.uint8, (E, d, h // 32), "w2s")
+    _want(w2q, torch.uint8, (E, d, h), "w2q")
+    _want(w_atoms, torch.uint8, (moe_mxfp8_weight_atom_bytes(E, d, h),), "w_atoms")
     for n, t in (("h1", h1), ("h3", h3), ("a", a)):
         if t is not None or n != "a":             # a may be None: quantised a only
             _want(t, torch.bfloat16, (R, h), n)
     _want(aq, torch.uint8, (R, h), "aq"); _want(as_, torch.uint8, (R, h // 32), "as")
     _want(yp, torch.bfloat16, (R, d), "yp")
     _ok("moe_grouped_swiglu_fwd_mxfp8", load().moe_grouped_swiglu_fwd_mxfp8(
-        _ptr(xq), _ptr(xs), _ptr(offsets), R, E, d, h, _ptr(w1q), _ptr(w1s), _ptr(w3q),
-        _ptr(w3s), _ptr(w2q), _ptr(w2s), _ptr(h1), _ptr(h3), _ptr(a), _ptr(aq), _ptr(as_),
-        _ptr(yp), _ptr(ws), _wsb(ws), _stream()))
+        _ptr(xq), _ptr(xs), _ptr(offsets), R, E, d, h, _ptr(w1q), _ptr(w3q), _ptr(w2q),
+        _ptr(w_atoms), _ptr(h1), _ptr(h3), _ptr(a), _ptr(aq), _ptr(as_), _ptr(yp),
+        _ptr(ws), _wsb(ws), _stream()))
