@@ -56,18 +56,19 @@ constexpr int A_STAGE = 128 * BK;               // 16 KB: one CTA's 128 A rows
 constexpr int SF_STAGE = 3 * mx::kAtomBytes;    // A atom + two B atoms
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts8 = 768;               // shared-memory tile table bound
+constexpr int kThreads8 = kThreads + 32;        // + the scale-copy warp
 
 // Per form: rows a tile covers, B rows a CTA stages, pipeline stages, and the
 // tensor-memory columns of the second accumulator and of stage s's scales
 // (A at sf_col(s), B at sf_col(s) + 4, 12 columns a stage).
 template <bool PAIR> struct Form;
 template <> struct Form<false> {
-  static constexpr int TM = 128, BROWS = 192, STAGES = 4, THREADS = kThreads;
+  static constexpr int TM = 128, BROWS = 192, STAGES = 4;
   __device__ static uint32_t acc_col(int acc) { return (uint32_t)acc * 256; }
   __device__ static uint32_t sf_col(int s) { return 448 + 12 * s; }
 };
 template <> struct Form<true> {
-  static constexpr int TM = 256, BROWS = 96, STAGES = 6, THREADS = kThreads;
+  static constexpr int TM = 256, BROWS = 96, STAGES = 6;
   __device__ static uint32_t acc_col(int acc) { return (uint32_t)acc * 256; }
   // the 64 columns after each 192-column accumulator hold five stages' scales
   __device__ static uint32_t sf_col(int s) { return s < 5 ? 192 + 12 * s : 448 + 12 * (s - 5); }
@@ -215,7 +216,7 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
 // on pairs) copies the atoms to tensor memory and issues the MMAs, warps 2-9
 // drain the other accumulator.
 template <int MODE, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads8, 1)
 grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                      const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSA,
                      const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmO0,
@@ -233,7 +234,8 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   uint8_t* sSF = sB + S * B_STAGE;                           // S x 1.5 KB
   uint8_t* sStage = sSF + S * SF_STAGE;                      // kEpiWarps x kStageBytes
   Shared* sh = reinterpret_cast<Shared*>(sStage + kEpiWarps * kStageBytes);
-  int* s_off = reinterpret_cast<int*>(sh + 1);
+  uint64_t* sfull = reinterpret_cast<uint64_t*>(sh + 1);      // [S] scales in TMEM, [S] copy drain
+  int* s_off = reinterpret_cast<int*>(sfull + S + 1);
   int* s_ts = s_off + (args.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -241,13 +243,15 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;      // pair or CTA
   const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
-  for (int i = threadIdx.x; i <= args.E; i += kThreads) s_off[i] = __ldg(args.offsets + i);
+  for (int i = threadIdx.x; i <= args.E; i += kThreads8) s_off[i] = __ldg(args.offsets + i);
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&sh->full[s]), 1);
       mbar_init(smem_u32(&sh->empty[s]), 1);
+      mbar_init(smem_u32(&sfull[s]), 1);
     }
+    mbar_init(smem_u32(&sfull[S]), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sh->tfull[s]), 1);
       mbar_init(smem_u32(&sh->tempty[s]), (PAIR ? 2 : 1) * kEpiWarps);
@@ -350,21 +354,13 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         tc_fence_after();
         const uint32_t dt = tmem + F::acc_col(acc);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+          // the stage's scales are in tensor memory (and so its operands have landed)
+          if (!bounded_wait(smem_u32(&sfull[stage]), phase, &sh->abort_flag, args.status) ||
+              !bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
             const uint32_t sfa_t = tmem + F::sf_col(stage), sfb_t = sfa_t + 4;
-            const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
             const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
-            if constexpr (PAIR) {
-              tmem_cp_warpx4_pair(sfa_t, sdesc_atom(ss));
-              tmem_cp_warpx4_pair(sfb_t, sdesc_atom(ss + 512));        // B columns 0..127
-              tmem_cp_warpx4_pair(sfb_t + 4, sdesc_atom(ss + 1024));   // B columns 128..191
-            } else {
-              tmem_cp_warpx4(sfa_t, sdesc_atom(ss));
-              tmem_cp_warpx4(sfb_t, sdesc_atom(ss + 512));
-              tmem_cp_warpx4(sfb_t + 4, sdesc_atom(ss + 1024));
-            }
 #pragma unroll
             for (int kk = 0; kk < BK / 32; ++kk) {
               const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
@@ -397,7 +393,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       }
     }
     // the odd CTA's MMA warp only holds its half of the TMEM allocation
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int lane_q = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -423,6 +419,49 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     stg_finish(lane);
+  } else if (leader) {
+    // ------------------------------------------------ scale copies (even CTA)
+    // A stage's atoms go to tensor memory from this warp, off the MMA lane:
+    // tcgen05.cp of both CTAs' atoms (the pair form) once the stage's copies
+    // have landed, then a commit to sfull[stage] that the MMA lane waits on.
+    // The stage's scale columns are rewritten only after the producer
+    // refilled the stage, i.e. after the MMAs that read them completed.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool issued = false;
+    for (int t = unit; t < total; t += nunits) {
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sfa_t = tmem + F::sf_col(stage), sfb_t = sfa_t + 4;
+          const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
+          const uint32_t sb = smem_u32(&sfull[stage]);
+          if constexpr (PAIR) {
+            tmem_cp_warpx4_pair(sfa_t, sdesc_atom(ss));
+            tmem_cp_warpx4_pair(sfb_t, sdesc_atom(ss + 512));        // B columns 0..127
+            tmem_cp_warpx4_pair(sfb_t + 4, sdesc_atom(ss + 1024));   // B columns 128..191
+            mma_commit_pair(mapa_shared(sb, 0));
+          } else {
+            tmem_cp_warpx4(sfa_t, sdesc_atom(ss));
+            tmem_cp_warpx4(sfb_t, sdesc_atom(ss + 512));
+            tmem_cp_warpx4(sfb_t + 4, sdesc_atom(ss + 1024));
+            mma_commit(sb);
+          }
+        }
+        issued = true;
+        __syncwarp();
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    if (issued && lane == 0) {            // every copy done before TMEM is freed
+      if constexpr (PAIR) mma_commit_pair(mapa_shared(smem_u32(&sfull[S]), 0));
+      else mma_commit(smem_u32(&sfull[S]));
+      drain_wait(smem_u32(&sfull[S]), 0);
+    }
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -498,7 +537,7 @@ inline bool map_atoms(CUtensorMap* m, const void* ptr, uint64_t n_atoms, uint32_
 template <bool PAIR>
 constexpr size_t smem_bytes8(int E) {
   return 1024 + (size_t)Form<PAIR>::STAGES * stage_bytes<PAIR>() + (size_t)kEpiWarps * kStageBytes +
-         sizeof(PipeShared<Form<PAIR>::STAGES>) + 2 * (size_t)(E + 1) * 4;
+         sizeof(PipeShared<Form<PAIR>::STAGES>) + 8 * (Form<PAIR>::STAGES + 1) + 2 * (size_t)(E + 1) * 4;
 }
 static_assert(smem_bytes8<true>(kMaxExperts8) <= 227 * 1024, "pair MXFP8 kernel fits in shared memory");
 static_assert(smem_bytes8<false>(kMaxExperts8) <= 227 * 1024, "MXFP8 kernel fits in shared memory");
@@ -516,7 +555,7 @@ int launch8(const Maps8& m, const Args8& args, long long tiles_upper, cudaStream
     const long long npairs = ub < half_sms ? ub : half_sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * (npairs > 0 ? npairs : 1)));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreads8);
     cfg.dynamicSmemBytes = smem_bytes8<PAIR>(args.E);
     cfg.stream = s;
     cudaLaunchAttribute at[2];
@@ -532,7 +571,7 @@ int launch8(const Maps8& m, const Args8& args, long long tiles_upper, cudaStream
     }
   } else {
     const long long g = ub < sm_count() ? ub : sm_count();
-    (void)launch_pdl(kern, (unsigned)g, kThreads, smem_bytes8<PAIR>(args.E), s, m.a, m.b0, m.b1, m.sa, m.sb,
+    (void)launch_pdl(kern, (unsigned)g, kThreads8, smem_bytes8<PAIR>(args.E), s, m.a, m.b0, m.b1, m.sa, m.sb,
                      m.o0, m.o1, m.o2, args);
   }
   MOE_LAUNCH_CHECK(1);
