@@ -151,3 +151,27 @@ def expert_ffn_forward_mxfp8(Xp, offsets, W1, W3, W2) -> Dict[str, np.ndarray]:
         A[lo:hi] = silu(H1[lo:hi]) * H3[lo:hi]
         Yp[lo:hi] = qdq(A[lo:hi], axis=1) @ w2
     return {"H1": H1, "H3": H3, "A": A, "Yp": Yp}
+
+
+def expert_dgrad_dx_mxfp8(dH1, dH3, offsets, W1, W3) -> np.ndarray:
+    """Dgrad of the expert rows with MXFP8 GEMM operands, fp64 arithmetic
+    otherwise: dXp_e = Q(dH1_e) Q(W1[e])^T + Q(dH3_e) Q(W3[e])^T.
+
+    The reduction runs over h, so every operand is quantised along h: the
+    rows of dH1 / dH3 [R, h] and the rows of W1[e] / W3[e] [d, h] (a different
+    quantisation of the weights than the forward's, which runs along d).
+    The same page quantises the Dgrad GEMM with the forward ones (OLMo-core 3
+    tutorial, section "一个低精度格式，同时压三个地方").
+    """
+    off = np.asarray(offsets, np.int64)
+    E = off.size - 1
+    q1 = qdq(dH1, axis=1)
+    q3 = qdq(dH3, axis=1)
+    d = np.asarray(W1).shape[1]
+    dXp = np.zeros((q1.shape[0], d))
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        dXp[lo:hi] = q1[lo:hi] @ qdq(W1[e], axis=1).T + q3[lo:hi] @ qdq(W3[e], axis=1).T
+    return dXp

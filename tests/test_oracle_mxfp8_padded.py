@@ -250,3 +250,59 @@ def test_capacity_route_map_by_hand_and_against_the_kept_mask():
         blk = sor[e * C:(e + 1) * C]
         assert np.all(blk[:c[e]] >= 0) and np.all(blk[c[e]:] == -1)
         assert np.all(np.diff(blk[:c[e]]) > 0)   # in slot order
+
+
+def test_mxfp8_dgrad_exact_on_representable_operands_and_at_format_precision():
+    # operands whose 32-blocks along h already lie on the E4M3 grid (block
+    # maximum exactly 448 * 2^s) pass through the quantisation unchanged, so
+    # the MXFP8 dgrad equals the exact expert dgrad; on Gaussian data its
+    # error is set by E4M3's 3 mantissa bits (a few percent)
+    rng = np.random.default_rng(15)
+    T, d, E, k, h = 24, 64, 3, 2, 64
+
+    def on_grid(shape):
+        codes = rng.integers(0, 0x7E, shape + (h // 32, 32))
+        codes[..., 0] = 0x7E
+        sgn = np.where(rng.random(codes.shape) < 0.5, -1.0, 1.0)
+        sc = np.exp2(rng.integers(-12, -4, shape + (h // 32, 1)).astype(float))
+        return (sgn * mx.e4m3_decode(codes) * sc).reshape(shape + (h,))
+
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    _, off, _, _ = ol.route_map(idx, E)
+    dH1, dH3 = on_grid((T * k,)), on_grid((T * k,))
+    W1 = np.stack([on_grid((d,)) for _ in range(E)]).transpose(0, 1, 2)    # [E, d, h]
+    W3 = np.stack([on_grid((d,)) for _ in range(E)])
+    exact = np.zeros((T * k, d))
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        exact[lo:hi] = dH1[lo:hi] @ W1[e].T + dH3[lo:hi] @ W3[e].T
+    got = mx.expert_dgrad_dx_mxfp8(dH1, dH3, off, W1, W3)
+    np.testing.assert_allclose(got, exact, rtol=1e-12, atol=1e-12)
+    # Gaussian operands: a few percent off the exact product, never zero
+    dH1, dH3 = rng.standard_normal((T * k, h)), rng.standard_normal((T * k, h))
+    W1, W3 = rng.standard_normal((E, d, h)), rng.standard_normal((E, d, h))
+    exact = np.zeros((T * k, d))
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        exact[lo:hi] = dH1[lo:hi] @ W1[e].T + dH3[lo:hi] @ W3[e].T
+    got = mx.expert_dgrad_dx_mxfp8(dH1, dH3, off, W1, W3)
+    rel = np.linalg.norm(got - exact) / np.linalg.norm(exact)
+    assert 0.015 < rel < 0.06
+    # quantised along h: with weight rows whose magnitudes vary along d, every
+    # output column stays at the format's precision, while quantising the
+    # weights along d (the forward's axis) crushes the small rows of a block
+    sc = np.exp2(rng.integers(-10, 11, (E, d, 1)).astype(float))   # one scale per output column
+    W1, W3 = W1 * sc, W3 * sc
+    exact = np.zeros((T * k, d)); wrong = np.zeros((T * k, d))
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        exact[lo:hi] = dH1[lo:hi] @ W1[e].T + dH3[lo:hi] @ W3[e].T
+        wrong[lo:hi] = (mx.qdq(dH1[lo:hi], axis=1) @ mx.qdq(W1[e], axis=0).T
+                        + mx.qdq(dH3[lo:hi], axis=1) @ mx.qdq(W3[e], axis=0).T)
+    got = mx.expert_dgrad_dx_mxfp8(dH1, dH3, off, W1, W3)
+    def col_err(v):       # worst relative error of one expert's output column
+        return max((np.linalg.norm(v[off[e]:off[e + 1]] - exact[off[e]:off[e + 1]], axis=0)
+                    / np.linalg.norm(exact[off[e]:off[e + 1]], axis=0)).max()
+                   for e in range(E) if off[e + 1] > off[e])
+    assert col_err(got) < 0.1
+    assert col_err(wrong) > 0.3
