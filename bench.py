@@ -430,9 +430,13 @@ def run_ours(args):
                           step=lambda mark=None: layer.step_mxfp8(mark, requantize=False,
                                                                   saved="mxfp8"))
         mxs["activation_bytes"] = layer.activation_bytes()
+        # the dgrad GEMM in MXFP8 as well (weights cached, dh1/dh3 quantised in the step)
+        mxd = timed_layer(layer, args.steps, args.warmup,
+                          step=lambda mark=None: layer.step_mxfp8(mark, requantize=False,
+                                                                  dgrad="mxfp8"))
         del layer
         torch.cuda.empty_cache()
-        mx_res = (w3, bf, mx, mxc, mxs)
+        mx_res = (w3, bf, mx, mxc, mxs, mxd)
 
     if rank != 0:
         if dist:
@@ -535,7 +539,7 @@ def run_ours(args):
                                "experts empty, the hottest holds a quarter of the routed rows); "
                                "the step includes the fp32 router GEMM and its backward"}
     if mx_res is not None:
-        w3, bf, mx, mxc, mxs = mx_res
+        w3, bf, mx, mxc, mxs, mxd = mx_res
         fl, _ = work_per_launch(w3)
         fwd_flops = fl["gemm_up"] + fl["gemm_down"]
         bf_fwd = bf["kernels_ms"]["gemm_up"] + bf["kernels_ms"]["gemm_down"]
@@ -556,6 +560,15 @@ def run_ours(args):
                 "activation_bytes_kept": {k: mxs["activation_bytes"][k] for k in ("saved", "mxfp8_saved")},
                 "note": "Xp and A kept between forward and backward as E4M3 codes + E8M0 scales "
                         "(no bf16 copy written in the forward), dequantised to bf16 before the backward"},
+            "mxfp8_fwd_and_dgrad_cached_weights": {
+                "value": world * w3.T / (mxd["ms_per_step"] / 1e3), "ms_per_step": mxd["ms_per_step"],
+                "dgrad_gemm_ms": mxd["kernels_ms"].get("gemm_dx_mxfp8"),
+                "dh_quantize_ms": mxd["kernels_ms"].get("mx_quantize_dh"),
+                "bf16_dgrad_gemm_ms": bf["kernels_ms"].get("gemm_dx"),
+                "dgrad_gemm_speedup": bf["kernels_ms"]["gemm_dx"] / mxd["kernels_ms"]["gemm_dx_mxfp8"],
+                "note": "dh1/dh3 quantised along h in the step, W1/W3 copies quantised along h once "
+                        "per optimizer step; wgrad stays bf16"},
+            "step_speedup_fwd_and_dgrad_cached_weights": bf["ms_per_step"] / mxd["ms_per_step"],
             "step_speedup": bf["ms_per_step"] / mx["ms_per_step"],
             "step_speedup_cached_weights": bf["ms_per_step"] / mxc["ms_per_step"],
             "fwd_gemm_speedup": bf_fwd / mx_fwd,

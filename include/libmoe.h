@@ -450,6 +450,30 @@ int moe_grouped_swiglu_fwd_mxfp8(const uint8_t* xq, const uint8_t* xs,
                                  uint8_t* aq, uint8_t* as, moe_bf16_t* yp,
                                  void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* MXFP8 dgrad of the expert rows (the Dgrad GEMM the same page quantises with
+ * the forward ones):
+ *   dxp_e = Q(dh1_e) Q(W1[e])^T + Q(dh3_e) Q(W3[e])^T      (fp32 accumulate, bf16 out)
+ * The reduction runs over h, so every operand is quantised along h: dh1q/dh3q
+ * [R][h] codes with row-major scales dh1s/dh3s [R][h/32] (moe_mxfp8_quantize_rows
+ * of dh1 and dh3), and the weights' rows along h, a second set of weight
+ * copies beside the forward's: w1q_h/w3q_h [E][d][h] with scales [E][d][h/32]
+ * (moe_mxfp8_quantize_rows of W1 and W3 viewed as [E*d][h]), whose scales
+ * moe_mxfp8_dx_weight_scale_atoms lays out as the GEMM's atoms (per expert,
+ * 192-column tile of d and 128-deep k-block of K = 2h: W1's k-blocks, then
+ * W3's; two atoms each, columns past d zero).  CTA pairs from 512 rows per
+ * expert on average.  d, h multiples of 128, E <= 768; ws as for
+ * moe_grouped_swiglu_fwd_mxfp8 (the call lays out the scales of dh1 | dh3 as
+ * atoms there). */
+size_t moe_mxfp8_dx_weight_atom_bytes(int E, int d, int h);
+int moe_mxfp8_dx_weight_scale_atoms(const uint8_t* w1s_h, const uint8_t* w3s_h, int E, int d, int h,
+                                    uint8_t* atoms, moe_stream_t stream);
+int moe_grouped_swiglu_bwd_dx_mxfp8(const uint8_t* dh1q, const uint8_t* dh1s,
+                                    const uint8_t* dh3q, const uint8_t* dh3s,
+                                    const int32_t* offsets, int R, int E, int d, int h,
+                                    const uint8_t* w1q_h, const uint8_t* w3q_h,
+                                    const uint8_t* dx_atoms, moe_bf16_t* dxp,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -343,3 +343,138 @@ def test_layer_step_mxfp8_saved_activations(T, E, k):
     for n, key in (("dxp", "dXp"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2")):
         assert_close(getattr(layer, n), b[key], n, rel_l2=MX_REL_L2, max_abs=0.1)
     assert_close(layer.dgate, dg, "dgate", rel_l2=MX_REL_L2, max_abs=0.1)
+
+
+# ------------------------------------------------------------ MXFP8 dgrad
+
+def test_dx_weight_scale_atoms_layout():
+    # the dgrad GEMM's atoms: 192-column tiles of d, k-blocks of K = 2h with
+    # W1's scales first, then W3's
+    E, d, h = 2, 640, 256
+    rng = np.random.default_rng(21)
+    w1s = rng.integers(0, 255, (E, d, h // 32), dtype=np.uint8)
+    w3s = rng.integers(0, 255, (E, d, h // 32), dtype=np.uint8)
+    n = L.moe_mxfp8_dx_weight_atom_bytes(E, d, h)
+    atoms = torch.full((n,), 7, dtype=torch.uint8, device=DEV)
+    L.moe_mxfp8_dx_weight_scale_atoms(torch.from_numpy(w1s).to(DEV), torch.from_numpy(w3s).to(DEV), atoms)
+    both = np.concatenate([w1s, w3s], axis=2)               # [E][d][2h/32]: K = 2h
+    ref = _atoms_of(both, 192, 2 * h)
+    assert n == ref.size
+    assert np.array_equal(u8(atoms), ref)
+
+
+def _dx_inputs(T, d, E, k, h, seed, empty=()):
+    rng = np.random.default_rng(seed)
+    keep = [e for e in range(E) if e not in empty]
+    idx = np.stack([rng.permutation(keep)[:k] for _ in range(T)]).astype(np.int32)
+    _, off, _, _ = ol.route_map(idx, E)
+    R = T * k
+    dh1 = wl.bf16_bits((rng.standard_normal((R, h)) * 0.1).astype(np.float32))
+    dh3 = wl.bf16_bits((rng.standard_normal((R, h)) * 0.1).astype(np.float32))
+    W1 = wl.bf16_bits((rng.standard_normal((E, d, h)) / np.sqrt(d)).astype(np.float32))
+    W3 = wl.bf16_bits((rng.standard_normal((E, d, h)) / np.sqrt(d)).astype(np.float32))
+    return off, dh1, dh3, W1, W3
+
+
+def _device_dx_mxfp8(off, dh1, dh3, W1, W3, E, d, h):
+    R = dh1.shape[0]
+    u = lambda *s: torch.empty(s, dtype=torch.uint8, device=DEV)  # noqa: E731
+    t = {}
+    for n, v in (("dh1", dh1), ("dh3", dh3)):
+        t[n + "q"], t[n + "s"] = u(R, h), u(R, h // 32)
+        L.moe_mxfp8_quantize_rows(bf16_tensor(v, DEV), t[n + "q"], t[n + "s"])
+    for n, v in (("w1", W1), ("w3", W3)):
+        t[n + "q"], t[n + "s"] = u(E, d, h), u(E, d, h // 32)
+        L.moe_mxfp8_quantize_rows(bf16_tensor(v, DEV).view(E * d, h), t[n + "q"].view(E * d, h),
+                                  t[n + "s"].view(E * d, h // 32))
+    atoms = u(L.moe_mxfp8_dx_weight_atom_bytes(E, d, h))
+    L.moe_mxfp8_dx_weight_scale_atoms(t["w1s"], t["w3s"], atoms)
+    dxp = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(L.moe_workspace_size(R, E, 1, d, h), dtype=torch.uint8, device=DEV)
+    L.moe_reset_status(ws)
+    L.moe_grouped_swiglu_bwd_dx_mxfp8(t["dh1q"], t["dh1s"], t["dh3q"], t["dh3s"],
+                                      torch.from_numpy(off.astype(np.int32)).to(DEV), t["w1q"], t["w3q"],
+                                      atoms, dxp, ws)
+    torch.cuda.synchronize()
+    assert L.moe_get_status(ws) == 0
+    return dxp
+
+
+@pytest.mark.parametrize("T,d,E,k,h,empty", [
+    (300, 256, 6, 2, 384, (2,)),       # single CTAs, ragged rows, an empty expert
+    (1000, 640, 16, 4, 256, ()),       # d not a multiple of the 192-column tile
+    (2600, 512, 4, 2, 256, (1,)),      # CTA pairs
+    (1100, 128, 1, 1, 128, ()),        # CTA pairs, the odd CTA of the last tile without rows
+])
+def test_dgrad_mxfp8_small(T, d, E, k, h, empty, record_property):
+    off, dh1, dh3, W1, W3 = _dx_inputs(T, d, E, k, h, seed=T + d, empty=empty)
+    dxp = _device_dx_mxfp8(off, dh1, dh3, W1, W3, E, d, h)
+    dec = ol.decode_bf16
+    ref = om.expert_dgrad_dx_mxfp8(dec(dh1), dec(dh3), off, dec(W1), dec(W3))
+    assert_close(dxp, ref, "dxp", rel_l2=MX_REL_L2, max_abs=0.1)
+    exact = np.zeros_like(ref)
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        exact[lo:hi] = dec(dh1)[lo:hi] @ dec(W1)[e].T + dec(dh3)[lo:hi] @ dec(W3)[e].T
+    rel_q = np.linalg.norm(as_f64(dxp) - ref) / np.linalg.norm(ref)
+    rel = np.linalg.norm(as_f64(dxp) - exact) / np.linalg.norm(exact)
+    record_property("dxp_rel_l2_vs_quantised", float(rel_q))
+    record_property("dxp_rel_l2_vs_unquantised", float(rel))
+    print(f"\nMXFP8 dxp T={T} d={d} E={E} k={k} h={h}: rel-L2 {rel_q:.2e} vs the quantise-dequantise "
+          f"oracle, {rel:.4f} vs the unquantised product")
+    assert rel_q < 1e-2 and 0.01 < rel < 0.08
+
+
+def test_layer_step_mxfp8_dgrad():
+    # the layer step with the forward GEMMs and the dgrad GEMM in MXFP8: the
+    # oracle composes its quantise->dequantise forward, the analytic backward
+    # at those values and its MXFP8 dgrad of the rows
+    from token_dispatch_grouped_router_gb300.layer import MoELayer
+    w = wl.small_workload(T=2600, d=256, E=4, k=2, h=256)
+    inp = wl.generate(w, seed=9)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=False, device=DEV)
+    layer.load_inputs(inp)
+    layer.enable_mxfp8()
+    L.moe_reset_status(layer.ws)
+    layer.step_mxfp8(dgrad="mxfp8")
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    k, E = w.k, w.E
+    g = ol.softmax_gates(inp["glogit"])
+    _, off, ros, _ = ol.route_map(inp["idx"], E)
+    Xp = ol.dispatch(inp["x"], ros, k)
+    f = om.expert_ffn_forward_mxfp8(Xp, off, inp["W1"], inp["W3"], inp["W2"])
+    dYp, dg = ol.combine_backward(inp["dY"], f["Yp"], ros, g, k)
+    b = ol.expert_ffn_backward(Xp, off, inp["W1"], inp["W3"], inp["W2"], f["H1"], f["H3"], f["A"], dYp)
+    dXp = om.expert_dgrad_dx_mxfp8(b["dH1"], b["dH3"], off, ol.decode_bf16(inp["W1"]),
+                                   ol.decode_bf16(inp["W3"]))
+    for n, ref in (("dh1", b["dH1"]), ("dh3", b["dH3"]), ("dxp", dXp),
+                   ("dX", ol.unpermute_sum(dXp, ros, k)), ("dW1", b["dW1"]), ("dW2", b["dW2"])):
+        assert_close(getattr(layer, n), ref, n, rel_l2=MX_REL_L2, max_abs=0.1)
+
+
+def test_full_size_dgrad_mxfp8_sampled():
+    # train_e128 sizes (T = 32768, d = 2048, h = 1024, E = 128, top-4): the
+    # layer's MXFP8 dgrad rows against the oracle's, from the device's dh1/dh3
+    from token_dispatch_grouped_router_gb300.layer import MoELayer
+    w = wl.get_workload("train_e128")
+    inp = wl.generate(w, seed=0)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=False, device=DEV)
+    layer.load_inputs(inp)
+    layer.enable_mxfp8()
+    L.moe_reset_status(layer.ws)
+    layer.step_mxfp8(dgrad="mxfp8")
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    off = layer.offsets.cpu().numpy().astype(np.int64)
+    rng = np.random.default_rng(13)
+    experts = sorted(set(int(e) for e in rng.choice(w.E, 3, replace=False)))
+    rows, ref = [], []
+    dh1 = as_f64(layer.dh1); dh3 = as_f64(layer.dh3)
+    for e in experts:
+        rr = np.sort(rng.choice(np.arange(off[e], off[e + 1]), 4, replace=False))
+        w1 = om.qdq(ol.decode_bf16(inp["W1"][e]), axis=1); w3 = om.qdq(ol.decode_bf16(inp["W3"][e]), axis=1)
+        ref.append(om.qdq(dh1[rr], axis=1) @ w1.T + om.qdq(dh3[rr], axis=1) @ w3.T)
+        rows.extend(rr.tolist())
+    got = layer.dxp[torch.tensor(rows, device=DEV, dtype=torch.long)]
+    assert_close(got, np.concatenate(ref), "dxp", rel_l2=MX_REL_L2, max_abs=0.1)

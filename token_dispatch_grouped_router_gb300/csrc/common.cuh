@@ -77,13 +77,16 @@ inline CapacityScratch capacity_scratch(long long R, int E) {
 
 // moe_grouped_swiglu_fwd_mxfp8: the E8M0 scale atoms of Xq (K = d), then of
 // Aq (K = h): (ceil(R / 128) + E) 128-row blocks x K / 128 atoms of 512 bytes
-// each (layout in mx_common.cuh).
+// each (layout in mx_common.cuh); moe_grouped_swiglu_bwd_dx_mxfp8 puts those
+// of [dh1 | dh3] (K = 2h) in the first region.
 inline size_t mx_act_atom_bytes(long long R, int E, int K) {
   return (size_t)((R + 127) / 128 + E) * (size_t)(K / 128) * 512;
 }
 inline size_t mx_scratch_x(long long R, int E, int d, int h) { (void)R; (void)E; (void)d; (void)h; return kStatusBytes; }
 inline size_t mx_scratch_a(long long R, int E, int d, int h) {
-  return round_up(mx_scratch_x(R, E, d, h) + mx_act_atom_bytes(R, E, d), 256);
+  // (the first region also holds the atoms of the MXFP8 dgrad's dh1 | dh3, K = 2h)
+  const int K = d > 2 * h ? d : 2 * h;
+  return round_up(mx_scratch_x(R, E, d, h) + mx_act_atom_bytes(R, E, K), 256);
 }
 inline size_t mx_scratch_end(long long R, int E, int d, int h) {
   return round_up(mx_scratch_a(R, E, d, h) + mx_act_atom_bytes(R, E, h), 256);

@@ -49,7 +49,7 @@ namespace {
 using namespace ptx;
 using namespace gemm;
 
-enum Mode8 : int { kUp8 = 0, kDown8 = 1 };
+enum Mode8 : int { kUp8 = 0, kDown8 = 1, kDx8 = 2 };
 
 constexpr int BN = 192, BK = 128;               // MMA N, k-block (fp8 bytes)
 constexpr int A_STAGE = 128 * BK;               // 16 KB: one CTA's 128 A rows
@@ -81,7 +81,8 @@ struct Args8 {
   int E, R, d, h;
   int n_tiles;                  // column tiles per expert
   int kb_total;                 // K / 128
-  int N;                        // rows of one weight matrix (UP8: h, DOWN8: d)
+  int kb_split;                 // DX8: k-blocks of (dh1, W1) before those of (dh3, W3)
+  int N;                        // rows of one weight matrix (UP8: h, DOWN8 and DX8: d)
   uint16_t* out0;               // UP8: h1 / DOWN8: yp
   uint16_t* out1;               // UP8: h3
   uint16_t* out2;               // UP8: a
@@ -217,7 +218,8 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
 // drain the other accumulator.
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads8, 1)
-grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB0,
                      const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSA,
                      const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmO0,
                      const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
@@ -275,7 +277,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     else { tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols); tmem_relinquish(); }
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmA); prefetch_tmap(&tmA1); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
     prefetch_tmap(&tmSA); prefetch_tmap(&tmSB);
     prefetch_tmap(&tmO0); prefetch_tmap(&tmO1); prefetch_tmap(&tmO2);
   }
@@ -305,27 +307,33 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
           const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
           const int arow = rt.row0 + 128 * (int)rank;
+          // DX8 reduces over [dh1 | dh3] x [W1 | W3]: the second pair of maps
+          // from k-block kb_split on
+          const bool second = MODE == kDx8 && kb >= args.kb_split;
+          const int kx = (second ? kb - args.kb_split : kb) * BK;
+          const CUtensorMap* ma = second ? &tmA1 : &tmA;
+          const CUtensorMap* mb = second ? &tmB1 : &tmB0;
           if constexpr (PAIR) {
             const uint32_t fb = mapa_shared(fb_local, 0);
             if (leader) mbar_arrive_expect_tx(fb_local, 2 * (A_STAGE + B_STAGE + SF_STAGE));
-            tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
+            tma_load_2d_pair(sa, ma, fb, kx, arow);
             if constexpr (MODE == kUp8) {
               // the even CTA stages the 96 W1 rows, the odd CTA the same W3 rows
-              tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, fb, kb * BK, n0, rt.e);
+              tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, fb, kx, n0, rt.e);
             } else {
-              tma_load_3d_pair(sb, &tmB0, fb, kb * BK, n0 + 96 * (int)rank, rt.e);
+              tma_load_3d_pair(sb, mb, fb, kx, n0 + 96 * (int)rank, rt.e);
             }
             tma_load_2d_pair(ss, &tmSA, fb, 0, blk * KB + kb);
             tma_load_2d_pair(ss + mx::kAtomBytes, &tmSB, fb, 0, (wat + kb) * 2);
           } else {
             mbar_arrive_expect_tx(fb_local, A_STAGE + B_STAGE + SF_STAGE);
-            tma_load_2d(sa, &tmA, fb_local, kb * BK, arow);
+            tma_load_2d(sa, ma, fb_local, kx, arow);
             if constexpr (MODE == kUp8) {
               // 96 rows of W1 then the same 96 rows of W3
-              tma_load_3d(sb, &tmB0, fb_local, kb * BK, n0, rt.e);
-              tma_load_3d(sb + 96 * BK, &tmB1, fb_local, kb * BK, n0, rt.e);
+              tma_load_3d(sb, &tmB0, fb_local, kx, n0, rt.e);
+              tma_load_3d(sb + 96 * BK, &tmB1, fb_local, kx, n0, rt.e);
             } else {
-              tma_load_3d(sb, &tmB0, fb_local, kb * BK, n0, rt.e);
+              tma_load_3d(sb, mb, fb_local, kx, n0, rt.e);
             }
             tma_load_2d(ss, &tmSA, fb_local, 0, blk * KB + kb);
             tma_load_2d(ss + mx::kAtomBytes, &tmSB, fb_local, 0, (wat + kb) * 2);
@@ -479,9 +487,11 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 // Thread per (row, k-block): the row's four scale bytes of the k-block, one
 // 32-bit word of an atom.  Offsets are clamped to [0, R] as the GEMM reads
 // them, so every word lands inside the (ceil(R/128) + E) K/128 atoms.
+// kb_off / KB_total place a table that covers only part of the reduction
+// (DX8's dh1 and dh3 halves of K = 2h) inside atoms of the whole K.
 __global__ void __launch_bounds__(256)
 act_atoms_kernel(const uint8_t* __restrict__ s, const int32_t* __restrict__ offsets, int E, int R, int K,
-                 uint32_t* __restrict__ atoms) {
+                 int kb_off, int KB_total, uint32_t* __restrict__ atoms) {
   pdl_enter();
   const int KB = K / 128;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -495,29 +505,31 @@ act_atoms_kernel(const uint8_t* __restrict__ s, const int32_t* __restrict__ offs
   const int off = max(0, min(__ldg(offsets + lo), row));
   const int srow = row - off + 128 * mx::act_block0(off, lo);
   const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(s + (size_t)row * (K / 32)) + kb);
-  atoms[((size_t)(srow >> 7) * KB + kb) * 128 + (srow & 31) * 4 + ((srow >> 5) & 3)] = v;
+  atoms[((size_t)(srow >> 7) * KB_total + kb_off + kb) * 128 + (srow & 31) * 4 + ((srow >> 5) & 3)] = v;
 }
 
-// Row-major weight scales [E][N][K/32] -> the atoms of the GEMM's column
-// tiles (cols = 96: 96 rows of s0 then the same rows of s1; cols = 192: 192
-// rows of s0).  Thread per (tile k-block, column 0..255); columns 192-255 and
-// rows past N are zero.
+// Row-major weight scales [E][N][Ksrc/32] -> the atoms of the GEMM's column
+// tiles of `cols` columns over KB 128-deep k-blocks.  col_split = 96: tile
+// columns 0-95 are rows of s0, 96-191 the same rows of s1 (the up-projection);
+// kb_split < KB: k-blocks from kb_split on come from s1 (DX8's [W1 | W3]).
+// Thread per (tile k-block, column 0..255); columns 192-255 and rows past N
+// are zero.
 __global__ void __launch_bounds__(256)
-weight_atoms_kernel(const uint8_t* __restrict__ s0, const uint8_t* __restrict__ s1, int E, int N, int K,
-                    int cols, int NT, uint32_t* __restrict__ atoms) {
+weight_atoms_kernel(const uint8_t* __restrict__ s0, const uint8_t* __restrict__ s1, int E, int N, int Ksrc,
+                    int cols, int col_split, int NT, int KB, int kb_split, uint32_t* __restrict__ atoms) {
   pdl_enter();
-  const int KB = K / 128;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)E * NT * KB * 256) return;
   const int c = (int)(i & 255);
   const long long p = i >> 8;                     // ((e * NT + nt) * KB + kb)
   const int kb = (int)(p % KB), nt = (int)((p / KB) % NT), e = (int)(p / ((long long)KB * NT));
   const uint8_t* tab = s0;
-  int n = nt * cols + c;
-  if (cols == mx::kUpCols && c >= mx::kUpCols) { tab = s1; n -= mx::kUpCols; }
+  int n = nt * cols + c, kk = kb;
+  if (col_split > 0 && c >= col_split) { tab = s1; n -= col_split; }
+  if (kb >= kb_split) { tab = s1; kk = kb - kb_split; }
   uint32_t v = 0;
   if (c < BN && n < N)
-    v = __ldg(reinterpret_cast<const uint32_t*>(tab + ((size_t)e * N + n) * (K / 32)) + kb);
+    v = __ldg(reinterpret_cast<const uint32_t*>(tab + ((size_t)e * N + n) * (Ksrc / 32)) + kk);
   atoms[(p * 2 + (c >> 7)) * 128 + (c & 31) * 4 + ((c >> 5) & 3)] = v;
 }
 
@@ -542,7 +554,7 @@ constexpr size_t smem_bytes8(int E) {
 static_assert(smem_bytes8<true>(kMaxExperts8) <= 227 * 1024, "pair MXFP8 kernel fits in shared memory");
 static_assert(smem_bytes8<false>(kMaxExperts8) <= 227 * 1024, "MXFP8 kernel fits in shared memory");
 
-struct Maps8 { CUtensorMap a, b0, b1, sa, sb, o0, o1, o2; };
+struct Maps8 { CUtensorMap a, a1, b0, b1, sa, sb, o0, o1, o2; };
 
 template <int MODE, bool PAIR>
 int launch8(const Maps8& m, const Args8& args, long long tiles_upper, cudaStream_t s) {
@@ -565,13 +577,13 @@ int launch8(const Maps8& m, const Args8& args, long long tiles_upper, cudaStream
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kern, m.a, m.b0, m.b1, m.sa, m.sb, m.o0, m.o1, m.o2, args) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, m.a, m.a1, m.b0, m.b1, m.sa, m.sb, m.o0, m.o1, m.o2, args) != cudaSuccess) {
       (void)cudaGetLastError();
       return MOE_ERR_CUDA;
     }
   } else {
     const long long g = ub < sm_count() ? ub : sm_count();
-    (void)launch_pdl(kern, (unsigned)g, kThreads8, smem_bytes8<PAIR>(args.E), s, m.a, m.b0, m.b1, m.sa, m.sb,
+    (void)launch_pdl(kern, (unsigned)g, kThreads8, smem_bytes8<PAIR>(args.E), s, m.a, m.a1, m.b0, m.b1, m.sa, m.sb,
                      m.o0, m.o1, m.o2, args);
   }
   MOE_LAUNCH_CHECK(1);
@@ -606,9 +618,9 @@ extern "C" int moe_mxfp8_weight_scale_atoms(const uint8_t* w1s, const uint8_t* w
   const int ntu = mx::up_tiles(h), ntd = mx::down_tiles(d);
   const long long nu = (long long)E * ntu * (d / 128) * 256, nd = (long long)E * ntd * (h / 128) * 256;
   (void)launch_pdl(weight_atoms_kernel, (unsigned)((nu + 255) / 256), 256, 0, s, w1s, w3s, E, h, d,
-                   mx::kUpCols, ntu, up);
+                   mx::kUpCols, mx::kUpCols, ntu, d / 128, d / 128, up);
   (void)launch_pdl(weight_atoms_kernel, (unsigned)((nd + 255) / 256), 256, 0, s, w2s, w2s, E, d, h,
-                   mx::kDownCols, ntd, dn);
+                   mx::kDownCols, 0, ntd, h / 128, h / 128, dn);
   MOE_LAUNCH_CHECK(2);
   return MOE_OK;
 }
@@ -646,13 +658,14 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint32_t brows = pair ? 96 : 192;
   Maps8 mu{}, md{};
-  if (!map2d(&mu.a, xq, d, R, BK, 128, U8, 1) || !map3d(&mu.b0, w1q, d, h, E, BK, 96, U8, 1) ||
+  if (!map2d(&mu.a, xq, d, R, BK, 128, U8, 1) || !map2d(&mu.a1, xq, d, R, BK, 128, U8, 1) ||
+      !map3d(&mu.b0, w1q, d, h, E, BK, 96, U8, 1) ||
       !map3d(&mu.b1, w3q, d, h, E, BK, 96, U8, 1) || !map_atoms(&mu.sa, xatoms, nbx, 1) ||
       !map_atoms(&mu.sb, up_atoms, n_up_atoms, 2) ||
       !map2d(&md.a, aq, h, R, BK, 128, U8, 1) || !map3d(&md.b0, w2q, h, d, E, BK, brows, U8, 1) ||
       !map_atoms(&md.sa, aatoms, nba, 1) || !map_atoms(&md.sb, dn_atoms, n_dn_atoms, 2))
     return MOE_ERR_CUDA;
-  md.b1 = md.b0;
+  md.b1 = md.b0; md.a1 = md.a;
   if (!map2d_out(&mu.o0, h1, h, R, h) || !map2d_out(&mu.o1, h3, h, R, h) ||
       !map2d_out(&mu.o2, a ? a : h1, h, R, h) || !map2d_out(&md.o0, yp, d, R, d))
     return MOE_ERR_CUDA;
@@ -660,20 +673,87 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   Args8 g{};
   g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
   // up-projection: K = d, 96 columns of W1 and of W3 per tile
-  g.kb_total = d / BK; g.n_tiles = mx::up_tiles(h); g.N = h;
+  g.kb_total = d / BK; g.kb_split = g.kb_total; g.n_tiles = mx::up_tiles(h); g.N = h;
   g.out0 = h1; g.out1 = h3; g.out2 = a; g.aq = aq; g.as = as;
   const long long lx = (long long)R * (d / 128), la = (long long)R * (h / 128);
-  (void)launch_pdl(act_atoms_kernel, (unsigned)((lx + 255) / 256), 256, 0, s, xs, offsets, E, R, d, xatoms);
+  (void)launch_pdl(act_atoms_kernel, (unsigned)((lx + 255) / 256), 256, 0, s, xs, offsets, E, R, d, 0,
+                   d / 128, xatoms);
   MOE_LAUNCH_CHECK(1);
   int st = pair ? launch8<kUp8, true>(mu, g, row_tiles_upper(R, E, g.n_tiles, TM), s)
                 : launch8<kUp8, false>(mu, g, row_tiles_upper(R, E, g.n_tiles, TM), s);
   if (st != MOE_OK) return st;
   // down-projection: K = h
   Args8 g2 = g;
-  g2.kb_total = h / BK; g2.n_tiles = mx::down_tiles(d); g2.N = d;
+  g2.kb_total = h / BK; g2.kb_split = g2.kb_total; g2.n_tiles = mx::down_tiles(d); g2.N = d;
   g2.out0 = yp; g2.out1 = nullptr; g2.out2 = nullptr; g2.aq = nullptr; g2.as = nullptr;
-  (void)launch_pdl(act_atoms_kernel, (unsigned)((la + 255) / 256), 256, 0, s, as, offsets, E, R, h, aatoms);
+  (void)launch_pdl(act_atoms_kernel, (unsigned)((la + 255) / 256), 256, 0, s, as, offsets, E, R, h, 0,
+                   h / 128, aatoms);
   MOE_LAUNCH_CHECK(1);
   return pair ? launch8<kDown8, true>(md, g2, row_tiles_upper(R, E, g2.n_tiles, TM), s)
               : launch8<kDown8, false>(md, g2, row_tiles_upper(R, E, g2.n_tiles, TM), s);
+}
+
+extern "C" size_t moe_mxfp8_dx_weight_atom_bytes(int E, int d, int h) {
+  if (E < 1 || d <= 0 || h <= 0 || d % 128 != 0 || h % 128 != 0) return 0;
+  return (size_t)E * mx::down_tiles(d) * (2 * h / 128) * 2 * mx::kAtomBytes;
+}
+
+extern "C" int moe_mxfp8_dx_weight_scale_atoms(const uint8_t* w1s_h, const uint8_t* w3s_h, int E, int d, int h,
+                                               uint8_t* atoms, moe_stream_t stream) {
+  if (E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || h % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  auto al4 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!al4(w1s_h) || !al4(w3s_h)) return MOE_ERR_INVALID_ARG;
+  MOE_CHECK_PTR(atoms);
+  const int nt = mx::down_tiles(d), KB = 2 * h / 128;
+  const long long n = (long long)E * nt * KB * 256;
+  (void)launch_pdl(weight_atoms_kernel, (unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream, w1s_h,
+                   w3s_h, E, d, h, mx::kDownCols, 0, nt, KB, h / 128, reinterpret_cast<uint32_t*>(atoms));
+  MOE_LAUNCH_CHECK(1);
+  return MOE_OK;
+}
+
+extern "C" int moe_grouped_swiglu_bwd_dx_mxfp8(
+    const uint8_t* dh1q, const uint8_t* dh1s, const uint8_t* dh3q, const uint8_t* dh3s,
+    const int32_t* offsets, int R, int E, int d, int h, const uint8_t* w1q_h, const uint8_t* w3q_h,
+    const uint8_t* dx_atoms, moe_bf16_t* dxp, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (R < 0 || E < 1 || E > kMaxExperts || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || h % 128 != 0 || E > kMaxExperts8) return MOE_ERR_UNSUPPORTED;
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < mx_scratch_end(R, E, d, h)) return MOE_ERR_WORKSPACE;
+  if (R == 0) return MOE_OK;
+  MOE_CHECK_PTR(dh1q); MOE_CHECK_PTR(dh3q); MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(w1q_h);
+  MOE_CHECK_PTR(w3q_h); MOE_CHECK_PTR(dx_atoms); MOE_CHECK_PTR(dxp);
+  auto al4 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!al4(dh1s) || !al4(dh3s)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* atoms = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + mx_scratch_x(R, E, d, h));
+  const int KB = 2 * h / BK, KBh = h / BK;
+  const long long nba = mx::act_atom_blocks(R, E) * KB;
+  const long long n_w_atoms = (long long)E * mx::down_tiles(d) * KB * 2;
+  const bool pair = (long long)R >= kPairMinRows8 * E;
+  const int TM = pair ? 256 : 128;
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t brows = pair ? 96 : 192;
+  Maps8 m{};
+  if (!map2d(&m.a, dh1q, h, R, BK, 128, U8, 1) || !map2d(&m.a1, dh3q, h, R, BK, 128, U8, 1) ||
+      !map3d(&m.b0, w1q_h, h, d, E, BK, brows, U8, 1) || !map3d(&m.b1, w3q_h, h, d, E, BK, brows, U8, 1) ||
+      !map_atoms(&m.sa, atoms, nba, 1) || !map_atoms(&m.sb, dx_atoms, n_w_atoms, 2) ||
+      !map2d_out(&m.o0, dxp, d, R, d))
+    return MOE_ERR_CUDA;
+  m.o1 = m.o0; m.o2 = m.o0;
+  // the row-major scales of dh1 and dh3 become the two halves of K = 2h
+  const long long l = (long long)R * KBh;
+  (void)launch_pdl(act_atoms_kernel, (unsigned)((l + 255) / 256), 256, 0, s, dh1s, offsets, E, R, h, 0, KB,
+                   atoms);
+  (void)launch_pdl(act_atoms_kernel, (unsigned)((l + 255) / 256), 256, 0, s, dh3s, offsets, E, R, h, KBh, KB,
+                   atoms);
+  MOE_LAUNCH_CHECK(2);
+  Args8 g{};
+  g.offsets = offsets; g.E = E; g.R = R; g.d = d; g.h = h; g.status = reinterpret_cast<int*>(ws);
+  g.kb_total = KB; g.kb_split = KBh; g.n_tiles = mx::down_tiles(d); g.N = d;
+  g.out0 = dxp;
+  return pair ? launch8<kDx8, true>(m, g, row_tiles_upper(R, E, g.n_tiles, TM), s)
+              : launch8<kDx8, false>(m, g, row_tiles_upper(R, E, g.n_tiles, TM), s);
 }

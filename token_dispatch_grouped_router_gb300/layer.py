@@ -198,9 +198,19 @@ class MoELayer:
         mark("gemm_dact")
         L.moe_grouped_swiglu_bwd_dact(self.offsets, self.W2, self.h1, self.h3, self.dyp,
                                       self.dh1, self.dh3, self.ws)
-        mark("gemm_dx")
-        L.moe_grouped_swiglu_bwd_dx(self.offsets, self.W1, self.W3, self.dh1, self.dh3,
-                                    self.dxp, self.ws)
+        if getattr(self, "mx_dgrad", False):
+            # dh1, dh3 quantised along h, then the block-scaled dgrad GEMM
+            mark("mx_quantize_dh")
+            L.moe_mxfp8_quantize_rows(self.dh1, self.dh1q, self.dh1s)
+            L.moe_mxfp8_quantize_rows(self.dh3, self.dh3q, self.dh3s)
+            mark("gemm_dx_mxfp8")
+            L.moe_grouped_swiglu_bwd_dx_mxfp8(self.dh1q, self.dh1s, self.dh3q, self.dh3s,
+                                              self.offsets, self.w1q_h, self.w3q_h,
+                                              self.dx_atoms, self.dxp, self.ws)
+        else:
+            mark("gemm_dx")
+            L.moe_grouped_swiglu_bwd_dx(self.offsets, self.W1, self.W3, self.dh1, self.dh3,
+                                        self.dxp, self.ws)
         mark("gemm_wgrad")
         L.moe_grouped_swiglu_bwd_wgrad(self.xp, self.offsets, self.a, self.dyp, self.dh1,
                                        self.dh3, self.dW1, self.dW3, self.dW2, self.ws)
@@ -234,15 +244,37 @@ class MoELayer:
         self.w_atoms = u(L.moe_mxfp8_weight_atom_bytes(E, d, h))
         self.xq, self.xs = u(R, d), u(R, d // 32)
         self.aq, self.as_ = u(R, h), u(R, h // 32)
+        # MXFP8 dgrad: W1 / W3 quantised along h (their own copies) and the
+        # quantised dh1 / dh3 of a step
+        self.w1q_h, self.w1s_h = u(E, d, h), u(E, d, h // 32)
+        self.w3q_h, self.w3s_h = u(E, d, h), u(E, d, h // 32)
+        self.dx_atoms = u(L.moe_mxfp8_dx_weight_atom_bytes(E, d, h))
+        if self.with_backward:
+            self.dh1q, self.dh1s = u(R, h), u(R, h // 32)
+            self.dh3q, self.dh3s = u(R, h), u(R, h // 32)
+        self.mx_dgrad = False
 
-    def quantize_weights(self, mark=None) -> None:
-        """Re-make the MXFP8 weight copies (once per optimizer step)."""
+    def quantize_weights(self, mark=None, dgrad: bool = True) -> None:
+        """Re-make the MXFP8 weight copies (once per optimizer step); dgrad
+        also makes the dgrad GEMM's copies of W1 / W3 (quantised along h)."""
         mark = mark or _nomark
         mark("mx_quantize_weights")
         L.moe_mxfp8_quantize_weights(self.W1, self.w1q, self.w1s)
         L.moe_mxfp8_quantize_weights(self.W3, self.w3q, self.w3s)
         L.moe_mxfp8_quantize_weights(self.W2, self.w2q, self.w2s)
         L.moe_mxfp8_weight_scale_atoms(self.w1s, self.w3s, self.w2s, self.w_atoms)
+        if dgrad:
+            self._quantize_dgrad_weights()
+
+    def _quantize_dgrad_weights(self) -> None:
+        """W1 and W3 quantised along h (the dgrad GEMM's reduction), from the
+        bf16 weights, and their scale atoms."""
+        E, d, h = self.E, self.d, self.h
+        L.moe_mxfp8_quantize_rows(self.W1.view(E * d, h), self.w1q_h.view(E * d, h),
+                                  self.w1s_h.view(E * d, h // 32))
+        L.moe_mxfp8_quantize_rows(self.W3.view(E * d, h), self.w3q_h.view(E * d, h),
+                                  self.w3s_h.view(E * d, h // 32))
+        L.moe_mxfp8_dx_weight_scale_atoms(self.w1s_h, self.w3s_h, self.dx_atoms)
 
     def quantize_weights_from_masters(self, W1m: torch.Tensor, W3m: torch.Tensor,
                                       W2m: torch.Tensor) -> None:
@@ -252,6 +284,7 @@ class MoELayer:
         L.moe_mxfp8_quantize_weights_f32(W3m, self.w3q, self.w3s)
         L.moe_mxfp8_quantize_weights_f32(W2m, self.w2q, self.w2s)
         L.moe_mxfp8_weight_scale_atoms(self.w1s, self.w3s, self.w2s, self.w_atoms)
+        self._quantize_dgrad_weights()
 
     def forward_mxfp8(self, mark=None, saved: str = "bf16") -> torch.Tensor:
         """Forward with MXFP8 GEMM operands.  saved="bf16": h1, h3, a and xp
@@ -283,14 +316,23 @@ class MoELayer:
         L.moe_mxfp8_dequantize_rows(self.xq, self.xs, self.xp)
         L.moe_mxfp8_dequantize_rows(self.aq, self.as_, self.a)
 
-    def step_mxfp8(self, mark=None, requantize: bool = True, saved: str = "bf16") -> None:
+    def step_mxfp8(self, mark=None, requantize: bool = True, saved: str = "bf16",
+                   dgrad: str = "bf16") -> None:
+        """Forward through the block-scaled GEMMs; backward in bf16, with the
+        dgrad GEMM in MXFP8 too when dgrad="mxfp8"."""
+        if dgrad not in ("bf16", "mxfp8"):
+            raise ValueError(f"dgrad must be 'bf16' or 'mxfp8', not {dgrad!r}")
         if requantize:
-            self.quantize_weights(mark)
+            self.quantize_weights(mark, dgrad=dgrad == "mxfp8")
         self.forward_mxfp8(mark, saved=saved)
         if self.with_backward:
             if saved == "mxfp8":
                 self.restore_saved_mxfp8(mark)
-            self.backward(mark)
+            self.mx_dgrad = dgrad == "mxfp8"
+            try:
+                self.backward(mark)
+            finally:
+                self.mx_dgrad = False
         if mark is not None:
             mark("end")
 

@@ -55,6 +55,10 @@ SIGNATURES = {
     "moe_mxfp8_dequantize_rows": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_dispatch_rows_mxfp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_mxfp8_weight_atom_bytes": (_Z, [_I, _I, _I]),
+    "moe_mxfp8_dx_weight_atom_bytes": (_Z, [_I, _I, _I]),
+    "moe_mxfp8_dx_weight_scale_atoms": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "moe_grouped_swiglu_bwd_dx_mxfp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                             _P, _Z, _P]),
     "moe_mxfp8_weight_scale_atoms": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P, _Z, _P]),
@@ -483,3 +487,35 @@ def moe_grouped_swiglu_fwd_mxfp8(xq, xs, offsets, w1q, w3q, w2q, w_atoms,
         _ptr(xq), _ptr(xs), _ptr(offsets), R, E, d, h, _ptr(w1q), _ptr(w3q), _ptr(w2q),
         _ptr(w_atoms), _ptr(h1), _ptr(h3), _ptr(a), _ptr(aq), _ptr(as_), _ptr(yp),
         _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_mxfp8_dx_weight_atom_bytes(E: int, d: int, h: int) -> int:
+    return int(load().moe_mxfp8_dx_weight_atom_bytes(E, d, h))
+
+
+def moe_mxfp8_dx_weight_scale_atoms(w1s_h, w3s_h, atoms) -> None:
+    """Scales of W1/W3 quantised along h ([E][d][h/32]) in the atom order of
+    the MXFP8 dgrad GEMM."""
+    E, d, kh = w1s_h.shape
+    h = kh * 32
+    _want(w1s_h, torch.uint8, (E, d, h // 32), "w1s_h"); _want(w3s_h, torch.uint8, (E, d, h // 32), "w3s_h")
+    _want(atoms, torch.uint8, (moe_mxfp8_dx_weight_atom_bytes(E, d, h),), "atoms")
+    _ok("moe_mxfp8_dx_weight_scale_atoms", load().moe_mxfp8_dx_weight_scale_atoms(
+        _ptr(w1s_h), _ptr(w3s_h), E, d, h, _ptr(atoms), _stream()))
+
+
+def moe_grouped_swiglu_bwd_dx_mxfp8(dh1q, dh1s, dh3q, dh3s, offsets, w1q_h, w3q_h, dx_atoms,
+                                    dxp, ws) -> None:
+    R, h = dh1q.shape
+    E, d, _ = w1q_h.shape
+    for n, t in (("dh1q", dh1q), ("dh3q", dh3q)):
+        _want(t, torch.uint8, (R, h), n)
+    for n, t in (("dh1s", dh1s), ("dh3s", dh3s)):
+        _want(t, torch.uint8, (R, h // 32), n)
+    for n, t in (("w1q_h", w1q_h), ("w3q_h", w3q_h)):
+        _want(t, torch.uint8, (E, d, h), n)
+    _want(dx_atoms, torch.uint8, (moe_mxfp8_dx_weight_atom_bytes(E, d, h),), "dx_atoms")
+    _want(dxp, torch.bfloat16, (R, d), "dxp")
+    _ok("moe_grouped_swiglu_bwd_dx_mxfp8", load().moe_grouped_swiglu_bwd_dx_mxfp8(
+        _ptr(dh1q), _ptr(dh1s), _ptr(dh3q), _ptr(dh3s), _ptr(offsets), R, E, d, h, _ptr(w1q_h),
+        _ptr(w3q_h), _ptr(dx_atoms), _ptr(dxp), _ptr(ws), _wsb(ws), _stream()))
