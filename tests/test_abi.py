@@ -169,3 +169,36 @@ def test_capacity_calls_check_arguments_on_the_host(lib):
     # T = 0: the padded combine does nothing
     assert lib.moe_combine_capacity(NULL, 8, 4, NULL, NULL, 0, 2, 16, NULL, NULL) == 0
     assert lib.moe_launch_count() == before
+
+
+def test_mxfp8_atom_and_dgrad_calls_check_arguments_on_the_host(lib):
+    NULL = None
+    fake = ctypes.c_void_p(0x1000)
+    odd4 = ctypes.c_void_p(0x1002)          # not 4-byte aligned
+    big = 1 << 34
+    before = lib.moe_launch_count()
+    # atom sizes: zero unless d and h are multiples of 128
+    assert lib.moe_mxfp8_weight_atom_bytes(2, 96, 128) == 0
+    assert lib.moe_mxfp8_dx_weight_atom_bytes(2, 128, 64) == 0
+    # per expert: ceil(h/96) up tiles x d/128 k-blocks + ceil(d/192) down tiles x h/128, 2 atoms each
+    assert lib.moe_mxfp8_weight_atom_bytes(2, 256, 384) == 2 * (4 * 2 + 2 * 3) * 2 * 512
+    assert lib.moe_mxfp8_dx_weight_atom_bytes(2, 256, 384) == 2 * 2 * 6 * 2 * 512
+    # weight atoms: sizes, scale-table alignment
+    assert lib.moe_mxfp8_weight_scale_atoms(fake, fake, fake, 2, 96, 128, fake, NULL) == -2
+    assert lib.moe_mxfp8_weight_scale_atoms(odd4, fake, fake, 2, 128, 128, fake, NULL) == -1
+    assert lib.moe_mxfp8_dx_weight_scale_atoms(fake, NULL, 2, 128, 128, fake, NULL) == -1
+    assert lib.moe_mxfp8_dx_weight_scale_atoms(fake, fake, 0, 128, 128, fake, NULL) == -1
+    # the MXFP8 dgrad: sizes, experts, workspace, pointers
+    args = lambda R, E, d, h, ws, n, s1=fake: (fake, s1, fake, fake, fake, R, E, d, h, fake, fake,  # noqa: E731
+                                             fake, fake, ws, n, NULL)
+    assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(64, 2, 192, 128, fake, big)) == -2
+    assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(64, 800, 128, 128, fake, big)) == -2
+    assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(64, 2, 128, 128, NULL, 0)) == -3
+    assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(64, 2, 128, 128, fake, 4096)) == -3
+    assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(64, 2, 128, 128, fake, big, s1=odd4)) == -1
+    # the MXFP8 forward checks its workspace for the activation scale atoms
+    fwd = (fake, fake, fake, 64, 2, 128, 128, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake)
+    assert lib.moe_grouped_swiglu_fwd_mxfp8(*fwd, fake, 4096, NULL) == -3
+    # R = 0 launches nothing
+    assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(0, 2, 128, 128, fake, big)) == 0
+    assert lib.moe_launch_count() == before
