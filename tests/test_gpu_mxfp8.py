@@ -478,3 +478,31 @@ def test_full_size_dgrad_mxfp8_sampled():
         rows.extend(rr.tolist())
     got = layer.dxp[torch.tensor(rows, device=DEV, dtype=torch.long)]
     assert_close(got, np.concatenate(ref), "dxp", rel_l2=MX_REL_L2, max_abs=0.1)
+
+
+def test_mxfp8_step_captures_into_a_graph():
+    # the MXFP8 step (forward and dgrad block-scaled, weights re-quantised in
+    # the step) has no host synchronisation either: captured and replayed, it
+    # reproduces the eager step bit for bit
+    from token_dispatch_grouped_router_gb300.layer import MoELayer
+    w = wl.small_workload(T=1300, d=256, E=4, k=2, h=256)
+    inp = wl.generate(w, seed=12)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=False, device=DEV)
+    layer.load_inputs(inp)
+    layer.enable_mxfp8()
+    step = lambda: layer.step_mxfp8(requantize=True, dgrad="mxfp8")  # noqa: E731
+    step()
+    torch.cuda.synchronize()
+    names = ("out", "dxp", "dX", "dW1", "dW2", "dgate", "aq")
+    eager = {n: getattr(layer, n).clone() for n in names}
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    for n in ("out", "dxp", "dX", "dW1", "dW2"):
+        getattr(layer, n).zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for n, v in eager.items():
+        assert torch.equal(getattr(layer, n), v), n

@@ -154,3 +154,41 @@ def test_padded_full_size_sampled(key):
     assert_close(layer.out[tk], np.array(out_ref), "out")
     assert_close(layer.dgate[tk], np.array(dg_ref), "dgate")
     assert_close(layer.dX[tk], np.array(dX_ref), "dX")
+
+
+def test_padded_layer_zero_tokens_and_graph_capture():
+    # T = 0: every expert holds one zero row; the weight gradients are zero
+    layer = MoELayer(0, 128, 4, 2, 128, learned=False, device=DEV, capacity_factor=1.25)
+    for n in ("W1", "W3", "W2"):
+        getattr(layer, n).normal_()
+    for n in ("dW1", "dW3", "dW2"):
+        getattr(layer, n).fill_(1.0)
+    L.moe_reset_status(layer.ws)
+    layer.step()
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    assert layer.C == 1 and np.all(i32(layer.counts) == 0)
+    for n in ("dW1", "dW3", "dW2"):
+        assert torch.count_nonzero(getattr(layer, n)).item() == 0
+    # the padded step has no host synchronisation: it captures into a CUDA
+    # graph and replays bit for bit (learned Zipf router, dropped slots)
+    w = wl.small_workload(T=640, d=256, E=32, k=4, h=192, routing="learned", zipf=True)
+    inp = wl.generate(w, seed=5)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=True, device=DEV, capacity_factor=1.25)
+    layer.load_inputs(inp)
+    layer.step()
+    torch.cuda.synchronize()
+    names = ("row_of_slot", "out", "dX", "dW1", "dW2", "dW_r", "dgate")
+    eager = {n: getattr(layer, n).clone() for n in names}
+    assert (i32(layer.row_of_slot) < 0).any()            # some slots dropped
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.step()
+    for n in ("out", "dX", "dW1", "dW2", "dW_r"):
+        getattr(layer, n).zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for n, v in eager.items():
+        assert torch.equal(getattr(layer, n), v), n

@@ -61,8 +61,8 @@ class MoELayer:
         self.recompute = recompute
         # capacity-padded layer: E * C rows in every expert-sorted buffer
         self.C = int(math.ceil(capacity_factor * T * k / E)) if capacity_factor else None
-        if self.C is not None and T > 0:
-            self.C = max(self.C, 1)
+        if self.C is not None:
+            self.C = max(self.C, 1)           # T = 0: one zero row an expert, dW = 0
         self.R = T * k if self.C is None else E * self.C
         dev = torch.device(device)
         bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
