@@ -465,6 +465,18 @@ int moe_grouped_swiglu_fwd_mxfp8(const uint8_t* xq, const uint8_t* xs,
  * moe_grouped_swiglu_fwd_mxfp8 (the call lays out the scales of dh1 | dh3 as
  * atoms there). */
 size_t moe_mxfp8_dx_weight_atom_bytes(int E, int d, int h);
+/* moe_grouped_swiglu_bwd_dact that also writes dh1 / dh3 quantised along h
+ * for the MXFP8 dgrad: dh1q/dh3q [R][h] codes, dh1s/dh3s [R][h/32] scales,
+ * from the epilogue's own bf16 dh1 / dh3 (the same bytes as
+ * moe_mxfp8_quantize_rows of them; the epilogue holds one row's 32-column
+ * block per thread, so no separate pass over dh1 / dh3 is made).  Codes
+ * 16-byte aligned. */
+int moe_grouped_swiglu_bwd_dact_mxfp8(const int32_t* offsets, int R, int E, int d, int h,
+                                      const moe_bf16_t* W2, const moe_bf16_t* h1,
+                                      const moe_bf16_t* h3, const moe_bf16_t* dyp,
+                                      moe_bf16_t* dh1, moe_bf16_t* dh3, uint8_t* dh1q,
+                                      uint8_t* dh1s, uint8_t* dh3q, uint8_t* dh3s, void* ws,
+                                      size_t ws_bytes, moe_stream_t stream);
 int moe_mxfp8_dx_weight_scale_atoms(const uint8_t* w1s_h, const uint8_t* w3s_h, int E, int d, int h,
                                     uint8_t* atoms, moe_stream_t stream);
 int moe_grouped_swiglu_bwd_dx_mxfp8(const uint8_t* dh1q, const uint8_t* dh1s,

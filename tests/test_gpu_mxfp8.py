@@ -506,3 +506,30 @@ def test_mxfp8_step_captures_into_a_graph():
     torch.cuda.synchronize()
     for n, v in eager.items():
         assert torch.equal(getattr(layer, n), v), n
+
+
+@pytest.mark.parametrize("T,E,k", [(500, 8, 2), (2600, 4, 2)])   # single CTAs / CTA pairs
+def test_dact_with_quantised_outputs(T, E, k):
+    # the dact epilogue also writing dh1 / dh3 quantised along h: the bf16
+    # outputs are those of the plain call bit for bit, and the codes and scales
+    # are the oracle's MXFP8 blocks of those bf16 values, bit for bit
+    from token_dispatch_grouped_router_gb300.layer import MoELayer
+    w = wl.small_workload(T=T, d=256, E=E, k=k, h=384)
+    inp = wl.generate(w, seed=16)
+    layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=False, device=DEV)
+    layer.load_inputs(inp)
+    layer.step()
+    torch.cuda.synchronize()
+    R, h = layer.R, w.h
+    dh1 = torch.empty_like(layer.dh1); dh3 = torch.empty_like(layer.dh3)
+    u = lambda *s: torch.full(s, 0xEE, dtype=torch.uint8, device=DEV)  # noqa: E731
+    q1, s1, q3, s3 = u(R, h), u(R, h // 32), u(R, h), u(R, h // 32)
+    L.moe_reset_status(layer.ws)
+    L.moe_grouped_swiglu_bwd_dact_mxfp8(layer.offsets, layer.W2, layer.h1, layer.h3, layer.dyp,
+                                        dh1, dh3, q1, s1, q3, s3, layer.ws)
+    torch.cuda.synchronize()
+    assert L.moe_get_status(layer.ws) == 0
+    assert torch.equal(dh1, layer.dh1) and torch.equal(dh3, layer.dh3)
+    for q, sc, src in ((q1, s1, dh1), (q3, s3, dh3)):
+        rq, rs = om.quantize_blocks(as_f64(src), axis=1)
+        assert np.array_equal(u8(q), rq) and np.array_equal(u8(sc), rs)

@@ -33,6 +33,7 @@
 // bounded: on timeout the kernel records MOE_DEV_WAIT_TIMEOUT, waits
 // (bounded) for its own in-flight copies and MMAs, frees TMEM and returns.
 #include "gemm_common.cuh"
+#include "mx_common.cuh"
 
 namespace moe {
 namespace {
@@ -60,6 +61,12 @@ struct GemmArgs {
   const uint16_t* in1;      // DA: h3
   int ldo;                  // row stride (elements) of the row-grouped outputs
   int* status;
+  // DA: when set, dh1 / dh3 also leave quantised along h for the MXFP8 dgrad
+  // (E4M3 codes [R][h], E8M0 scales [R][h/32]; the blocks of the stored bf16)
+  uint8_t* q0;
+  uint8_t* q1;
+  uint8_t* qs0;
+  uint8_t* qs1;
   int wg_t1, wg_t2;         // WG: tiles per expert of dW1 (= dW3) and of dW2
   int wg_mt1, wg_mt2;       // WG: M tiles of dW1 and dW2
   const CUtensorMap* wg_maps;  // WG: [E][5] descriptors of xp, a, dh1, dh3, dyp
@@ -145,6 +152,31 @@ __device__ __forceinline__ void issue_loads(const Tile& tl, int kb, uint32_t sa,
 struct OutMaps {
   const CUtensorMap *o0, *o1, *o2;
 };
+
+// DA with quantised outputs: this lane's row of a 32-column chunk, packed in
+// bf16 (o), as one MXFP8 block: 32 E4M3 codes to q, the E8M0 byte to *s.  The
+// block is the stored bf16 values, so the codes equal a separate quantising
+// pass over dh1 / dh3 (moe_mxfp8_quantize_rows).
+__device__ __forceinline__ void quantize_chunk_row(const uint4 (&o)[4], uint8_t* q, uint8_t* s) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(o);
+  float v[32];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+  }
+  const int e = mx::block_exponent(amax);
+  const float inv = mx::inv_scale(e);
+  uint4 c[2];
+  uint32_t* cw = reinterpret_cast<uint32_t*>(c);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) cw[i] = mx::e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+  st_v4(q, c[0]);
+  st_v4(q + 16, c[1]);
+  *s = (uint8_t)(e + 127);
+}
 
 // Epilogue of one tile for the 32 rows of this warp's TMEM lane quarter and
 // the half `half` of the tile's columns (two warps share a lane quarter).
@@ -253,6 +285,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile& tl, uint32_t tacc, int
           store_chunk(stg, g1, lane, a.out0 + r0 * a.ldo + col, a.ldo, nrows);
           store_chunk(stg, reinterpret_cast<const float*>(q), lane, a.out1 + r0 * a.ldo + col,
                       a.ldo, nrows);
+          if (a.q0 != nullptr && lane < nrows) {
+            uint4 o1[4], o3[4];
+            pack_row32(g1, o1);
+            pack_row32(reinterpret_cast<const float*>(q), o3);
+            const size_t rq = (r0 + lane) * (size_t)a.h + col, rs = (r0 + lane) * (size_t)(a.h / 32) + col / 32;
+            quantize_chunk_row(o1, a.q0 + rq, a.qs0 + rs);
+            quantize_chunk_row(o3, a.q1 + rq, a.qs1 + rs);
+          }
         }
       }
     } else {  // kDown, kDX: plain bf16 store of the accumulator
@@ -633,6 +673,11 @@ __device__ __forceinline__ bool epilogue_da_ring(const Tile& tl, uint32_t tacc, 
           st_v4(d1 + 8 * i, o1[i]);
           st_v4(d3 + 8 * i, o3[i]);
         }
+      }
+      if (a.q0 != nullptr && lane < nrows) {
+        const size_t rq = (size_t)(r0 + lane) * a.h + col, rs = (size_t)(r0 + lane) * (a.h / 32) + col / 32;
+        quantize_chunk_row(o1, a.q0 + rq, a.qs0 + rs);
+        quantize_chunk_row(o3, a.q1 + rq, a.qs1 + rs);
       }
     }
     if (lane == 0) {
@@ -1191,9 +1236,14 @@ int run_down(const moe_bf16_t* a, const int32_t* offsets, int R, int E, int d, i
 // dA = dyp_e @ W2[e]^T with the SwiGLU backward epilogue -> dh1, dh3
 int run_dact(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_t* W2,
              const moe_bf16_t* h1, const moe_bf16_t* h3, const moe_bf16_t* dyp, moe_bf16_t* dh1,
-             moe_bf16_t* dh3, void* ws, cudaStream_t s) {
+             moe_bf16_t* dh3, void* ws, cudaStream_t s, uint8_t* dh1q = nullptr,
+             uint8_t* dh1s = nullptr, uint8_t* dh3q = nullptr, uint8_t* dh3s = nullptr) {
   MOE_CHECK_PTR(offsets); MOE_CHECK_PTR(W2); MOE_CHECK_PTR(h1); MOE_CHECK_PTR(h3);
   MOE_CHECK_PTR(dyp); MOE_CHECK_PTR(dh1); MOE_CHECK_PTR(dh3);
+  if (dh1q != nullptr) {
+    MOE_CHECK_PTR(dh1q); MOE_CHECK_PTR(dh3q);
+    if (dh1s == nullptr || dh3s == nullptr) return MOE_ERR_INVALID_ARG;
+  }
   const bool pairs = rows_on_pairs(R, E) && E <= pair_max_experts<kDA>();
   CUtensorMap m_dyp, m_w2k;
   if (!map2d(&m_dyp, dyp, d, R, 64, BM) || !map3d(&m_w2k, W2, d, h, E, 64, pairs ? BN / 2 : BN))
@@ -1202,6 +1252,7 @@ int run_dact(const int32_t* offsets, int R, int E, int d, int h, const moe_bf16_
   g.n_tiles = (h + BN - 1) / BN;
   g.kb_total = d / BK;
   g.out0 = dh1; g.out1 = dh3; g.in0 = h1; g.in1 = h3; g.ldo = h;
+  g.q0 = dh1q; g.q1 = dh3q; g.qs0 = dh1s; g.qs1 = dh3s;
   OutDescs o;   // TMA stores on pairs; the single-CTA kernel stores without them
   if (!row_outs(&o, R, h, dh1, dh3)) return MOE_ERR_CUDA;
   if (pairs) {
@@ -1371,6 +1422,17 @@ int moe_grouped_swiglu_bwd_dact(const int32_t* offsets, int R, int E, int d, int
   MOE_GEMM_PROLOGUE();
   if (R == 0) return MOE_OK;
   return run_dact(offsets, R, E, d, h, W2, h1, h3, dyp, dh1, dh3, ws, s);
+}
+
+int moe_grouped_swiglu_bwd_dact_mxfp8(const int32_t* offsets, int R, int E, int d, int h,
+                                      const moe_bf16_t* W2, const moe_bf16_t* h1, const moe_bf16_t* h3,
+                                      const moe_bf16_t* dyp, moe_bf16_t* dh1, moe_bf16_t* dh3,
+                                      uint8_t* dh1q, uint8_t* dh1s, uint8_t* dh3q, uint8_t* dh3s, void* ws,
+                                      size_t ws_bytes, moe_stream_t stream) {
+  MOE_GEMM_PROLOGUE();
+  if (R == 0) return MOE_OK;
+  if (dh1q == nullptr) return MOE_ERR_INVALID_ARG;
+  return run_dact(offsets, R, E, d, h, W2, h1, h3, dyp, dh1, dh3, ws, s, dh1q, dh1s, dh3q, dh3s);
 }
 
 int moe_grouped_swiglu_bwd_dx(const int32_t* offsets, int R, int E, int d, int h,

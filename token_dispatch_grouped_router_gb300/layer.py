@@ -196,13 +196,16 @@ class MoELayer:
             L.moe_combine_bwd(self.dY, self.yp, self.row_of_slot, self.gate, self.k,
                               self.dyp, self.dgate)
         mark("gemm_dact")
-        L.moe_grouped_swiglu_bwd_dact(self.offsets, self.W2, self.h1, self.h3, self.dyp,
-                                      self.dh1, self.dh3, self.ws)
         if getattr(self, "mx_dgrad", False):
-            # dh1, dh3 quantised along h, then the block-scaled dgrad GEMM
-            mark("mx_quantize_dh")
-            L.moe_mxfp8_quantize_rows(self.dh1, self.dh1q, self.dh1s)
-            L.moe_mxfp8_quantize_rows(self.dh3, self.dh3q, self.dh3s)
+            # dh1, dh3 also leave quantised along h for the MXFP8 dgrad
+            L.moe_grouped_swiglu_bwd_dact_mxfp8(self.offsets, self.W2, self.h1, self.h3, self.dyp,
+                                                self.dh1, self.dh3, self.dh1q, self.dh1s,
+                                                self.dh3q, self.dh3s, self.ws)
+        else:
+            L.moe_grouped_swiglu_bwd_dact(self.offsets, self.W2, self.h1, self.h3, self.dyp,
+                                          self.dh1, self.dh3, self.ws)
+        if getattr(self, "mx_dgrad", False):
+            # the block-scaled dgrad GEMM on the dact epilogue's quantised dh1, dh3
             mark("gemm_dx_mxfp8")
             L.moe_grouped_swiglu_bwd_dx_mxfp8(self.dh1q, self.dh1s, self.dh3q, self.dh3s,
                                               self.offsets, self.w1q_h, self.w3q_h,

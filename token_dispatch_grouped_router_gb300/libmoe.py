@@ -56,6 +56,8 @@ SIGNATURES = {
     "moe_dispatch_rows_mxfp8": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_mxfp8_weight_atom_bytes": (_Z, [_I, _I, _I]),
     "moe_mxfp8_dx_weight_atom_bytes": (_Z, [_I, _I, _I]),
+    "moe_grouped_swiglu_bwd_dact_mxfp8": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                               _P, _P, _P, _P, _Z, _P]),
     "moe_mxfp8_dx_weight_scale_atoms": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_grouped_swiglu_bwd_dx_mxfp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                              _P, _Z, _P]),
@@ -519,3 +521,19 @@ def moe_grouped_swiglu_bwd_dx_mxfp8(dh1q, dh1s, dh3q, dh3s, offsets, w1q_h, w3q_
     _ok("moe_grouped_swiglu_bwd_dx_mxfp8", load().moe_grouped_swiglu_bwd_dx_mxfp8(
         _ptr(dh1q), _ptr(dh1s), _ptr(dh3q), _ptr(dh3s), _ptr(offsets), R, E, d, h, _ptr(w1q_h),
         _ptr(w3q_h), _ptr(dx_atoms), _ptr(dxp), _ptr(ws), _wsb(ws), _stream()))
+
+
+def moe_grouped_swiglu_bwd_dact_mxfp8(offsets, W2, h1, h3, dyp, dh1, dh3, dh1q, dh1s, dh3q, dh3s,
+                                      ws) -> None:
+    """moe_grouped_swiglu_bwd_dact that also writes dh1 / dh3 quantised along h."""
+    R, d = dyp.shape
+    E, h, _ = W2.shape
+    for n, t in (("h1", h1), ("h3", h3), ("dh1", dh1), ("dh3", dh3)):
+        _want(t, torch.bfloat16, (R, h), n)
+    for n, t in (("dh1q", dh1q), ("dh3q", dh3q)):
+        _want(t, torch.uint8, (R, h), n)
+    for n, t in (("dh1s", dh1s), ("dh3s", dh3s)):
+        _want(t, torch.uint8, (R, h // 32), n)
+    _ok("moe_grouped_swiglu_bwd_dact_mxfp8", load().moe_grouped_swiglu_bwd_dact_mxfp8(
+        _ptr(offsets), R, E, d, h, _ptr(W2), _ptr(h1), _ptr(h3), _ptr(dyp), _ptr(dh1), _ptr(dh3),
+        _ptr(dh1q), _ptr(dh1s), _ptr(dh3q), _ptr(dh3s), _ptr(ws), _wsb(ws), _stream()))
