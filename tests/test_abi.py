@@ -202,3 +202,19 @@ def test_mxfp8_atom_and_dgrad_calls_check_arguments_on_the_host(lib):
     # R = 0 launches nothing
     assert lib.moe_grouped_swiglu_bwd_dx_mxfp8(*args(0, 2, 128, 128, fake, big)) == 0
     assert lib.moe_launch_count() == before
+
+
+def test_the_header_alone_serves_a_c_program(lib, tmp_path):
+    # a plain C caller: compiled with gcc against include/libmoe.h, linked to
+    # libmoe.so, host-side calls only (no CUDA call is reached)
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c_abi", "host_checks.c")
+    exe = str(tmp_path / "host_checks")
+    libdir = os.path.dirname(LM.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), src, "-o", exe,
+                    "-L", libdir, "-lmoe", "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
