@@ -53,28 +53,38 @@ enum Mode8 : int { kUp8 = 0, kDown8 = 1, kDx8 = 2 };
 
 constexpr int BN = 192, BK = 128;               // MMA N, k-block (fp8 bytes)
 constexpr int A_STAGE = 128 * BK;               // 16 KB: one CTA's 128 A rows
-constexpr int SF_STAGE = 3 * mx::kAtomBytes;    // A atom + two B atoms
+constexpr int SF_STAGE = 3 * mx::kAtomBytes;    // a k-block's A atom + two B atoms
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts8 = 768;               // shared-memory tile table bound
 constexpr int kThreads8 = kThreads + 32;        // + the scale-copy warp
 
-// Per form: rows a tile covers, B rows a CTA stages, pipeline stages, and the
-// tensor-memory columns of the second accumulator and of stage s's scales
-// (A at sf_col(s), B at sf_col(s) + 4, 12 columns a stage).
+// Per form: rows a tile covers, B rows a CTA stages, pipeline stages, k-blocks
+// a stage holds (KPS), and the tensor-memory columns of the second
+// accumulator and of stage s's scales (k-block j of the stage: A at
+// sf_col(s) + 12j, B at sf_col(s) + 12j + 4; 12 columns a k-block).
+// A stage is one barrier wait and one commit on the MMA lane.  Each of those
+// takes the issuing thread off the tensor pipe for about a short MMA's time
+// (measured on the GB300 with operands resident: a pair loop with one wait
+// and two commits per 4-MMA k-block issues at 0.57 of the fp8 rate, with one
+// wait and one commit per 8 MMAs at 0.92), so the pair form stages two
+// k-blocks at a time.
 template <bool PAIR> struct Form;
 template <> struct Form<false> {
-  static constexpr int TM = 128, BROWS = 192, STAGES = 4;
+  static constexpr int TM = 128, BROWS = 192, STAGES = 4, KPS = 1;
   __device__ static uint32_t acc_col(int acc) { return (uint32_t)acc * 256; }
   __device__ static uint32_t sf_col(int s) { return 448 + 12 * s; }
 };
 template <> struct Form<true> {
-  static constexpr int TM = 256, BROWS = 96, STAGES = 6;
+  static constexpr int TM = 256, BROWS = 96, STAGES = 3, KPS = 2;
   __device__ static uint32_t acc_col(int acc) { return (uint32_t)acc * 256; }
-  // the 64 columns after each 192-column accumulator hold five stages' scales
-  __device__ static uint32_t sf_col(int s) { return s < 5 ? 192 + 12 * s : 448 + 12 * (s - 5); }
+  // the 64 columns after each 192-column accumulator hold the three stages'
+  // 24 scale columns (two after the first, one after the second)
+  __device__ static uint32_t sf_col(int s) { return s == 0 ? 192u : s == 1 ? 216u : 448u; }
 };
 template <bool PAIR> constexpr int b_stage() { return Form<PAIR>::BROWS * BK; }
-template <bool PAIR> constexpr int stage_bytes() { return A_STAGE + b_stage<PAIR>() + SF_STAGE; }
+// one k-block's slot; a stage holds KPS consecutive slots of each operand
+template <bool PAIR> constexpr int slot_bytes() { return A_STAGE + b_stage<PAIR>() + SF_STAGE; }
+template <bool PAIR> constexpr int stage_bytes() { return Form<PAIR>::KPS * slot_bytes<PAIR>(); }
 
 struct Args8 {
   const int32_t* offsets;
@@ -225,16 +235,17 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                      const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
                      const Args8 args) {
   using F = Form<PAIR>;
-  constexpr int S = F::STAGES, TM = F::TM;
+  constexpr int S = F::STAGES, TM = F::TM, KPS = F::KPS;
   constexpr int B_STAGE = b_stage<PAIR>();
   using Shared = PipeShared<S>;
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // S * KPS k-block slots of each: A (16 KB), B, scale atoms (1.5 KB)
   uint8_t* sA = smem;
-  uint8_t* sB = sA + S * A_STAGE;
-  uint8_t* sSF = sB + S * B_STAGE;                           // S x 1.5 KB
-  uint8_t* sStage = sSF + S * SF_STAGE;                      // kEpiWarps x kStageBytes
+  uint8_t* sB = sA + S * KPS * A_STAGE;
+  uint8_t* sSF = sB + S * KPS * B_STAGE;
+  uint8_t* sStage = sSF + S * KPS * SF_STAGE;                // kEpiWarps x kStageBytes
   Shared* sh = reinterpret_cast<Shared*>(sStage + kEpiWarps * kStageBytes);
   uint64_t* sfull = reinterpret_cast<uint64_t*>(sh + 1);      // [S] scales in TMEM, [S] copy drain
   int* s_off = reinterpret_cast<int*>(sfull + S + 1);
@@ -300,43 +311,55 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       const int e_off = max(0, min(s_off[rt.e], args.R));
       const int blk = mx::act_block0(e_off, rt.e) + (rt.row0 - e_off) / 128 + (int)rank;
       const int wat = (rt.e * args.n_tiles + rt.n_idx) * KB;
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb0 = 0; kb0 < KB; kb0 += KPS) {
+        const int nk = min(KPS, KB - kb0);
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t fb_local = smem_u32(&sh->full[stage]);
-          const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
-          const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
           const int arow = rt.row0 + 128 * (int)rank;
-          // DX8 reduces over [dh1 | dh3] x [W1 | W3]: the second pair of maps
-          // from k-block kb_split on
-          const bool second = MODE == kDx8 && kb >= args.kb_split;
-          const int kx = (second ? kb - args.kb_split : kb) * BK;
-          const CUtensorMap* ma = second ? &tmA1 : &tmA;
-          const CUtensorMap* mb = second ? &tmB1 : &tmB0;
+          // the scale atoms of a stage's k-blocks are adjacent in HBM: one copy
+          // of KPS A atoms and one of 2 * KPS B atoms (a copy past the end of a
+          // tile's k-blocks reads atoms it does not use, zeros past the table)
+          const uint32_t ssa = smem_u32(sSF + stage * KPS * SF_STAGE);
+          const uint32_t ssb = ssa + KPS * mx::kAtomBytes;
           if constexpr (PAIR) {
+            if (leader) mbar_arrive_expect_tx(fb_local, 2 * (nk * (A_STAGE + B_STAGE) + KPS * SF_STAGE));
             const uint32_t fb = mapa_shared(fb_local, 0);
-            if (leader) mbar_arrive_expect_tx(fb_local, 2 * (A_STAGE + B_STAGE + SF_STAGE));
-            tma_load_2d_pair(sa, ma, fb, kx, arow);
-            if constexpr (MODE == kUp8) {
-              // the even CTA stages the 96 W1 rows, the odd CTA the same W3 rows
-              tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, fb, kx, n0, rt.e);
-            } else {
-              tma_load_3d_pair(sb, mb, fb, kx, n0 + 96 * (int)rank, rt.e);
-            }
-            tma_load_2d_pair(ss, &tmSA, fb, 0, blk * KB + kb);
-            tma_load_2d_pair(ss + mx::kAtomBytes, &tmSB, fb, 0, (wat + kb) * 2);
+            tma_load_2d_pair(ssa, &tmSA, fb, 0, blk * KB + kb0);
+            tma_load_2d_pair(ssb, &tmSB, fb, 0, (wat + kb0) * 2);
           } else {
-            mbar_arrive_expect_tx(fb_local, A_STAGE + B_STAGE + SF_STAGE);
-            tma_load_2d(sa, ma, fb_local, kx, arow);
-            if constexpr (MODE == kUp8) {
-              // 96 rows of W1 then the same 96 rows of W3
-              tma_load_3d(sb, &tmB0, fb_local, kx, n0, rt.e);
-              tma_load_3d(sb + 96 * BK, &tmB1, fb_local, kx, n0, rt.e);
+            mbar_arrive_expect_tx(fb_local, nk * (A_STAGE + B_STAGE) + KPS * SF_STAGE);
+            tma_load_2d(ssa, &tmSA, fb_local, 0, blk * KB + kb0);
+            tma_load_2d(ssb, &tmSB, fb_local, 0, (wat + kb0) * 2);
+          }
+          for (int j = 0; j < nk; ++j) {
+            const int kb = kb0 + j, q = stage * KPS + j;
+            const uint32_t sa = smem_u32(sA + q * A_STAGE), sb = smem_u32(sB + q * B_STAGE);
+            // DX8 reduces over [dh1 | dh3] x [W1 | W3]: the second pair of maps
+            // from k-block kb_split on
+            const bool second = MODE == kDx8 && kb >= args.kb_split;
+            const int kx = (second ? kb - args.kb_split : kb) * BK;
+            const CUtensorMap* ma = second ? &tmA1 : &tmA;
+            const CUtensorMap* mb = second ? &tmB1 : &tmB0;
+            if constexpr (PAIR) {
+              const uint32_t fb = mapa_shared(fb_local, 0);
+              tma_load_2d_pair(sa, ma, fb, kx, arow);
+              if constexpr (MODE == kUp8) {
+                // the even CTA stages the 96 W1 rows, the odd CTA the same W3 rows
+                tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, fb, kx, n0, rt.e);
+              } else {
+                tma_load_3d_pair(sb, mb, fb, kx, n0 + 96 * (int)rank, rt.e);
+              }
             } else {
-              tma_load_3d(sb, mb, fb_local, kx, n0, rt.e);
+              tma_load_2d(sa, ma, fb_local, kx, arow);
+              if constexpr (MODE == kUp8) {
+                // 96 rows of W1 then the same 96 rows of W3
+                tma_load_3d(sb, &tmB0, fb_local, kx, n0, rt.e);
+                tma_load_3d(sb + 96 * BK, &tmB1, fb_local, kx, n0, rt.e);
+              } else {
+                tma_load_3d(sb, mb, fb_local, kx, n0, rt.e);
+              }
             }
-            tma_load_2d(ss, &tmSA, fb_local, 0, blk * KB + kb);
-            tma_load_2d(ss + mx::kAtomBytes, &tmSB, fb_local, 0, (wat + kb) * 2);
           }
         }
         __syncwarp();
@@ -361,24 +384,29 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         if (!bounded_wait(smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dt = tmem + F::acc_col(acc);
-        for (int kb = 0; kb < KB; ++kb) {
-          // the stage's scales are in tensor memory (and so its operands have landed)
-          if (!bounded_wait(smem_u32(&sfull[stage]), phase, &sh->abort_flag, args.status) ||
-              !bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+        for (int kb0 = 0; kb0 < KB; kb0 += KPS) {
+          const int nk = min(KPS, KB - kb0);
+          // The stage's scales are in tensor memory.  Their copies were issued
+          // after the scale-copy warp saw the stage's full barrier complete, so
+          // the stage's operands have landed as well: one wait is enough.
+          if (!bounded_wait(smem_u32(&sfull[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t sfa_t = tmem + F::sf_col(stage), sfb_t = sfa_t + 4;
-            const uint32_t sa = smem_u32(sA + stage * A_STAGE), sb = smem_u32(sB + stage * B_STAGE);
+            for (int j = 0; j < nk; ++j) {
+              const int q = stage * KPS + j;
+              const uint32_t sfa_t = tmem + F::sf_col(stage) + 12 * j, sfb_t = sfa_t + 4;
+              const uint32_t sa = smem_u32(sA + q * A_STAGE), sb = smem_u32(sB + q * B_STAGE);
 #pragma unroll
-            for (int kk = 0; kk < BK / 32; ++kk) {
-              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-              const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-              if constexpr (PAIR) mma_mxf8_pair(dt, ad, bd, idesc_mxf8(256, BN, kk), sfa_t, sfb_t, accum);
-              else mma_mxf8(dt, ad, bd, idesc_mxf8(128, BN, kk), sfa_t, sfb_t, accum);
+              for (int kk = 0; kk < BK / 32; ++kk) {
+                const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+                const uint32_t accum = (kb0 + j > 0 || kk > 0) ? 1u : 0u;
+                if constexpr (PAIR) mma_mxf8_pair(dt, ad, bd, idesc_mxf8(256, BN, kk), sfa_t, sfb_t, accum);
+                else mma_mxf8(dt, ad, bd, idesc_mxf8(128, BN, kk), sfa_t, sfb_t, accum);
+              }
             }
             const uint32_t eb = smem_u32(&sh->empty[stage]);
-            if constexpr (PAIR) { mma_commit_pair(mapa_shared(eb, 0)); mma_commit_pair(mapa_shared(eb, 1)); }
+            if constexpr (PAIR) mma_commit_pair_both(eb);
             else mma_commit(eb);
           }
           issued_any = true;
@@ -388,7 +416,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         if (!ok) break;
         if (lane == 0) {
           const uint32_t tf = smem_u32(&sh->tfull[acc]);
-          if constexpr (PAIR) { mma_commit_pair(mapa_shared(tf, 0)); mma_commit_pair(mapa_shared(tf, 1)); }
+          if constexpr (PAIR) mma_commit_pair_both(tf);
           else mma_commit(tf);
         }
         __syncwarp();
@@ -439,24 +467,29 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     bool issued = false;
     for (int t = unit; t < total; t += nunits) {
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb0 = 0; kb0 < KB; kb0 += KPS) {
+        const int nk = min(KPS, KB - kb0);
         if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sfa_t = tmem + F::sf_col(stage), sfb_t = sfa_t + 4;
-          const uint32_t ss = smem_u32(sSF + stage * SF_STAGE);
-          const uint32_t sb = smem_u32(&sfull[stage]);
-          if constexpr (PAIR) {
-            tmem_cp_warpx4_pair(sfa_t, sdesc_atom(ss));
-            tmem_cp_warpx4_pair(sfb_t, sdesc_atom(ss + 512));        // B columns 0..127
-            tmem_cp_warpx4_pair(sfb_t + 4, sdesc_atom(ss + 1024));   // B columns 128..191
-            mma_commit_pair(mapa_shared(sb, 0));
-          } else {
-            tmem_cp_warpx4(sfa_t, sdesc_atom(ss));
-            tmem_cp_warpx4(sfb_t, sdesc_atom(ss + 512));
-            tmem_cp_warpx4(sfb_t + 4, sdesc_atom(ss + 1024));
-            mma_commit(sb);
+          for (int j = 0; j < nk; ++j) {
+            const uint32_t sfa_t = tmem + F::sf_col(stage) + 12 * j, sfb_t = sfa_t + 4;
+            // the stage's A atoms, then its B atoms (two a k-block)
+            const uint32_t ssa = smem_u32(sSF + stage * KPS * SF_STAGE) + j * mx::kAtomBytes;
+            const uint32_t ssb = smem_u32(sSF + stage * KPS * SF_STAGE) + (KPS + 2 * j) * mx::kAtomBytes;
+            if constexpr (PAIR) {
+              tmem_cp_warpx4_pair(sfa_t, sdesc_atom(ssa));
+              tmem_cp_warpx4_pair(sfb_t, sdesc_atom(ssb));             // B columns 0..127
+              tmem_cp_warpx4_pair(sfb_t + 4, sdesc_atom(ssb + 512));   // B columns 128..191
+            } else {
+              tmem_cp_warpx4(sfa_t, sdesc_atom(ssa));
+              tmem_cp_warpx4(sfb_t, sdesc_atom(ssb));
+              tmem_cp_warpx4(sfb_t + 4, sdesc_atom(ssb + 512));
+            }
           }
+          const uint32_t sb = smem_u32(&sfull[stage]);
+          if constexpr (PAIR) mma_commit_pair(mapa_shared(sb, 0));
+          else mma_commit(sb);
         }
         issued = true;
         __syncwarp();
@@ -657,13 +690,14 @@ extern "C" int moe_grouped_swiglu_fwd_mxfp8(
   const int TM = pair ? 256 : 128;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint32_t brows = pair ? 96 : 192;
+  const uint32_t kps = pair ? Form<true>::KPS : Form<false>::KPS;
   Maps8 mu{}, md{};
   if (!map2d(&mu.a, xq, d, R, BK, 128, U8, 1) || !map2d(&mu.a1, xq, d, R, BK, 128, U8, 1) ||
       !map3d(&mu.b0, w1q, d, h, E, BK, 96, U8, 1) ||
-      !map3d(&mu.b1, w3q, d, h, E, BK, 96, U8, 1) || !map_atoms(&mu.sa, xatoms, nbx, 1) ||
-      !map_atoms(&mu.sb, up_atoms, n_up_atoms, 2) ||
+      !map3d(&mu.b1, w3q, d, h, E, BK, 96, U8, 1) || !map_atoms(&mu.sa, xatoms, nbx, kps) ||
+      !map_atoms(&mu.sb, up_atoms, n_up_atoms, 2 * kps) ||
       !map2d(&md.a, aq, h, R, BK, 128, U8, 1) || !map3d(&md.b0, w2q, h, d, E, BK, brows, U8, 1) ||
-      !map_atoms(&md.sa, aatoms, nba, 1) || !map_atoms(&md.sb, dn_atoms, n_dn_atoms, 2))
+      !map_atoms(&md.sa, aatoms, nba, kps) || !map_atoms(&md.sb, dn_atoms, n_dn_atoms, 2 * kps))
     return MOE_ERR_CUDA;
   md.b1 = md.b0; md.a1 = md.a;
   if (!map2d_out(&mu.o0, h1, h, R, h) || !map2d_out(&mu.o1, h3, h, R, h) ||
@@ -736,10 +770,11 @@ extern "C" int moe_grouped_swiglu_bwd_dx_mxfp8(
   const int TM = pair ? 256 : 128;
   const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint32_t brows = pair ? 96 : 192;
+  const uint32_t kps = pair ? Form<true>::KPS : Form<false>::KPS;
   Maps8 m{};
   if (!map2d(&m.a, dh1q, h, R, BK, 128, U8, 1) || !map2d(&m.a1, dh3q, h, R, BK, 128, U8, 1) ||
       !map3d(&m.b0, w1q_h, h, d, E, BK, brows, U8, 1) || !map3d(&m.b1, w3q_h, h, d, E, BK, brows, U8, 1) ||
-      !map_atoms(&m.sa, atoms, nba, 1) || !map_atoms(&m.sb, dx_atoms, n_w_atoms, 2) ||
+      !map_atoms(&m.sa, atoms, nba, kps) || !map_atoms(&m.sb, dx_atoms, n_w_atoms, 2 * kps) ||
       !map2d_out(&m.o0, dxp, d, R, d))
     return MOE_ERR_CUDA;
   m.o1 = m.o0; m.o2 = m.o0;

@@ -507,7 +507,16 @@ constexpr int P_TILE = 256;
 constexpr int kRingSlots = 4;
 constexpr int kRingChunk = 128 * 32 * 2;              // 8 KB
 constexpr int kRingSlotBytes = 2 * kRingChunk;
-template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_STAGES; }
+// A stage is one barrier wait and one commit on the MMA lane, each of which
+// keeps the issuing thread off the tensor pipe for about a short MMA's time
+// (measured on the GB300 with operands resident: a pair loop with one wait and
+// two commits per 4-MMA k-block issues at 0.88 of the bf16 rate, with one of
+// each per 8 MMAs at the full rate), so the pair GEMMs stage two k-blocks at
+// a time: 3 stages of 2 k-block slots.  DA keeps 5 one-k-block stages next to
+// its h1/h3 ring.
+template <int MODE> __host__ __device__ constexpr int pair_kps() { return MODE == kDA ? 1 : 2; }
+template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_STAGES / 2; }
+template <int MODE> __host__ __device__ constexpr int pair_slots() { return pair_stages<MODE>() * pair_kps<MODE>(); }
 template <int MODE> __host__ __device__ constexpr int pair_ring_bytes() { return MODE == kDA ? kRingSlots * kRingSlotBytes : 0; }
 template <int MODE> __host__ __device__ constexpr int pair_stage_bytes() { return MODE == kDA ? 0 : kEpiWarps * kStageBytes; }
 // WG: a 32 x 32 bf16 box of zeros, the source of every store of an empty expert's dW tiles
@@ -767,10 +776,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  constexpr int PS = pair_stages<MODE>();
+  constexpr int PS = pair_stages<MODE>(), KPS = pair_kps<MODE>();
   using PairShared = PairSharedT<MODE>;
-  uint8_t* sB = smem + PS * P_HALF;
-  uint8_t* ring = sB + PS * P_HALF;                          // DA only
+  // PS * KPS k-block slots of A, then of B (slot q = stage * KPS + j)
+  uint8_t* sB = smem + PS * KPS * P_HALF;
+  uint8_t* ring = sB + PS * KPS * P_HALF;                    // DA only
   uint8_t* sStage = ring + pair_ring_bytes<MODE>();                 // not DA
   uint8_t* sZero = sStage + pair_stage_bytes<MODE>();               // WG only
   PairShared* sh = reinterpret_cast<PairShared*>(sZero + pair_zero_bytes<MODE>());
@@ -857,16 +867,19 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
           if (!(wg_seen & (1u << ob))) { tensormap_acquire(em + ob); wg_seen |= 1u << ob; }
         }
       }
-      for (int kb = 0; kb < tl.nkb; ++kb) {
+      for (int kb0 = 0; kb0 < tl.nkb; kb0 += KPS) {
+        const int nk = min(KPS, tl.nkb - kb0);
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t fb_local = smem_u32(&sh->full[stage]);
-          if (leader) mbar_arrive_expect_tx(fb_local, 4 * P_HALF);   // both CTAs' copies
-          int kbr = kb;
-          if constexpr (MODE == kWG) kbr = wg_kblock(tl, t, pair, npairs, kb);
-          issue_loads_pair<MODE>(tl, kbr, rank, smem_u32(sA + stage * P_HALF),
-                                 smem_u32(sB + stage * P_HALF), mapa_shared(fb_local, 0), &tmA0,
-                                 &tmA1, &tmB0, &tmB1, args);
+          if (leader) mbar_arrive_expect_tx(fb_local, nk * 4 * P_HALF);   // both CTAs' copies
+          for (int j = 0; j < nk; ++j) {
+            int kbr = kb0 + j;
+            if constexpr (MODE == kWG) kbr = wg_kblock(tl, t, pair, npairs, kbr);
+            const int q = stage * KPS + j;
+            issue_loads_pair<MODE>(tl, kbr, rank, smem_u32(sA + q * P_HALF), smem_u32(sB + q * P_HALF),
+                                   mapa_shared(fb_local, 0), &tmA0, &tmA1, &tmB0, &tmB1, args);
+          }
         }
         __syncwarp();
         issued |= 1u << stage;
@@ -901,31 +914,33 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
           if (lane == 0) { mbar_arrive_cluster(mapa_shared(tf, 0)); mbar_arrive_cluster(mapa_shared(tf, 1)); }
         } else {
           const uint32_t dt = tmem + (uint32_t)(acc * P_TILE);
-          for (int kb = 0; kb < tl.nkb; ++kb) {
-            int nkk = BK / 16;
-            if constexpr (MODE == kWG) nkk = wg_groups(tl, wg_kblock(tl, t, pair, npairs, kb));
+          for (int kb0 = 0; kb0 < tl.nkb; kb0 += KPS) {
+            const int nk = min(KPS, tl.nkb - kb0);
             if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
             tc_fence_after();
             if (lane == 0) {
-              const uint32_t sa = smem_u32(sA + stage * P_HALF), sb = smem_u32(sB + stage * P_HALF);
-              for (int kk = 0; kk < nkk; ++kk) {
-                uint64_t ad, bd;
-                if constexpr (a_mn) ad = sdesc_sw128(sa + kk * 2048, SUB, 1024);
-                else ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-                if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
-                else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-                mma_f16_pair(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              for (int j = 0; j < nk; ++j) {
+                const int kb = kb0 + j, q = stage * KPS + j;
+                int nkk = BK / 16;
+                if constexpr (MODE == kWG) nkk = wg_groups(tl, wg_kblock(tl, t, pair, npairs, kb));
+                const uint32_t sa = smem_u32(sA + q * P_HALF), sb = smem_u32(sB + q * P_HALF);
+                for (int kk = 0; kk < nkk; ++kk) {
+                  uint64_t ad, bd;
+                  if constexpr (a_mn) ad = sdesc_sw128(sa + kk * 2048, SUB, 1024);
+                  else ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+                  if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
+                  else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+                  mma_f16_pair(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                }
               }
-              const uint32_t eb = smem_u32(&sh->empty[stage]);
-              mma_commit_pair(mapa_shared(eb, 0));
-              mma_commit_pair(mapa_shared(eb, 1));
+              mma_commit_pair_both(smem_u32(&sh->empty[stage]));
             }
             issued_any = true;
             __syncwarp();
             if (++stage == PS) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          if (lane == 0) { mma_commit_pair(mapa_shared(tf, 0)); mma_commit_pair(mapa_shared(tf, 1)); }
+          if (lane == 0) mma_commit_pair_both(tf);
           __syncwarp();
         }
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
@@ -1073,7 +1088,7 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
 
 template <int MODE>
 constexpr size_t pair_smem_bytes(int E) {
-  return 1024 + (size_t)pair_stages<MODE>() * 2 * P_HALF + pair_ring_bytes<MODE>() +
+  return 1024 + (size_t)pair_slots<MODE>() * 2 * P_HALF + pair_ring_bytes<MODE>() +
          (size_t)pair_stage_bytes<MODE>() + pair_zero_bytes<MODE>() + sizeof(PairSharedT<MODE>) +
          2 * (size_t)(E + 1) * 4;
 }
@@ -1087,7 +1102,7 @@ constexpr int pair_max_experts() {
   return e < kMaxExperts ? (int)e : kMaxExperts;
 }
 static_assert(pair_max_experts<kUp>() == kMaxExperts && pair_max_experts<kWG>() == kMaxExperts,
-              "the 6-stage pair GEMMs fit every expert count");
+              "the 3-stage (6-slot) pair GEMMs fit every expert count");
 static_assert(pair_max_experts<kDA>() >= 128, "DA on pairs covers pools of 128 experts");
 
 // at[] must hold two attributes: the 2-CTA cluster shape and programmatic

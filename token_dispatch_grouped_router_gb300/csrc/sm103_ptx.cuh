@@ -261,6 +261,15 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t cluster_bar) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(cluster_bar)
       : "memory");
 }
+// the same, arriving on the mbarrier at this shared-memory offset in both
+// CTAs of the pair with one commit (a commit costs the tensor pipe about as
+// much as a short MMA, so one instead of two per stage)
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05 format), 128-byte swizzle:
 //   bits  0-13 start address >> 4
