@@ -43,7 +43,12 @@ using namespace gemm;
 
 enum Mode : int { kUp = 0, kDown = 1, kDA = 2, kDX = 3, kWG = 4 };
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
+// 4 k-block slots of A and B; a stage (one barrier wait and one commit on the
+// MMA lane) holds KPS1 of them.  Two k-blocks a stage leave this kernel only
+// two stages, and the lost latency cover costs more than the waits it saves
+// (measured: DX at T = 16384, E = 128 410 -> 449 us), so one.
+constexpr int SLOTS = 4, KPS1 = 1, STAGES = SLOTS / KPS1;
 constexpr int A_STAGE = BM * BK * 2;            // 16 KB
 constexpr int B_STAGE = BN * BK * 2;            // 32 KB
 constexpr int SUB = 64 * 64 * 2;                // one 64x64 bf16 TMA box (8 KB)
@@ -330,8 +335,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_STAGE;
-  uint8_t* sStage = sB + STAGES * B_STAGE;                   // kEpiWarps x kStageBytes
+  uint8_t* sB = smem + SLOTS * A_STAGE;
+  uint8_t* sStage = sB + SLOTS * B_STAGE;                    // kEpiWarps x kStageBytes
   Shared* sh = reinterpret_cast<Shared*>(sStage + kEpiWarps * kStageBytes);
   int* s_off = reinterpret_cast<int*>(sh + 1);
   int* s_ts = s_off + (args.E + 1);
@@ -382,13 +387,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<MODE>(t, args, s_off, s_ts);
-      for (int kb = 0; kb < tl.nkb; ++kb) {
+      for (int kb0 = 0; kb0 < tl.nkb; kb0 += KPS1) {
+        const int nk = min(KPS1, tl.nkb - kb0);
         if (!bounded_wait(smem_u32(&sh->empty[stage]), phase ^ 1u, &sh->abort_flag, args.status)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t fb = smem_u32(&sh->full[stage]);
-          mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
-          issue_loads<MODE>(tl, kb, smem_u32(sA + stage * A_STAGE), smem_u32(sB + stage * B_STAGE),
-                            fb, &tmA0, &tmA1, &tmB0, &tmB1, &tmB2, args);
+          mbar_arrive_expect_tx(fb, nk * (A_STAGE + B_STAGE));
+          for (int j = 0; j < nk; ++j) {
+            const int q = stage * KPS1 + j;
+            issue_loads<MODE>(tl, kb0 + j, smem_u32(sA + q * A_STAGE), smem_u32(sB + q * B_STAGE),
+                              fb, &tmA0, &tmA1, &tmB0, &tmB1, &tmB2, args);
+          }
         }
         __syncwarp();
         issued |= 1u << stage;
@@ -417,22 +426,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
       if (tl.nkb == 0) {
         if (lane == 0) mbar_arrive(smem_u32(&sh->tfull[acc]));
       } else {
-        for (int kb = 0; kb < tl.nkb; ++kb) {
+        for (int kb0 = 0; kb0 < tl.nkb; kb0 += KPS1) {
           constexpr int nkk = BK / 16;
+          const int nk = min(KPS1, tl.nkb - kb0);
           if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(sA + stage * A_STAGE);
-          const uint32_t sb = smem_u32(sB + stage * B_STAGE);
           if (lane == 0) {
-            for (int kk = 0; kk < nkk; ++kk) {
-              uint64_t bd;
-              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-              if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
-              else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-              mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int j = 0; j < nk; ++j) {
+              const int kb = kb0 + j, q = stage * KPS1 + j;
+              const uint32_t sa = smem_u32(sA + q * A_STAGE);
+              const uint32_t sb = smem_u32(sB + q * B_STAGE);
+              for (int kk = 0; kk < nkk; ++kk) {
+                uint64_t bd;
+                const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+                if constexpr (b_mn) bd = sdesc_sw128(sb + kk * 2048, SUB, 1024);
+                else bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+                mma_f16(dt, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             mma_commit(smem_u32(&sh->empty[stage]));
           }
@@ -513,7 +526,8 @@ constexpr int kRingSlotBytes = 2 * kRingChunk;
 // two commits per 4-MMA k-block issues at 0.88 of the bf16 rate, with one of
 // each per 8 MMAs at the full rate), so the pair GEMMs stage two k-blocks at
 // a time: 3 stages of 2 k-block slots.  DA keeps 5 one-k-block stages next to
-// its h1/h3 ring.
+// its h1/h3 ring (2 stages of 2 slots there: 203 -> 234 us at T = 16384,
+// E = 8).
 template <int MODE> __host__ __device__ constexpr int pair_kps() { return MODE == kDA ? 1 : 2; }
 template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_STAGES / 2; }
 template <int MODE> __host__ __device__ constexpr int pair_slots() { return pair_stages<MODE>() * pair_kps<MODE>(); }
@@ -1063,7 +1077,7 @@ wgrad_maps_kernel(const __grid_constant__ WgradTemplates tp, const int32_t* __re
 // ------------------------------------------------------------------ host side
 
 constexpr size_t smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)kEpiWarps * kStageBytes +
+  return 1024 + (size_t)SLOTS * (A_STAGE + B_STAGE) + (size_t)kEpiWarps * kStageBytes +
          sizeof(Shared) + 2 * (size_t)(E + 1) * 4;
 }
 
