@@ -1182,13 +1182,13 @@ int launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
 // UP, DOWN, DA and DX run on CTA pairs (256-row tiles) unless the experts are
 // small on average: then the 128-row tiles of the single-CTA kernel waste
 // less on each expert's last, partial tile.  DX (K = 2h, the longest
-// mainloop per tile) gains least from the pairs: with about 512 rows per
-// expert its single-CTA form is the faster one (event-timed on the GB300,
-// T = 16384, d = 2048, h = 1024, E = 128, top-4: 404 vs 417 us uniform,
-// 348 vs 357 us Zipf-skewed; at 1024 rows per expert 718 vs 718 us), so it
-// moves to pairs only from 1024 rows per expert.
+// mainloop per tile) gains least from the pairs; since the pair loop stages
+// two k-blocks per barrier it is no slower there at 512 rows per expert
+// (event-timed on the GB300, T = 16384, d = 2048, h = 1024, E = 128, top-4:
+// 402-410 vs 406-410 us uniform, 326-330 vs 351-353 us Zipf-skewed), so it
+// takes the same threshold.
 constexpr long long kPairMinRowsPerExpert = 512;
-constexpr long long kPairMinRowsPerExpertDX = 1024;
+constexpr long long kPairMinRowsPerExpertDX = 512;
 inline bool rows_on_pairs(int R, int E, long long min_rows = kPairMinRowsPerExpert) {
   return (long long)R >= min_rows * E;
 }
