@@ -43,8 +43,11 @@ constexpr int kMaxTopK = 8;
 //              moe_router_logits_bwd: dW_r split-K partials [splits][d][E] f32;
 //              moe_grouped_swiglu_bwd(_wgrad): per-expert TMA descriptors
 //                                  [E][5] x 128 B (needs a 128-byte aligned ws),
-//                                  then up to kWgradParts fp32 256 x 256
-//                                  partial tiles of the K-split last round.
+//                                  the tile plan (kWgradPlanHead int32 then
+//                                  the [E] order of the experts with rows and
+//                                  the [E] list of those without), then up to
+//                                  kWgradParts fp32 256 x 256 partial tiles of
+//                                  the K-split last round.
 constexpr size_t kStatusBytes = 256;
 constexpr int kRouteChunk = 1024;     // slots per route-map block
 constexpr int kRouterSplits = 16;     // deterministic split-K for dW_r
@@ -99,7 +102,13 @@ inline size_t router_scratch_end(int E, int d) {
 constexpr int kWgradMaps = 5;          // xp, a, dh1, dh3, dyp
 constexpr int kWgradParts = 80;        // fp32 256 x 256 partial tiles (20 MB)
 inline size_t wgrad_maps_end(int E) { return kStatusBytes + (size_t)E * kWgradMaps * 128; }
-inline size_t wgrad_parts_offset(int E) { return round_up(wgrad_maps_end(E), 256); }
+// the wgrad tile plan, written on the device from the offsets: head words
+// (non-empty experts, empty experts, whole units, K-split chunks, units,
+// zero tiles), then the order of the non-empty experts and the empty ones
+constexpr int kWgradPlanHead = 8;
+inline size_t wgrad_plan_offset(int E) { return round_up(wgrad_maps_end(E), 256); }
+inline size_t wgrad_plan_end(int E) { return wgrad_plan_offset(E) + (size_t)(kWgradPlanHead + 2 * E) * 4; }
+inline size_t wgrad_parts_offset(int E) { return round_up(wgrad_plan_end(E), 256); }
 inline size_t wgrad_parts_end(int E) {
   return wgrad_parts_offset(E) + (size_t)kWgradParts * 256 * 256 * 4;
 }

@@ -32,6 +32,7 @@ struct PipeShared {
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
+  int wg_whole, wg_split, wg_zero;   // CTA-pair wgrad: the device-built tile plan
 };
 
 // Wait for the phase `parity` of an mbarrier; give up after kWaitLimitNs (or

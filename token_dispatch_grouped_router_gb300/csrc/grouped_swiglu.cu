@@ -76,10 +76,12 @@ struct GemmArgs {
   int wg_mt1, wg_mt2;       // WG: M tiles of dW1 and dW2
   const CUtensorMap* wg_maps;  // WG: [E][5] descriptors of xp, a, dh1, dh3, dyp
                                //     whose row extent ends at the expert's last row
-  // WG on CTA pairs, K split of the last round: work units [0, wg_whole) are
-  // whole tiles; unit wg_whole + v is k-chunk v % wg_split of tile
-  // wg_whole + v / wg_split, accumulated in fp32 into wg_part[v] (256 x 256)
-  int wg_whole, wg_split, wg_units;
+  // WG on CTA pairs: the tile plan wgrad_maps_kernel writes from the offsets
+  // (head words, then the order of the experts with rows, deepest first, then
+  // the experts without rows).  Work unit u < whole is tile u of that order
+  // (per tiles an expert); unit whole + v is k-chunk v % split of tile
+  // whole + v / split, accumulated in fp32 into wg_part[v] (256 x 256).
+  const int* wg_plan;
   float* wg_part;
 };
 
@@ -114,14 +116,25 @@ __device__ __forceinline__ int wg_groups(const Tile& tl, int kb) {
   return valid >= BK ? BK / 16 : (valid + 15) >> 4;
 }
 
-// wgrad only: the k-block a pair processes at loop step kb of its tile t.
-// Every other deep tile of a pair (t = pair + i * npairs, i odd; 32 k-blocks
-// or more) runs its k-blocks from the last to the first, so a tile starts on
-// the expert rows its predecessor read last, which the L2 still holds:
-// dense_e8's wgrad reads 1128 instead of 1209 MB from DRAM, in the same time.
-// (Shallow tiles' rows fit in the L2 anyway; reversing them cost 0.5%.)
-__device__ __forceinline__ int wg_kblock(const Tile& tl, int t, int pair, int npairs, int kb) {
-  return (tl.nkb >= 32 && (((t - pair) / npairs) & 1)) ? tl.nkb - 1 - kb : kb;
+// wgrad only: the k-block a pair processes at loop step kb of its i-th unit.
+// Every other deep tile of a pair (i odd; 32 k-blocks or more) runs its
+// k-blocks from the last to the first, so a tile starts on the expert rows its
+// predecessor read last, which the L2 still holds: dense_e8's wgrad reads 1128
+// instead of 1209 MB from DRAM, in the same time.  (Shallow tiles' rows fit
+// in the L2 anyway; reversing them cost 0.5%.)
+__device__ __forceinline__ int wg_kblock(const Tile& tl, int i, int kb) {
+  return (tl.nkb >= 32 && (i & 1)) ? tl.nkb - 1 - kb : kb;
+}
+
+// The i-th work unit of a pair.  WG deals its units (deepest experts first)
+// in snake order, round i running over the pairs forwards when i is even and
+// backwards when odd, so every pair's sum of tile depths comes out nearly the
+// same (skew_e128: largest pair 1.03x the mean, against 1.18x round-robin in
+// expert order); the row-grouped modes deal round-robin.
+template <int MODE>
+__device__ __forceinline__ int pair_unit(int i, int pair, int npairs) {
+  if constexpr (MODE == kWG) return i * npairs + ((i & 1) ? npairs - 1 - pair : pair);
+  else return i * npairs + pair;
 }
 
 template <int MODE>
@@ -536,24 +549,28 @@ template <int MODE> __host__ __device__ constexpr int pair_stage_bytes() { retur
 // WG: a 32 x 32 bf16 box of zeros, the source of every store of an empty expert's dW tiles
 template <int MODE> __host__ __device__ constexpr int pair_zero_bytes() { return MODE == kWG ? 2048 : 0; }
 template <int MODE> using PairSharedT = PipeShared<pair_stages<MODE>()>;
-constexpr int kPairThreads = kThreads + 32;           // + DA's ring loader warp
+constexpr int kPairThreads = kThreads + 32;           // + DA's ring loader / WG's zero-tile warp
 
+// WG: s_ts holds the plan's expert order (deepest first) and wg = {whole,
+// split} its unit counts; the row-grouped modes ignore wg.
 template <int MODE>
 __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const int* s_off,
-                                                 const int* s_ts) {
+                                                 const int* s_ts, const int* wg = nullptr) {
   Tile tl{};
   tl.part = -1;
   if constexpr (MODE == kWG) {
+    const int whole = wg[0], split = wg[1];
     int chunk = 0;
-    if (a.wg_split > 0 && t >= a.wg_whole) {
-      const int v = t - a.wg_whole;
+    if (split > 0 && t >= whole) {
+      const int v = t - whole;
       tl.part = v;
-      chunk = v % a.wg_split;
-      t = a.wg_whole + v / a.wg_split;
+      chunk = v % split;
+      t = whole + v / split;
     }
     const int per = 2 * a.wg_t1 + a.wg_t2;
-    tl.e = t / per;
-    int l = t - tl.e * per;
+    const int rank = t / per;
+    tl.e = s_ts[rank];
+    int l = t - rank * per;
     int mt;
     if (l < a.wg_t1) { tl.which = 0; mt = a.wg_mt1; }
     else if (l < 2 * a.wg_t1) { tl.which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
@@ -568,7 +585,7 @@ __device__ __forceinline__ Tile decode_pair_tile(int t, const GemmArgs& a, const
     tl.nkb = (tl.krows + BK - 1) / BK;
     if (tl.part >= 0) {
       // k-blocks [kb0, kb1) of the expert's rows
-      const int kc = (tl.nkb + a.wg_split - 1) / a.wg_split;
+      const int kc = (tl.nkb + split - 1) / split;
       const int kb0 = min(tl.nkb, chunk * kc), kb1 = min(tl.nkb, kb0 + kc);
       tl.krow0 = lo + kb0 * BK;
       tl.krows = max(0, min(tl.krows - kb0 * BK, (kb1 - kb0) * BK));
@@ -758,26 +775,94 @@ __device__ __forceinline__ void epilogue_partial(const Tile& tl, uint32_t tacc, 
 }
 
 // Sum of the K-chunks of every split wgrad tile, in chunk order (so the
-// result does not depend on timing), rounded once to bf16.  Block = one row of
-// one split tile, thread = one column.
+// result does not depend on timing), rounded once to bf16.  The plan says how
+// many tiles were split (none: every block returns at once); block b takes
+// row b of the split tiles (and b + gridDim.x, ..), thread = one column.
 __global__ void __launch_bounds__(P_TILE) wgrad_fixup_kernel(const GemmArgs a) {
   pdl_enter();
-  const int i = blockIdx.x / P_TILE, r = blockIdx.x % P_TILE, col = threadIdx.x;
-  const int t = a.wg_whole + i;
+  const int* plan = a.wg_plan;
+  const int whole = plan[2], split = plan[3], units = plan[4];
+  if (split <= 0 || a.wg_part == nullptr) return;
+  const int L = (units - whole) / split;
   const int per = 2 * a.wg_t1 + a.wg_t2;
-  const int e = t / per;
-  int l = t - e * per, which, mt;
-  if (l < a.wg_t1) { which = 0; mt = a.wg_mt1; }
-  else if (l < 2 * a.wg_t1) { which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
-  else { which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
-  const int m = (l % mt) * P_TILE + r, n = (l / mt) * P_TILE + col;
-  const int M = which == 2 ? a.h : a.d, N = which == 2 ? a.d : a.h;
-  if (m >= M || n >= N) return;
-  const float* src = a.wg_part + (size_t)i * a.wg_split * (P_TILE * P_TILE) + (size_t)r * P_TILE + col;
-  float acc = 0.f;
-  for (int c = 0; c < a.wg_split; ++c) acc += src[(size_t)c * (P_TILE * P_TILE)];
-  uint16_t* out = which == 0 ? a.out0 : (which == 1 ? a.out1 : a.out2);
-  out[((size_t)e * M + m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+  const int col = threadIdx.x;
+  for (int b = blockIdx.x; b < L * P_TILE; b += gridDim.x) {
+    const int i = b / P_TILE, r = b % P_TILE;
+    const int t = whole + i;
+    const int e = plan[kWgradPlanHead + t / per];
+    int l = t % per, which, mt;
+    if (l < a.wg_t1) { which = 0; mt = a.wg_mt1; }
+    else if (l < 2 * a.wg_t1) { which = 1; l -= a.wg_t1; mt = a.wg_mt1; }
+    else { which = 2; l -= 2 * a.wg_t1; mt = a.wg_mt2; }
+    const int m = (l % mt) * P_TILE + r, n = (l / mt) * P_TILE + col;
+    const int M = which == 2 ? a.h : a.d, N = which == 2 ? a.d : a.h;
+    if (m >= M || n >= N) continue;
+    const float* src = a.wg_part + (size_t)i * split * (P_TILE * P_TILE) + (size_t)r * P_TILE + col;
+    float acc = 0.f;
+    for (int c = 0; c < split; ++c) acc += src[(size_t)c * (P_TILE * P_TILE)];
+    uint16_t* out = which == 0 ? a.out0 : (which == 1 ? a.out1 : a.out2);
+    out[((size_t)e * M + m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+  }
+}
+
+// The wgrad tile plan, from the offsets (one CTA of 1024 threads): the experts with rows in
+// order of decreasing k-block count (ties: lower expert first), those without
+// rows in expert order, and the units.  Thread e ranks expert e against all
+// others (E <= 1024).  The last round of whole tiles holds the shallowest
+// expert's tiles (2L <= npairs < tiles per expert); when it keeps at most
+// half of the pairs busy, its L tiles are split along K into S chunks (L * S
+// <= npairs, at most parts_max partial tiles, 4 or more of that expert's
+// k-blocks a chunk).
+__device__ __forceinline__ void wgrad_plan(const int32_t* __restrict__ offsets, int E, int R, int per,
+                                           int npairs, int parts_max, int* __restrict__ plan) {
+  __shared__ int s_kb[kMaxExperts];
+  __shared__ int s_nc;
+  if (threadIdx.x == 0) s_nc = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int lo = max(0, min(__ldg(offsets + e), R));
+    const int hi = max(lo, min(__ldg(offsets + e + 1), R));
+    s_kb[e] = (hi - lo + BK - 1) / BK;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int k = s_kb[e];
+    int rank = 0;
+    if (k > 0) {
+      for (int j = 0; j < E; ++j) {
+        const int kj = s_kb[j];
+        rank += (kj > k) || (kj == k && j < e);
+      }
+      plan[kWgradPlanHead + rank] = e;
+      atomicAdd(&s_nc, 1);
+    } else {
+      for (int j = 0; j < e; ++j) rank += s_kb[j] == 0;
+      plan[kWgradPlanHead + E + rank] = e;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int nc = s_nc;
+    const long long tiles = (long long)nc * per;
+    const long long L = tiles % npairs;
+    int whole = (int)tiles, split = 0, units = (int)tiles;
+    if (L > 0 && 2 * L <= npairs && parts_max > 0 && nc > 0) {
+      long long S = npairs / L;
+      S = S < parts_max / L ? S : parts_max / L;
+      const int kb_last = s_kb[plan[kWgradPlanHead + nc - 1]];
+      S = S < kb_last / 4 ? S : kb_last / 4;
+      if (S >= 2) {
+        whole = (int)(tiles - L);
+        split = (int)S;
+        units = (int)(whole + L * S);
+      }
+    }
+    plan[0] = nc;
+    plan[1] = E - nc;
+    plan[2] = whole;
+    plan[3] = split;
+    plan[4] = units;
+    plan[5] = (E - nc) * per;
+  }
 }
 
 template <int MODE>
@@ -832,7 +917,16 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   }
   __syncthreads();
   if constexpr (MODE == kWG) {
-    if (threadIdx.x == 0) sh->total_tiles = args.wg_units;
+    // the device-built plan: units, K-split, zero tiles; the expert order
+    // goes where the row-grouped modes keep their tile table
+    if (threadIdx.x == 0) {
+      sh->total_tiles = args.wg_plan[4];
+      sh->wg_whole = args.wg_plan[2];
+      sh->wg_split = args.wg_plan[3];
+      sh->wg_zero = args.wg_plan[5];
+    }
+    const int nc = min(args.wg_plan[0], args.E);
+    for (int i = threadIdx.x; i < nc; i += blockDim.x) s_ts[i] = args.wg_plan[kWgradPlanHead + i];
   } else {
     if (warp == 0) {
       const int n = build_row_tile_table<P_TILE>(s_off, s_ts, args.E, args.R, args.n_tiles, lane);
@@ -843,7 +937,10 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
   // CTAs of a pair see the same offsets and so the same tile count
   cluster_sync();
   const int total = sh->total_tiles;
-  if (pair >= total) return;                 // uniform across the pair; no TMEM taken
+  // uniform across the pair; no TMEM taken.  (WG: a pair without compute
+  // units stays for its share of the zero tiles when no pair has any.)
+  if (pair >= (MODE == kWG ? max(total, 1) : total)) return;
+  const int* wgp = &sh->wg_whole;                 // {whole, split} for decode_pair_tile<kWG>
 
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&sh->tmem_base), kTmemCols);
@@ -867,8 +964,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     int wg_e = -1;                          // WG: expert of the descriptors acquired
     uint32_t wg_seen = 0;
     bool ok = true;
-    for (int t = pair; t < total && ok; t += npairs) {
-      const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+    for (int i = 0, t = pair_unit<MODE>(0, pair, npairs); t < total && ok; t = pair_unit<MODE>(++i, pair, npairs)) {
+      const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts, wgp);
       if constexpr (MODE == kWG) {
         // the descriptors were written by an earlier kernel through the
         // generic proxy; make them visible to the tensormap proxy, once per
@@ -889,7 +986,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
           if (leader) mbar_arrive_expect_tx(fb_local, nk * 4 * P_HALF);   // both CTAs' copies
           for (int j = 0; j < nk; ++j) {
             int kbr = kb0 + j;
-            if constexpr (MODE == kWG) kbr = wg_kblock(tl, t, pair, npairs, kbr);
+            if constexpr (MODE == kWG) kbr = wg_kblock(tl, i, kbr);
             const int q = stage * KPS + j;
             issue_loads_pair<MODE>(tl, kbr, rank, smem_u32(sA + q * P_HALF), smem_u32(sB + q * P_HALF),
                                    mapa_shared(fb_local, 0), &tmA0, &tmA1, &tmB0, &tmB1, args);
@@ -916,8 +1013,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued_any = false;
-      for (int t = pair; t < total && ok; t += npairs) {
-        const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+      for (int i = 0, t = pair_unit<MODE>(0, pair, npairs); t < total && ok; t = pair_unit<MODE>(++i, pair, npairs)) {
+        const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts, wgp);
         if constexpr (MODE == kWG) {
           if (tl.part < 0 && tl.nkb == 0) continue;     // empty expert: no accumulator (epilogue stores zeros)
         }
@@ -936,7 +1033,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
               for (int j = 0; j < nk; ++j) {
                 const int kb = kb0 + j, q = stage * KPS + j;
                 int nkk = BK / 16;
-                if constexpr (MODE == kWG) nkk = wg_groups(tl, wg_kblock(tl, t, pair, npairs, kb));
+                if constexpr (MODE == kWG) nkk = wg_groups(tl, wg_kblock(tl, i, kb));
                 const uint32_t sa = smem_u32(sA + q * P_HALF), sb = smem_u32(sB + q * P_HALF);
                 for (int kk = 0; kk < nkk; ++kk) {
                   uint64_t ad, bd;
@@ -973,8 +1070,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t rn = 0;                          // DA: ring chunks of the tiles before
-    for (int t = pair; t < total; t += npairs, rn += 8) {
-      Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+    for (int i = 0, t = pair_unit<MODE>(0, pair, npairs); t < total; t = pair_unit<MODE>(++i, pair, npairs), rn += 8) {
+      Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts, wgp);
       // this CTA's rows of the output tile
       if constexpr (MODE == kWG) {
         tl.m0 += 128 * (int)rank;
@@ -1015,8 +1112,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
     // slot g % kRingSlots, g counting the chunks in order
     uint32_t g = 0, issued = 0, last_par = 0;
     bool ok = true;
-    for (int t = pair; t < total && ok; t += npairs) {
-      const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts);
+    for (int i = 0, t = pair_unit<MODE>(0, pair, npairs); t < total && ok; t = pair_unit<MODE>(++i, pair, npairs)) {
+      const Tile tl = decode_pair_tile<MODE>(t, args, s_off, s_ts, wgp);
       const int y = tl.row0 + 128 * (int)rank;
       for (int c = 0; c < 8; ++c, ++g) {
         const int slot = (int)(g % kRingSlots);
@@ -1039,6 +1136,35 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
         if (issued & (1u << s)) drain_wait(smem_u32(&sh->rfull[s]), (last_par >> s) & 1u);
     }
     __syncwarp();
+  } else if constexpr (MODE == kWG) {
+    // ------------------------------------------- WG: the empty experts' dW
+    // Experts without rows get dW = 0.  Their tiles are not work units: this
+    // warp stores them from the shared box of zeros, round-robin over the
+    // pairs that run, beside the MMAs and on its own bulk-store queue (so the
+    // epilogue's waits for its staging buffers never wait for these stores),
+    // with at most two tiles' stores in flight.
+    const int per = 2 * args.wg_t1 + args.wg_t2;
+    const int nz = sh->wg_zero;
+    const int active = min(npairs, max(total, 1));
+    if (lane == 0) {
+      int n = 0;
+      for (int z = pair; z < nz; z += active) {
+        const int e = args.wg_plan[kWgradPlanHead + args.E + z / per];
+        int l = z % per, which, mt;
+        if (l < args.wg_t1) { which = 0; mt = args.wg_mt1; }
+        else if (l < 2 * args.wg_t1) { which = 1; l -= args.wg_t1; mt = args.wg_mt1; }
+        else { which = 2; l -= 2 * args.wg_t1; mt = args.wg_mt2; }
+        const int M = which == 2 ? args.h : args.d, N = which == 2 ? args.d : args.h;
+        const int m0 = (l % mt) * P_TILE + 128 * (int)rank, n0 = (l / mt) * P_TILE;
+        const CUtensorMap* map = which == 0 ? &tmO0 : (which == 1 ? &tmO1 : &tmO2);
+        for (int q = 0; q < 4 && m0 + 32 * q < M; ++q)
+          for (int c = 0; c < 8 && n0 + 32 * c < N; ++c) tma_store_3d(map, smem_u32(sZero), n0 + 32 * c, m0 + 32 * q, e);
+        bulk_commit();
+        if (++n >= 2) bulk_wait_group<1>();
+      }
+      bulk_wait_all();
+    }
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1056,10 +1182,17 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant
 // writes descriptor i of the [E][5] table.
 struct WgradTemplates { CUtensorMap m[kWgradMaps]; };
 
-__global__ void __launch_bounds__(128)
+// One launch prepares the wgrad: the last block writes the tile plan
+// (wgrad_plan), the others the descriptors, thread i descriptor i.
+__global__ void __launch_bounds__(1024)
 wgrad_maps_kernel(const __grid_constant__ WgradTemplates tp, const int32_t* __restrict__ offsets,
-                  int E, int R, CUtensorMap* __restrict__ maps) {
+                  int E, int R, CUtensorMap* __restrict__ maps, int per, int npairs, int parts_max,
+                  int* __restrict__ plan) {
   pdl_enter();
+  if (blockIdx.x == gridDim.x - 1) {
+    wgrad_plan(offsets, E, R, per, npairs, parts_max, plan);
+    return;
+  }
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= E * kWgradMaps) return;
   const int e = i / kWgradMaps, op = i - e * kWgradMaps;
@@ -1324,7 +1457,7 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
               size_t ws_bytes, cudaStream_t s) {
   MOE_CHECK_PTR(dW1); MOE_CHECK_PTR(dW3); MOE_CHECK_PTR(dW2);
   if (R > 0) {
-    if (ws_bytes < wgrad_maps_end(E)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < wgrad_plan_end(E)) return MOE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 127) != 0) return MOE_ERR_INVALID_ARG;
   }
   if (R == 0) {
@@ -1345,8 +1478,6 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
       !map2d(&tp.m[4], dyp, d, R, 64, 64))
     return MOE_ERR_CUDA;
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(static_cast<uint8_t*>(ws) + kStatusBytes);
-  (void)launch_pdl(wgrad_maps_kernel, (E * kWgradMaps + 127) / 128, 128, 0, s, tp, offsets, E, R, maps);
-  MOE_LAUNCH_CHECK(1);
   GemmArgs g = base_args(offsets, R, E, d, h, ws);
   g.wg_maps = maps;
   g.out0 = dW1; g.out1 = dW3; g.out2 = dW2;
@@ -1355,35 +1486,33 @@ int run_wgrad(const moe_bf16_t* xp, const int32_t* offsets, int R, int E, int d,
   g.wg_mt2 = (h + P_TILE - 1) / P_TILE;
   g.wg_t1 = g.wg_mt1 * ((h + P_TILE - 1) / P_TILE);
   g.wg_t2 = g.wg_mt2 * ((d + P_TILE - 1) / P_TILE);
-  const long long tiles = (long long)E * (2 * g.wg_t1 + g.wg_t2);
-  // The pairs take whole tiles round-robin.  When the last round would keep
-  // at most half of them busy, its L tiles are split along K into S chunks
-  // (L * S <= pairs, 4 or more k-blocks a chunk on average) whose fp32 partial
-  // sums a second kernel adds in chunk order.
+  const int per = 2 * g.wg_t1 + g.wg_t2;
+  const long long tiles = (long long)E * per;
+  // The work units are the tiles of the experts that have rows, deepest
+  // expert first (the host never learns the row counts: a one-CTA kernel
+  // writes the plan from the offsets); the pairs take them in snake order and
+  // split the last round along K when it would keep at most half of them busy
+  // (fp32 partials a second kernel adds in chunk order).  The empty experts'
+  // zero tiles are stored beside the work units by one warp of each pair.
   const int P = pair_limit<kWG>(s);
   if (P <= 0) return MOE_ERR_CUDA;
-  const long long L = tiles % P;
-  g.wg_whole = (int)(tiles - L);
-  g.wg_split = 0;
-  g.wg_units = (int)tiles;
-  if (L > 0 && 2 * L <= P && ws_bytes >= wgrad_parts_end(E)) {
-    long long S = P / L;
-    S = S < kWgradParts / L ? S : kWgradParts / L;
-    const long long k_blocks = (long long)R / ((long long)E * BK);   // per expert, on average
-    S = S < k_blocks / 4 ? S : k_blocks / 4;
-    if (S >= 2) {
-      g.wg_split = (int)S;
-      g.wg_units = (int)(g.wg_whole + L * S);
-      g.wg_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wgrad_parts_offset(E));
-    }
-  }
+  const int npairs = (int)(tiles < P ? tiles : P);
+  const bool parts = ws_bytes >= wgrad_parts_end(E);
+  int* plan = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + wgrad_plan_offset(E));
+  (void)launch_pdl(wgrad_maps_kernel, (E * kWgradMaps + 1023) / 1024 + 1, 1024, 0, s, tp, offsets, E, R, maps,
+                   per, npairs, parts ? kWgradParts : 0, plan);
+  MOE_LAUNCH_CHECK(1);
+  g.wg_plan = plan;
+  g.wg_part = parts ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + wgrad_parts_offset(E)) : nullptr;
   OutDescs o;
   if (!map3d_out(&o.m[0], dW1, h, d, E) || !map3d_out(&o.m[1], dW3, h, d, E) ||
       !map3d_out(&o.m[2], dW2, d, h, E))
     return MOE_ERR_CUDA;
-  const int st = launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], o, g, g.wg_units, s);
-  if (st != MOE_OK || g.wg_split == 0) return st;
-  (void)launch_pdl(wgrad_fixup_kernel, (unsigned)(L * P_TILE), P_TILE, 0, s, g);
+  const int st = launch_pair<kWG>(tp.m[0], tp.m[1], tp.m[2], tp.m[3], o, g, tiles, s);
+  if (st != MOE_OK || !parts) return st;
+  // up to npairs / 2 split tiles of 256 rows; 2048 blocks take them (one row
+  // each at dense_e8's 8 split tiles) and return at once when nothing was split
+  (void)launch_pdl(wgrad_fixup_kernel, 2048u, P_TILE, 0, s, g);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
