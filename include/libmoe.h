@@ -258,13 +258,15 @@ int moe_grouped_swiglu_fwd(const moe_bf16_t* xp, const int32_t* offsets,
  * give exactly zero).  dh1/dh3[R,h] are caller-provided intermediates (also
  * outputs).  dW1/dW3[E,d,h], dW2[E,h,d] bf16 from fp32 accumulators, no
  * atomics, deterministic.  The weight-gradient phase keeps five TMA
- * descriptors per expert in ws (bytes [256, 256 + 640 E)), written on the
- * device from offsets, and, when the last round of its 256 x 256 tiles would
- * leave most SMs idle, splits those tiles along the rows into chunks whose
- * fp32 partial sums (up to 80 tiles of 256 KB after the descriptors) are
- * added in a fixed order.  For R > 0 ws must be 128-byte aligned
- * (MOE_ERR_INVALID_ARG) and hold at least the descriptors (else
- * MOE_ERR_WORKSPACE); moe_workspace_size(...) also covers the partials. */
+ * descriptors per expert in ws (bytes [256, 256 + 640 E)) and, after them, a
+ * tile plan ((8 + 2E) int32: the experts with rows ordered by depth, the
+ * empty ones, the unit counts), both written on the device from offsets; when
+ * the last round of its 256 x 256 tiles would leave most SMs idle, it splits
+ * those tiles along the rows into chunks whose fp32 partial sums (up to 80
+ * tiles of 256 KB after the plan) are added in a fixed order.  For R > 0 ws
+ * must be 128-byte aligned (MOE_ERR_INVALID_ARG) and hold at least the
+ * descriptors and the plan (else MOE_ERR_WORKSPACE); moe_workspace_size(...)
+ * also covers the partials. */
 int moe_grouped_swiglu_bwd(const moe_bf16_t* xp, const int32_t* offsets,
                            int R, int E, int d, int h,
                            const moe_bf16_t* W1, const moe_bf16_t* W3,
