@@ -96,16 +96,19 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
 
 
 def test_wgrad_workspace_holds_the_per_expert_descriptors(lib):
-    # five 128-byte TMA descriptors per expert after the 256-byte status word
+    # five 128-byte TMA descriptors per expert after the 256-byte status word,
+    # the tile plan ((8 + 2E) int32) after them
     for E in (1, 8, 128, 1024):
         # + the weight-gradient GEMM's fp32 partial tiles (80 x 256 x 256)
-        assert lib.moe_workspace_size(16, E, 1, 64, 64) >= 256 + 640 * E + 80 * 256 * 256 * 4
+        assert lib.moe_workspace_size(16, E, 1, 64, 64) >= 256 + 640 * E + (8 + 2 * E) * 4 + 80 * 256 * 256 * 4
     fake = ctypes.c_void_p(0x1000)
     args = lambda ws, n: (fake, fake, 64, 128, 128, 128, fake, fake, fake, fake, fake, fake,
                           fake, ws, n, None)
     need = lib.moe_workspace_size(16, 128, 4, 128, 128)
     # too small for 128 experts' descriptors (but larger than the status word)
     assert lib.moe_grouped_swiglu_bwd_wgrad(*args(fake, 256 + 640 * 127)) == -3
+    # the descriptors fit, the tile plan does not
+    assert lib.moe_grouped_swiglu_bwd_wgrad(*args(fake, 256 + 640 * 128 + (8 + 2 * 128) * 4 - 4)) == -3
     # descriptors must sit on 128-byte boundaries
     assert lib.moe_grouped_swiglu_bwd_wgrad(*args(ctypes.c_void_p(0x1010), need)) == -1
 
