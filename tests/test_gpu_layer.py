@@ -94,6 +94,11 @@ def compare_full(layer, w, inp, backward=True):
     # more experts than DA's CTA-pair tile table holds: DA on single CTAs
     # beside the CTA-pair UP, DOWN, DX and wgrad GEMMs
     (31000, 64, 240, 4, 64, ()),
+    # one expert holds every row: the weight gradient's plan has fewer work
+    # units (3) than pairs, and the other experts' zero tiles go to the pairs
+    # that stay (single-CTA, then CTA-pair row GEMMs)
+    (600, 256, 8, 1, 256, (0, 1, 2, 4, 5, 6, 7)),
+    (2100, 256, 4, 1, 256, (0, 1, 3)),
 ])
 def test_layer_small_full_compare(T, d, E, k, h, empty):
     w = wl.small_workload(T=T, d=d, E=E, k=k, h=h)
