@@ -13,8 +13,8 @@
 //          epilogue writes h1, h3, a = silu(h1) * h3 (bf16) and quantises a
 //          (one 32-column block per thread: Aq codes + As scale bytes)
 //   DOWN8: yp = Aq_e @ W2q[e]
-// Tiles are 128 x 192 with BK = 128 fp8 (one 128-byte swizzled row per
-// operand row), 4 pipeline stages.  Operands are K-major: activations
+// Tiles are 192 columns wide with BK = 128 fp8 a k-block (one 128-byte
+// swizzled row per operand row).  Operands are K-major: activations
 // [R][K], weights [E][N][K] (moe_mxfp8_quantize_weights transposes).
 // Issue rates of block-scaled MMAs with their per-k-block scale copies,
 // measured on the GB300 with operands resident in shared memory: N = 256 runs
@@ -32,14 +32,15 @@
 // base + m/32, and column n's B scale at lane n%32 of the issuing quarter,
 // column base + n/32, byte = the MMA's scale-factor id (0..3).
 //
-// Two kernel forms.  Single CTA: 128 x 192 tiles, 4 stages.  CTA pairs
-// (2-CTA clusters, cta_group::2): 256 x 192 tiles, each CTA stages its own
-// 128 A rows, half of the B columns (UP8: the even CTA the 96 W1 columns, the
-// odd CTA the same 96 W3 columns) and the scale atoms its half of the MMA
-// reads (its own A atom, both B atoms); all of a stage's copies, of both
-// CTAs, complete on the even CTA's barrier, whose MMA lane also copies both
-// CTAs' atoms into their tensor memory (tcgen05.cp.cta_group::2).  Per MMA a
-// CTA then moves 7 KB through shared memory instead of 10 KB on one CTA.
+// Two kernel forms.  Single CTA: 128 x 192 tiles, 4 stages of one k-block.
+// CTA pairs (2-CTA clusters, cta_group::2): 256 x 192 tiles, 3 stages of two
+// k-blocks; each CTA stages its own 128 A rows, half of the B columns (UP8:
+// the even CTA the 96 W1 columns, the odd CTA the same 96 W3 columns) and the
+// scale atoms its half of the MMA reads (its own A atom, both B atoms); all of
+// a stage's copies, of both CTAs, complete on the even CTA's barrier, and the
+// even CTA's scale-copy warp moves both CTAs' atoms into their tensor memory
+// (tcgen05.cp.cta_group::2).  Per MMA a CTA then moves 7 KB through shared
+// memory instead of 10 KB on one CTA.
 #include "gemm_common.cuh"
 #include "mx_common.cuh"
 
@@ -224,8 +225,8 @@ __device__ __forceinline__ void epilogue8(const RowTile& rt, int n0, uint32_t ta
 
 // One persistent kernel per mode and form.  Warp 0 loads operands and scale
 // atoms by TMA, warp 1 allocates tensor memory and one lane (of the even CTA,
-// on pairs) copies the atoms to tensor memory and issues the MMAs, warps 2-9
-// drain the other accumulator.
+// on pairs) issues the MMAs, warps 2-9 drain the other accumulator, warp 10
+// (of the even CTA) copies each stage's scale atoms to tensor memory.
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads8, 1)
 grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA1,
