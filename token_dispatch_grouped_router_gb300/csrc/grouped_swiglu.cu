@@ -524,8 +524,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 //                      staging buffers (its stores go out of the ring slots),
 //                      and at most pair_max_experts<kDA>() experts (the tile
 //                      table shares the 227 KB).
-//   WG:                256 x 256 tiles of dW over the expert's rows.
-constexpr int P_STAGES = 6;
+//   WG:                256 x 256 tiles of dW over the expert's rows; units
+//                      from a device-built plan, and a warp that stores the
+//                      empty experts' zero tiles.
+constexpr int P_SLOTS = 6;                            // 32 KB k-block slots (DA: 5)
 constexpr int P_HALF = 128 * BK * 2;                  // 16 KB: 128 rows x 64 deep
 constexpr int P_TILE = 256;
 // DA's epilogue ring: slot = one 32-column chunk of h1 and of h3 for the
@@ -542,7 +544,7 @@ constexpr int kRingSlotBytes = 2 * kRingChunk;
 // its h1/h3 ring (2 stages of 2 slots there: 203 -> 234 us at T = 16384,
 // E = 8).
 template <int MODE> __host__ __device__ constexpr int pair_kps() { return MODE == kDA ? 1 : 2; }
-template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_STAGES / 2; }
+template <int MODE> __host__ __device__ constexpr int pair_stages() { return MODE == kDA ? 5 : P_SLOTS / 2; }
 template <int MODE> __host__ __device__ constexpr int pair_slots() { return pair_stages<MODE>() * pair_kps<MODE>(); }
 template <int MODE> __host__ __device__ constexpr int pair_ring_bytes() { return MODE == kDA ? kRingSlots * kRingSlotBytes : 0; }
 template <int MODE> __host__ __device__ constexpr int pair_stage_bytes() { return MODE == kDA ? 0 : kEpiWarps * kStageBytes; }
