@@ -60,59 +60,82 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float g, uint4 v) {
   acc[6] = fmaf(g, bf16_lo(v.w), acc[6]); acc[7] = fmaf(g, bf16_hi(v.w), acc[7]);
 }
 
-// out[t] = sum_j g[t,j] * yp[row(t,j)] in slot order, fp32, one rounding.
-template <int U>
+// out[t] = sum_j g[t,j] * yp[row(t,j)] in slot order, fp32, one rounding
+// (g = 1 without gates: the unpermute-sum).  k is a template parameter so
+// that all K x U row loads of a pass are in flight before the first FMA (8 to
+// 16 vectors of 16 bytes a lane; a generic copy loading one row at a time ran
+// at 0.88-0.89 of the HBM copy rate, this one at 0.93-0.95); slots with no
+// row read row 0 and add nothing.
+template <int K, int U>
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const uint16_t* __restrict__ yp, int R, const int32_t* __restrict__ row_of_slot,
-               const float* __restrict__ gate, int T, int k, int d, uint16_t* __restrict__ out) {
+combine_k_kernel(const uint16_t* __restrict__ yp, int R, const int32_t* __restrict__ row_of_slot,
+                 const float* __restrict__ gate, int T, int d, uint16_t* __restrict__ out) {
   pdl_enter();
   const int t = (int)((blockIdx.x * (size_t)kThreads + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const int nvec = d >> 3;
-  int rows[kMaxTopK];
-  float g[kMaxTopK];
+  int rows[K];
+  float g[K];
+  bool ok[K];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    rows[j] = j < k ? __ldg(row_of_slot + (size_t)t * k + j) : -1;
-    g[j] = (j < k) ? (gate ? __ldg(gate + (size_t)t * k + j) : 1.f) : 0.f;
+  for (int j = 0; j < K; ++j) {
+    rows[j] = __ldg(row_of_slot + (size_t)t * K + j);
+    ok[j] = row_ok(rows[j], R);
+    if (!ok[j]) rows[j] = 0;
+    g[j] = gate ? __ldg(gate + (size_t)t * K + j) : 1.f;
   }
   uint16_t* dst = out + (size_t)t * d;
   for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
-    float acc[U][8];
+    uint4 val[K][U];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+    for (int j = 0; j < K; ++j) {
+      const uint16_t* src = yp + (size_t)rows[j] * d;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (row_ok(rows[j], R)) {
-        const uint16_t* src = yp + (size_t)rows[j] * d;
-        uint4 val[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          int v = v0 + 32 * u;
-          if (v < nvec) val[u] = ld_nc_v4(src + (size_t)v * 8);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          int v = v0 + 32 * u;
-          if (v < nvec) fma8(acc[u], g[j], val[u]);
-        }
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) val[j][u] = ld_nc_v4(src + (size_t)v * 8);
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      int v = v0 + 32 * u;
+      const int v = v0 + 32 * u;
       if (v < nvec) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+          if (ok[j]) fma8(acc, g[j], val[j][u]);
         uint4 o;
-        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
         st_v4(dst + (size_t)v * 8, o);
       }
     }
+  }
+}
+
+template <int K>
+void launch_combine_k(dim3 grid, cudaStream_t s, const uint16_t* yp, int R, const int32_t* row_of_slot,
+                      const float* gate, int T, int d, uint16_t* out) {
+  constexpr int U = K <= 2 ? 8 : (K <= 4 ? 4 : 2);
+  (void)launch_pdl(combine_k_kernel<K, U>, grid, kThreads, 0, s, yp, R, row_of_slot, gate, T, d, out);
+}
+
+void combine_switch(dim3 grid, cudaStream_t s, const moe_bf16_t* yp, int R, const int32_t* row_of_slot,
+                    const float* gate, int T, int k, int d, moe_bf16_t* out) {
+  switch (k) {
+    case 1: launch_combine_k<1>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    case 2: launch_combine_k<2>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    case 3: launch_combine_k<3>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    case 4: launch_combine_k<4>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    case 5: launch_combine_k<5>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    case 6: launch_combine_k<6>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    case 7: launch_combine_k<7>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
+    default: launch_combine_k<8>(grid, s, yp, R, row_of_slot, gate, T, d, out); break;
   }
 }
 
@@ -268,11 +291,7 @@ int moe_combine(const moe_bf16_t* yp, const int32_t* row_of_slot, const float* g
   MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(out);
   if (gate && !aligned16(gate)) return MOE_ERR_INVALID_ARG;
   dim3 grid((T + kWarps - 1) / kWarps);
-  // 8 vectors a lane: a 2048-wide row in one pass.  (A copy specialised on k
-  // issues all k x 8 loads up front, needs 136 registers and runs 1.8x slower
-  // at one block per SM; this one stays at 127 and two blocks.)
-  (void)launch_pdl(combine_kernel<8>, grid, kThreads, 0, (cudaStream_t)stream, yp, T * k, row_of_slot, gate, T,
-                   k, d, out);
+  combine_switch(grid, (cudaStream_t)stream, yp, T * k, row_of_slot, gate, T, k, d, out);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
@@ -319,8 +338,7 @@ int moe_combine_capacity(const moe_bf16_t* yp, int E, int C, const int32_t* row_
   if (T == 0) return MOE_OK;
   MOE_CHECK_PTR(yp); MOE_CHECK_PTR(row_of_slot); MOE_CHECK_PTR(out);
   if (gate && !aligned16(gate)) return MOE_ERR_INVALID_ARG;
-  (void)launch_pdl(combine_kernel<8>, dim3((T + kWarps - 1) / kWarps), kThreads, 0, (cudaStream_t)stream, yp,
-                   E * C, row_of_slot, gate, T, k, d, out);
+  combine_switch(dim3((T + kWarps - 1) / kWarps), (cudaStream_t)stream, yp, E * C, row_of_slot, gate, T, k, d, out);
   MOE_LAUNCH_CHECK(1);
   return MOE_OK;
 }
