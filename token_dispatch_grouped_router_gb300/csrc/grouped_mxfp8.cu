@@ -63,12 +63,12 @@ constexpr int kThreads8 = kThreads + 32;        // + the scale-copy warp
 // a stage holds (KPS), and the tensor-memory columns of the second
 // accumulator and of stage s's scales (k-block j of the stage: A at
 // sf_col(s) + 12j, B at sf_col(s) + 12j + 4; 12 columns a k-block).
-// A stage is one barrier wait and one commit on the MMA lane.  Each of those
+// A stage costs the MMA lane its barrier waits and one commit.  Each of those
 // takes the issuing thread off the tensor pipe for about a short MMA's time
-// (measured on the GB300 with operands resident: a pair loop with one wait
+// (measured on the GB300 with operands resident: a pair loop with two waits
 // and two commits per 4-MMA k-block issues at 0.57 of the fp8 rate, with one
-// wait and one commit per 8 MMAs at 0.92), so the pair form stages two
-// k-blocks at a time.
+// wait and one commit per 8 MMAs at 0.92, two waits and one commit at 0.86),
+// so the pair form stages two k-blocks at a time.
 template <bool PAIR> struct Form;
 template <> struct Form<false> {
   static constexpr int TM = 128, BROWS = 192, STAGES = 4, KPS = 1;
@@ -249,7 +249,8 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   uint8_t* sStage = sSF + S * KPS * SF_STAGE;                // kEpiWarps x kStageBytes
   Shared* sh = reinterpret_cast<Shared*>(sStage + kEpiWarps * kStageBytes);
   uint64_t* sfull = reinterpret_cast<uint64_t*>(sh + 1);      // [S] scales in TMEM, [S] copy drain
-  int* s_off = reinterpret_cast<int*>(sfull + S + 1);
+  uint64_t* sfa = sfull + S + 1;                               // [S] a stage's scale atoms landed
+  int* s_off = reinterpret_cast<int*>(sfull + 2 * S + 1);
   int* s_ts = s_off + (args.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -266,6 +267,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       mbar_init(smem_u32(&sfull[s]), 1);
     }
     mbar_init(smem_u32(&sfull[S]), 1);
+    for (int q = 0; q < S; ++q) mbar_init(smem_u32(&sfa[q]), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sh->tfull[s]), 1);
       mbar_init(smem_u32(&sh->tempty[s]), (PAIR ? 2 : 1) * kEpiWarps);
@@ -320,18 +322,22 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
           const int arow = rt.row0 + 128 * (int)rank;
           // the scale atoms of a stage's k-blocks are adjacent in HBM: one copy
           // of KPS A atoms and one of 2 * KPS B atoms (a copy past the end of a
-          // tile's k-blocks reads atoms it does not use, zeros past the table)
+          // tile's k-blocks reads atoms it does not use, zeros past the table),
+          // counted on a barrier of their own so that their tensor-memory
+          // copies need not wait for the stage's operands
           const uint32_t ssa = smem_u32(sSF + stage * KPS * SF_STAGE);
           const uint32_t ssb = ssa + KPS * mx::kAtomBytes;
+          const uint32_t sb_local = smem_u32(&sfa[stage]);
           if constexpr (PAIR) {
-            if (leader) mbar_arrive_expect_tx(fb_local, 2 * (nk * (A_STAGE + B_STAGE) + KPS * SF_STAGE));
-            const uint32_t fb = mapa_shared(fb_local, 0);
-            tma_load_2d_pair(ssa, &tmSA, fb, 0, blk * KB + kb0);
-            tma_load_2d_pair(ssb, &tmSB, fb, 0, (wat + kb0) * 2);
+            if (leader) { mbar_arrive_expect_tx(fb_local, 2 * nk * (A_STAGE + B_STAGE)); mbar_arrive_expect_tx(sb_local, 2 * KPS * SF_STAGE); }
+            const uint32_t sbb = mapa_shared(sb_local, 0);
+            tma_load_2d_pair(ssa, &tmSA, sbb, 0, blk * KB + kb0);
+            tma_load_2d_pair(ssb, &tmSB, sbb, 0, (wat + kb0) * 2);
           } else {
-            mbar_arrive_expect_tx(fb_local, nk * (A_STAGE + B_STAGE) + KPS * SF_STAGE);
-            tma_load_2d(ssa, &tmSA, fb_local, 0, blk * KB + kb0);
-            tma_load_2d(ssb, &tmSB, fb_local, 0, (wat + kb0) * 2);
+            mbar_arrive_expect_tx(fb_local, nk * (A_STAGE + B_STAGE));
+            mbar_arrive_expect_tx(sb_local, KPS * SF_STAGE);
+            tma_load_2d(ssa, &tmSA, sb_local, 0, blk * KB + kb0);
+            tma_load_2d(ssb, &tmSB, sb_local, 0, (wat + kb0) * 2);
           }
           for (int j = 0; j < nk; ++j) {
             const int kb = kb0 + j, q = stage * KPS + j;
@@ -372,7 +378,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     if (!ok && leader && lane == 0) {
       // the (even CTA's) full barriers count every copy of the stage
       for (int s = 0; s < S; ++s)
-        if (issued & (1u << s)) drain_wait(smem_u32(&sh->full[s]), (last_par >> s) & 1u);
+        if (issued & (1u << s)) { drain_wait(smem_u32(&sh->full[s]), (last_par >> s) & 1u); drain_wait(smem_u32(&sfa[s]), (last_par >> s) & 1u); }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -387,10 +393,13 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         const uint32_t dt = tmem + F::acc_col(acc);
         for (int kb0 = 0; kb0 < KB; kb0 += KPS) {
           const int nk = min(KPS, KB - kb0);
-          // The stage's scales are in tensor memory.  Their copies were issued
-          // after the scale-copy warp saw the stage's full barrier complete, so
-          // the stage's operands have landed as well: one wait is enough.
-          if (!bounded_wait(smem_u32(&sfull[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+          // the stage's scales are in tensor memory and its operands have landed
+          // (two barriers: with the scale copies waiting for the atoms alone,
+          // their latency hides under the operand copies, which costs the MMA
+          // lane a second wait but took the train_e128 forward from 0.822 to
+          // 0.796 ms against one wait on copies issued after the full barrier)
+          if (!bounded_wait(smem_u32(&sfull[stage]), phase, &sh->abort_flag, args.status) ||
+              !bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
             for (int j = 0; j < nk; ++j) {
@@ -459,7 +468,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   } else if (leader) {
     // ------------------------------------------------ scale copies (even CTA)
     // A stage's atoms go to tensor memory from this warp, off the MMA lane:
-    // tcgen05.cp of both CTAs' atoms (the pair form) once the stage's copies
+    // tcgen05.cp of both CTAs' atoms (the pair form) once the stage's atoms
     // have landed, then a commit to sfull[stage] that the MMA lane waits on.
     // The stage's scale columns are rewritten only after the producer
     // refilled the stage, i.e. after the MMAs that read them completed.
@@ -470,7 +479,7 @@ grouped_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       bool ok = true;
       for (int kb0 = 0; kb0 < KB; kb0 += KPS) {
         const int nk = min(KPS, KB - kb0);
-        if (!bounded_wait(smem_u32(&sh->full[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
+        if (!bounded_wait(smem_u32(&sfa[stage]), phase, &sh->abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
           for (int j = 0; j < nk; ++j) {
@@ -583,7 +592,7 @@ inline bool map_atoms(CUtensorMap* m, const void* ptr, uint64_t n_atoms, uint32_
 template <bool PAIR>
 constexpr size_t smem_bytes8(int E) {
   return 1024 + (size_t)Form<PAIR>::STAGES * stage_bytes<PAIR>() + (size_t)kEpiWarps * kStageBytes +
-         sizeof(PipeShared<Form<PAIR>::STAGES>) + 8 * (Form<PAIR>::STAGES + 1) + 2 * (size_t)(E + 1) * 4;
+         sizeof(PipeShared<Form<PAIR>::STAGES>) + 8 * (2 * Form<PAIR>::STAGES + 1) + 2 * (size_t)(E + 1) * 4;
 }
 static_assert(smem_bytes8<true>(kMaxExperts8) <= 227 * 1024, "pair MXFP8 kernel fits in shared memory");
 static_assert(smem_bytes8<false>(kMaxExperts8) <= 227 * 1024, "MXFP8 kernel fits in shared memory");
