@@ -10,7 +10,9 @@ wgrad), unpermute-sum and router backward.  Inputs are seeded synthetic
 tensors resident in HBM.  Between timed steps a 256 MB buffer is written to
 flush the 129 MB L2 (twice over); every library call of a step is bracketed by CUDA events
 on the launching stream, so the per-kernel times below come from the timed
-steps themselves.
+steps themselves.  The unpermute and the router backward run on a second
+stream beside the weight-gradient GEMM; their times come from that stream's
+events, and the step ends after the streams have joined.
 
 Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs its own
 token batch with its own copy of the experts (replicas, no collective in the
@@ -272,13 +274,16 @@ def run_ours(args):
         torch.cuda.synchronize()
         L.moe_reset_status(layer.ws)
         # ---------------------------------------------------------- timed region
-        events = []                          # per step: [(label, event), ...]
+        events = []                          # per step: [(label, event, stream), ...]
 
         def new_mark(lst):
             def mark(label):
+                # on the current stream: the layer runs part of its backward
+                # on a second stream, whose calls are timed by its own events
+                st = torch.cuda.current_stream()
                 ev = torch.cuda.Event(enable_timing=True)
-                ev.record()
-                lst.append((label, ev))
+                ev.record(st)
+                lst.append((label, ev, st.cuda_stream))
             return mark
 
         barrier()
@@ -303,14 +308,42 @@ def run_ours(args):
         status = L.moe_get_status(layer.ws)
         if status != 0:
             raise RuntimeError(f"device status {status} after the timed steps")
-        step_ms, per_label = [], {}
+        step_ms, per_label, side_labels = [], {}, set()
         for lst in events:
-            step_ms.append(lst[0][1].elapsed_time(lst[-1][1]))
-            for (lab, ev), (_, nxt) in zip(lst[:-1], lst[1:]):
-                per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
+            # the step: first to last event of the launching stream (the last
+            # one follows the join of the second stream); a call: its event
+            # to the next one on the same stream
+            by_stream = {}
+            for lab, ev, st in lst:
+                by_stream.setdefault(st, []).append((lab, ev))
+            main_seq = by_stream[lst[0][2]]
+            side_labels |= {lab for lab, _, st in lst if st != lst[0][2]}
+            step_ms.append(main_seq[0][1].elapsed_time(main_seq[-1][1]))
+            for seq in by_stream.values():
+                for (lab, ev), (_, nxt) in zip(seq[:-1], seq[1:]):
+                    per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
         return {"ms_per_step": allmax(statistics.mean(step_ms), dev),
                 "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
+                "side_labels": sorted(side_labels),
                 "launches": launches, "clocks": clocks, "wall_s": wall}
+
+    def time_alone(fn, reps=5):
+        """Mean event-timed duration of one library call run by itself, L2
+        flushed before each (the calls the step runs beside another kernel
+        get their roofline from this)."""
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.mean(ts)
 
     def tile_overhead(layer):
         """Rows the row-grouped GEMMs multiply beyond the T*k routed rows: each
@@ -326,6 +359,9 @@ def run_ours(args):
         layer = make_layer(w, inp)
         res = timed_layer(layer, K, W, sample_clocks=sample_clocks)
         res["row_tile_overhead"] = tile_overhead(layer)
+        if "unpermute" in res["side_labels"]:
+            res["alone_ms"] = {"unpermute": time_alone(
+                lambda: L.moe_combine(layer.dxp, layer.row_of_slot, None, layer.k, layer.dX))}
         if with_e2e:
             res["e2e"] = e2e(layer, inp, K)
             # the recompute policy (Xp gathered again, H1/H3/A recomputed in
@@ -447,8 +483,10 @@ def run_ours(args):
     value = throughput(w.T, world, ms)
     km = main["kernels_ms"]
     flops, bytes_ = work_per_launch(w)
-    # the dominant kernel: the single-kernel call with the largest share of the step
-    single = {k: v for k, v in km.items() if k in flops or k in bytes_}
+    # the dominant kernel: the single-kernel call with the largest share of the
+    # step, among the calls on the step's own stream
+    single = {k: v for k, v in km.items()
+              if (k in flops or k in bytes_) and k not in main["side_labels"]}
     dom = max(single, key=single.get)
     traffic = None
     try:
@@ -486,6 +524,12 @@ def run_ours(args):
     rows = {k: {"ms": km[k], "GB_s": bytes_[k] / (km[k] / 1e3) / 1e9,
                 "frac_hbm": bytes_[k] / (km[k] / 1e3) / 1e9 / peaks["hbm_gbs"]}
             for k in bytes_ if k in km}
+    for k, ms_alone in main.get("alone_ms", {}).items():
+        # run beside the wgrad GEMM on the layer's second stream: its time
+        # there is shared; its bandwidth is that of the call timed by itself
+        gbs = bytes_[k] / (ms_alone / 1e3) / 1e9
+        rows[k] = {"ms": ms_alone, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                   "ms_beside_gemm_wgrad": km.get(k), "timed": "alone, L2 flushed"}
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -39,7 +39,12 @@
  *    be a multiple of 8.  T * k must fit in int32.
  *  - Calls are stateless apart from a per-device cache of the SM count and of
  *    kernel attributes; they are safe to call from several host threads on
- *    different streams with distinct workspaces.
+ *    different streams with distinct workspaces.  One pairing may share a
+ *    workspace: moe_grouped_swiglu_bwd_wgrad and moe_router_logits_bwd_topk
+ *    use disjoint parts of it (the router backward's scratch lies past the
+ *    weight-gradient GEMM's descriptors, plan and partial tiles), so they, and
+ *    calls that take no workspace (moe_combine, moe_router_topk_bwd), may run
+ *    at the same time on two streams; the status word is set atomically.
  */
 #ifndef LIBMOE_H
 #define LIBMOE_H

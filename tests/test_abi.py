@@ -131,6 +131,14 @@ def test_router_and_mxfp8_additions_check_arguments_on_the_host(lib):
                                           fake, fake, NULL, fake, big, NULL) == -1
     assert lib.moe_router_logits_bwd_topk(fake, fake, fake, fake, fake, fake, 64, 16, 8, 2,
                                           fake, fake, NULL, fake, 300, NULL) == -3
+    # its scratch lies past the weight-gradient GEMM's part of the workspace
+    # (descriptors, tile plan, fp32 partial tiles), so that part alone is too small
+    E = 8
+    plan = -(-(256 + 640 * E) // 256) * 256 + (8 + 2 * E) * 4
+    wgrad_part = -(-plan // 256) * 256 + 80 * 256 * 256 * 4
+    assert lib.moe_workspace_size(64, E, 2, 16, 64) > wgrad_part
+    assert lib.moe_router_logits_bwd_topk(fake, fake, fake, fake, fake, fake, 64, 16, E, 2,
+                                          fake, fake, NULL, fake, wgrad_part, NULL) == -3
     # MXFP8: dequantise needs K % 32, the fp32-master quantiser N % 128
     assert lib.moe_mxfp8_dequantize_rows(fake, fake, 4, 48, fake, NULL) == -2
     assert lib.moe_mxfp8_dequantize_rows(fake, NULL, 4, 64, fake, NULL) == -1

@@ -158,6 +158,34 @@ def test_graph_capture_proves_no_host_sync_and_replays_bitwise():
         assert torch.equal(getattr(layer, n), v), n
 
 
+@pytest.mark.parametrize("routing,factor", [("uniform", None), ("learned", None), ("learned", 1.25)])
+def test_second_stream_backward_equals_one_stream_bitwise(routing, factor):
+    # the unpermute and the router backward run on a second stream beside the
+    # weight-gradient GEMM (the padded layer's unpadded route map after it);
+    # the results equal the single-stream step bit for bit, also with three
+    # steps queued back to back (each step's forward after the last join)
+    w = wl.small_workload(T=2304, d=256, E=8, k=4, h=256, routing=routing,
+                          zipf=(routing == "learned"))
+    inp = wl.generate(w, seed=9)
+    names = ("out", "dgate", "dlogits", "dxp", "dW1", "dW3", "dW2", "dX")
+    if routing == "learned":
+        names += ("dW_r", "db")
+    res = []
+    for side in (False, True):
+        layer = MoELayer(w.T, w.d, w.E, w.k, w.h, learned=(routing == "learned"), device=DEV,
+                         capacity_factor=factor, side_stream=side)
+        assert (layer._side is not None) == side
+        layer.load_inputs(inp)
+        L.moe_reset_status(layer.ws)
+        for _ in range(3):
+            layer.step()
+        torch.cuda.synchronize()
+        assert L.moe_get_status(layer.ws) == 0
+        res.append({n: getattr(layer, n).clone() for n in names})
+    for n in names:
+        assert torch.equal(res[0][n], res[1][n]), n
+
+
 @pytest.mark.parametrize("T,E", [(2000, 16), (2048, 4)])   # single-CTA / CTA-pair row GEMMs
 def test_deterministic_bitwise(T, E):
     w = wl.small_workload(T=T, d=256, E=E, k=4, h=256)

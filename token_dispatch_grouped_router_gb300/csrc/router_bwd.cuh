@@ -1,5 +1,7 @@
 // Workspace layout of moe_router_logits_bwd_topk (bytes from the start of ws,
-// after the 256-byte status word): W_r transposed [E][d] fp32, the row-chunk
+// after the weight-gradient GEMM's part: its descriptors, tile plan and fp32
+// partial tiles, so the two may run at once on two streams sharing one
+// workspace): W_r transposed [E][d] fp32, the row-chunk
 // table of the dW_r reduction (one entry per chunk of at most kRouterChunk
 // rows of an expert's segment, plus per-expert first chunk and chunk count),
 // the chunks' fp32 partial sums [chunks][d] and partial bias sums [chunks].
@@ -16,7 +18,7 @@ struct RouterTopkScratch { size_t wt, units, estart, ecount, total, part, pbias,
 inline RouterTopkScratch router_topk_scratch(long long R, int E, int d) {
   RouterTopkScratch s;
   s.max_units = (R + kRouterChunk - 1) / kRouterChunk + E;
-  s.wt = kStatusBytes;
+  s.wt = round_up(wgrad_parts_end(E), 256);
   s.units = round_up(s.wt + (size_t)E * d * 4, 256);
   s.estart = round_up(s.units + (size_t)s.max_units * 16, 256);
   s.ecount = round_up(s.estart + (size_t)E * 4, 256);

@@ -54,7 +54,7 @@ class MoELayer:
 
     def __init__(self, T: int, d: int, E: int, k: int, h: int, learned: bool,
                  device="cuda", with_backward: bool = True, recompute: bool = False,
-                 capacity_factor: Optional[float] = None):
+                 capacity_factor: Optional[float] = None, side_stream: bool = True):
         self.T, self.d, self.E, self.k, self.h = T, d, E, k, h
         self.learned = learned
         self.with_backward = with_backward
@@ -106,6 +106,11 @@ class MoELayer:
             if learned:
                 self.dW_r = e(d, E, dt=f32)
                 self.db = e(E, dt=f32)
+            # the backward's second stream (see backward)
+            self._side = None
+            if side_stream and dev.type == "cuda":
+                self._side = torch.cuda.Stream(device=dev)
+                self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
 
     # ------------------------------------------------------------- inputs
     def load_inputs(self, inp: Dict[str, np.ndarray]) -> None:
@@ -215,22 +220,51 @@ class MoELayer:
             L.moe_grouped_swiglu_bwd_dx(self.offsets, self.W1, self.W3, self.dh1, self.dh3,
                                         self.dxp, self.ws)
         mark("gemm_wgrad")
+        side = self._side
+        if side is None:
+            L.moe_grouped_swiglu_bwd_wgrad(self.xp, self.offsets, self.a, self.dyp, self.dh1,
+                                           self.dh3, self.dW1, self.dW3, self.dW2, self.ws)
+            self._unpermute_and_router_bwd(mark, logits_bwd=True)
+            return
+        # The unpermute, the router backward through the top-k and, for a
+        # learned router without capacity padding, the router logits backward
+        # read nothing the weight-gradient GEMM writes and use a part of the
+        # workspace it does not, so they run on a second stream beside it, in
+        # what its one block an SM leaves free (registers, threads, a few KB of
+        # shared memory).  The padded layer's unpadded route map reuses the
+        # GEMM's part of the workspace and waits for it.
+        main = torch.cuda.current_stream(self.dX.device)
+        self._fork.record(main)
         L.moe_grouped_swiglu_bwd_wgrad(self.xp, self.offsets, self.a, self.dyp, self.dh1,
                                        self.dh3, self.dW1, self.dW3, self.dW2, self.ws)
+        mark("join_side")
+        side.wait_event(self._fork)
+        with torch.cuda.stream(side):
+            self._unpermute_and_router_bwd(mark, logits_bwd=self.C is None)
+            mark("side_end")
+            self._join.record(side)
+        main.wait_event(self._join)
+        if self.learned and self.C is not None:
+            self._router_logits_bwd(mark)
+
+    def _unpermute_and_router_bwd(self, mark, logits_bwd: bool) -> None:
         mark("unpermute")
         self._combine(self.dxp, None, self.dX)
         mark("router_bwd")
         L.moe_router_topk_bwd(self.gate, self.dgate, self.idx, self.E, self.dlogits)
-        if self.learned:
-            offsets, slot_of_row = self.offsets, self.slot_of_row
-            if self.C is not None:
-                mark("expert_offsets_unpadded")
-                L.moe_expert_offsets(self.idx, self.E, self.u_counts, self.u_offsets,
-                                     self.u_row_of_slot, self.u_slot_of_row, self.ws)
-                offsets, slot_of_row = self.u_offsets, self.u_slot_of_row
-            mark("router_logits_bwd")
-            L.moe_router_logits_bwd_topk(self.x, self.W_r, self.dlogits, self.idx, offsets,
-                                         slot_of_row, self.dX, self.dW_r, self.db, self.ws)
+        if self.learned and logits_bwd:
+            self._router_logits_bwd(mark)
+
+    def _router_logits_bwd(self, mark) -> None:
+        offsets, slot_of_row = self.offsets, self.slot_of_row
+        if self.C is not None:
+            mark("expert_offsets_unpadded")
+            L.moe_expert_offsets(self.idx, self.E, self.u_counts, self.u_offsets,
+                                 self.u_row_of_slot, self.u_slot_of_row, self.ws)
+            offsets, slot_of_row = self.u_offsets, self.u_slot_of_row
+        mark("router_logits_bwd")
+        L.moe_router_logits_bwd_topk(self.x, self.W_r, self.dlogits, self.idx, offsets,
+                                     slot_of_row, self.dX, self.dW_r, self.db, self.ws)
 
     # ------------------------------------------------------------- MXFP8
     def enable_mxfp8(self) -> None:
