@@ -62,7 +62,7 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float g, uint4 v) {
 
 // out[t] = sum_j g[t,j] * yp[row(t,j)] in slot order, fp32, one rounding
 // (g = 1 without gates: the unpermute-sum).  k is a template parameter so
-// that all K x U row loads of a pass are in flight before the first FMA (8 to
+// that all K x U row loads of a pass are in flight before the first FMA (6 to
 // 16 vectors of 16 bytes a lane; a generic copy loading one row at a time ran
 // at 0.88-0.89 of the HBM copy rate, this one at 0.93-0.95); slots with no
 // row read row 0 and add nothing.
@@ -121,7 +121,10 @@ combine_k_kernel(const uint16_t* __restrict__ yp, int R, const int32_t* __restri
 template <int K>
 void launch_combine_k(dim3 grid, cudaStream_t s, const uint16_t* yp, int R, const int32_t* row_of_slot,
                       const float* gate, int T, int d, uint16_t* out) {
-  constexpr int U = K <= 2 ? 8 : (K <= 4 ? 4 : 2);
+  // two 16-byte vectors a row from k = 3 up: at k = 4, 64 registers instead of
+  // 100 (twice the blocks an SM holds, 2 us faster at T = 16384, d = 2048, and
+  // room for two blocks beside a CTA-pair GEMM's block)
+  constexpr int U = K <= 2 ? 8 : 2;
   (void)launch_pdl(combine_k_kernel<K, U>, grid, kThreads, 0, s, yp, R, row_of_slot, gate, T, d, out);
 }
 
