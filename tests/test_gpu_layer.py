@@ -160,10 +160,11 @@ def test_graph_capture_proves_no_host_sync_and_replays_bitwise():
 
 @pytest.mark.parametrize("routing,factor", [("uniform", None), ("learned", None), ("learned", 1.25)])
 def test_second_stream_backward_equals_one_stream_bitwise(routing, factor):
-    # the unpermute and the router backward run on a second stream beside the
-    # weight-gradient GEMM (the padded layer's unpadded route map after it);
-    # the results equal the single-stream step bit for bit, also with three
-    # steps queued back to back (each step's forward after the last join)
+    # with side_stream=True the unpermute and the router backward run on a
+    # second stream beside the weight-gradient GEMM (the padded layer's
+    # unpadded route map after it); the results equal the single-stream step
+    # bit for bit, also with three steps queued back to back (each step's
+    # forward after the last join)
     w = wl.small_workload(T=2304, d=256, E=8, k=4, h=256, routing=routing,
                           zipf=(routing == "learned"))
     inp = wl.generate(w, seed=9)
@@ -184,6 +185,18 @@ def test_second_stream_backward_equals_one_stream_bitwise(routing, factor):
         res.append({n: getattr(layer, n).clone() for n in names})
     for n in names:
         assert torch.equal(res[0][n], res[1][n]), n
+    # the fork and the join capture into a CUDA graph and replay bit for bit
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            layer.step()
+    for n in names:
+        getattr(layer, n).zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for n in names:
+        assert torch.equal(getattr(layer, n), res[1][n]), n
 
 
 @pytest.mark.parametrize("T,E", [(2000, 16), (2048, 4)])   # single-CTA / CTA-pair row GEMMs

@@ -54,7 +54,7 @@ class MoELayer:
 
     def __init__(self, T: int, d: int, E: int, k: int, h: int, learned: bool,
                  device="cuda", with_backward: bool = True, recompute: bool = False,
-                 capacity_factor: Optional[float] = None, side_stream: bool = True):
+                 capacity_factor: Optional[float] = None, side_stream: bool = False):
         self.T, self.d, self.E, self.k, self.h = T, d, E, k, h
         self.learned = learned
         self.with_backward = with_backward
@@ -106,7 +106,8 @@ class MoELayer:
             if learned:
                 self.dW_r = e(d, E, dt=f32)
                 self.db = e(E, dt=f32)
-            # the backward's second stream (see backward)
+            # the backward's optional second stream (see backward); off by
+            # default: with steps queued back to back it made the step slower
             self._side = None
             if side_stream and dev.type == "cuda":
                 self._side = torch.cuda.Stream(device=dev)
