@@ -148,6 +148,48 @@ def test_mxfp8_forward_error_matches_format_precision():
     assert 0.015 < rel1 < 0.06
 
 
+@pytest.mark.parametrize("case", ["Xp and W1/W3", "A and W2"])
+def test_mxfp8_forward_blocks_run_along_each_reduction_dimension(case):
+    # Powers of two from 2^-10 to 2^10 scale the rows of a GEMM's left operand
+    # and the output columns of its right one.  A block of 32 along the
+    # reduction dimension (the pages' rule) never holds two of those scales,
+    # so once the column scales are divided out every output row keeps E4M3
+    # precision; a block across rows or across output columns would span up
+    # to 2^20, beyond E4M3's range of about 2^17.8, and flush or coarsen the
+    # small members.  Case one checks H1, H3 (Xp, W1, W3); case two Yp (A, W2).
+    T, d, E, k, h = 32, 64, 2, 2, 64
+    R = T * k
+    rng = np.random.default_rng(22 if case == "A and W2" else 21)
+    p2 = lambda lo, hi, shape: np.exp2(rng.integers(lo, hi + 1, shape).astype(float))  # noqa: E731
+    one = lambda n: np.ones((E, 1, n))  # noqa: E731
+    if case == "Xp and W1/W3":
+        sx, c1, c3, c2 = p2(-10, 10, (R, 1)), p2(-10, 10, (E, 1, h)), p2(-10, 10, (E, 1, h)), one(d)
+        checks = (("H1", c1), ("H3", c3))
+    else:                       # rows of A vary like those of Xp squared
+        sx, c1, c3, c2 = p2(-5, 5, (R, 1)), one(h), one(h), p2(-10, 10, (E, 1, d))
+        checks = (("Yp", c2),)
+    Xp = rng.standard_normal((R, d)) * sx
+    W1 = rng.standard_normal((E, d, h)) / 8 * c1
+    W3 = rng.standard_normal((E, d, h)) / 8 * c3
+    W2 = rng.standard_normal((E, h, d)) / 8 * c2
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    _, off, _, _ = ol.route_map(idx, E)
+    with np.errstate(over="ignore"):        # silu of very negative inputs: exp overflows to -0
+        exact = ol.expert_ffn_forward(Xp, off, W1, W3, W2)
+        q = mx.expert_ffn_forward_mxfp8(Xp, off, W1, W3, W2)
+    for name, cs in checks:
+        rel = []
+        for e in range(E):
+            a = exact[name][off[e]:off[e + 1]] / cs[e]
+            b = q[name][off[e]:off[e + 1]] / cs[e]
+            rel.append(np.linalg.norm(b - a, axis=1) / np.linalg.norm(a, axis=1))
+        rel = np.concatenate(rel)
+        # two quantised operands: about 3.7 % a row; with A's as well about 6 %
+        assert np.median(rel) < (0.06 if name != "Yp" else 0.12), (name, np.median(rel))
+        assert rel.max() < (0.15 if name != "Yp" else 0.3), (name, rel.max())
+        assert rel.min() > 0
+
+
 def _padded_case(seed, T=12, d=5, E=3, k=2, h=4):
     rng = np.random.default_rng(seed)
     x = rng.standard_normal((T, d))
