@@ -23,8 +23,9 @@ import test_oracle_routing as tr
 
 _ORIG = {n: getattr(ol, n) for n in (
     "topk", "route_map", "expert_ffn_forward", "combine", "combine_backward",
-    "expert_ffn_backward", "dispatch")}
-_ORIG_MX = {n: getattr(mx, n) for n in ("block_exponent", "e4m3_decode")}
+    "expert_ffn_backward", "dispatch", "router_logits", "unpermute_sum")}
+_ORIG_MX = {n: getattr(mx, n) for n in ("block_exponent", "e4m3_decode", "dequantize_blocks")}
+_ORIG_PD = {n: getattr(pd, n) for n in ("capacity_route_map",)}
 
 
 def _tiny(routing):
@@ -166,6 +167,32 @@ def _capacity_keeps_last(idx, E, C):
     return tuple(a.astype(np.int32) for a in (counts, offsets, ros, sor, routed))
 
 
+def _router_logits_without_bias(x, W_r, b=None, out_dtype=np.float32):
+    return _ORIG["router_logits"](x, W_r, None, out_dtype)
+
+
+def _combine_bwd_dg_next_row(dOut, Yp, row_of_slot, g, k):
+    dYp, _ = _ORIG["combine_backward"](dOut, Yp, row_of_slot, g, k)
+    rows = np.asarray(row_of_slot, np.int64).reshape(-1, k)
+    dOut = np.asarray(dOut, np.float64); Yp = np.asarray(Yp, np.float64)
+    dg = np.stack([np.einsum("td,td->t", dOut, Yp[rows[:, (j + 1) % k]]) for j in range(k)], axis=1)
+    return dYp, dg
+
+
+def _unpermute_first_slot_only(dXp, row_of_slot, k):
+    rows = np.asarray(row_of_slot, np.int64).reshape(-1, k)
+    return np.asarray(dXp, np.float64)[rows[:, 0]]
+
+
+def _dequantize_bias_126(q, s, axis=-1):
+    return _ORIG_MX["dequantize_blocks"](q, (np.asarray(s).astype(np.int64) + 1).astype(np.uint8), axis)
+
+
+def _capacity_counts_not_clamped(idx, E, C):
+    counts, offsets, ros, sor, routed = _ORIG_PD["capacity_route_map"](idx, E, C)
+    return routed.copy(), offsets, ros, sor, routed
+
+
 def _e4m3_truncating(v):
     v = np.asarray(v, np.float64)
     pos = mx._POS_VALUES
@@ -230,6 +257,11 @@ MISTAKES = {
         lambda c: np.where(((np.asarray(c).astype(np.int64) >> 3) & 0xF) == 0,
                            _ORIG_MX["e4m3_decode"](c) / 2, _ORIG_MX["e4m3_decode"](c)), MXFP8),
     "padded: the last C slots kept instead of the first": (pd, "capacity_route_map", _capacity_keeps_last, PADDED),
+    "router logits: bias dropped": (ol, "router_logits", _router_logits_without_bias, BACKWARD),
+    "combine backward: dg from the next slot's row": (ol, "combine_backward", _combine_bwd_dg_next_row, BACKWARD),
+    "unpermute-sum: first slot only": (ol, "unpermute_sum", _unpermute_first_slot_only, BACKWARD),
+    "MXFP8: scale byte read with bias 126": (mx, "dequantize_blocks", _dequantize_bias_126, MXFP8),
+    "padded: kept counts not clamped at C": (pd, "capacity_route_map", _capacity_counts_not_clamped, PADDED),
     "MXFP8 forward: Xp blocks across rows": (mx, "expert_ffn_forward_mxfp8", _mxfp8_forward_axes(0, 0, 1, 0), MXFP8_GEMMS),
     "MXFP8 forward: W1/W3 blocks along h": (mx, "expert_ffn_forward_mxfp8", _mxfp8_forward_axes(1, 1, 1, 0), MXFP8_GEMMS),
     "MXFP8 forward: A blocks across rows": (mx, "expert_ffn_forward_mxfp8", _mxfp8_forward_axes(1, 0, 0, 0), MXFP8_GEMMS),
