@@ -257,7 +257,10 @@ def test_bad_expert_id_sets_device_status_without_faulting():
     assert L.moe_get_status(ws) == 0
 
 
-@pytest.mark.parametrize("T,d,k", [(1, 8, 1), (333, 2048, 4), (1024, 264, 2), (97, 4096, 8)])
+# k = 3 and 6 take two 16-byte vectors a row a pass (k = 4 too); d = 264 and
+# 520 leave a ragged last pass, d = 8 a single vector a row
+@pytest.mark.parametrize("T,d,k", [(1, 8, 1), (333, 2048, 4), (1024, 264, 2), (97, 4096, 8),
+                                   (129, 264, 3), (64, 8, 3), (50, 520, 6)])
 def test_dispatch_exact_and_combine(T, d, k):
     E = 16
     rng = np.random.default_rng(T * 3 + d)
