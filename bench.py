@@ -208,6 +208,31 @@ class ClockSampler:
                 "samples": len(inside), "which": how, "interval_ms": 50}
 
 
+def step_timings(events):
+    """Per-step and per-call times from the marks of the timed steps.
+
+    `events` holds, per step, the (label, event, stream) marks in the order the
+    step made them; each mark was recorded on the stream that was current.
+    A step lasts from the first to the last mark of the stream its first mark
+    is on (the step's stream: its last mark follows the join of any second
+    stream); a call lasts from its mark to the next mark on the same stream.
+    Returns (step times, {label: [times]}, labels marked on another stream).
+    """
+    step_ms, per_label, side_labels = [], {}, set()
+    for lst in events:
+        main = lst[0][2]
+        by_stream = {}
+        for lab, ev, st in lst:
+            by_stream.setdefault(st, []).append((lab, ev))
+        side_labels |= {lab for lab, _, st in lst if st != main}
+        seq = by_stream[main]
+        step_ms.append(seq[0][1].elapsed_time(seq[-1][1]))
+        for seq in by_stream.values():
+            for (lab, ev), (_, nxt) in zip(seq[:-1], seq[1:]):
+                per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
+    return step_ms, per_label, side_labels
+
+
 def capacity_stats(counts, T: int, k: int, E: int, factor: float = 1.25):
     """What a layer padded to one capacity per expert would do with these
     per-expert row counts: capacity ceil(factor*T*k/E), every expert keeping
@@ -308,20 +333,7 @@ def run_ours(args):
         status = L.moe_get_status(layer.ws)
         if status != 0:
             raise RuntimeError(f"device status {status} after the timed steps")
-        step_ms, per_label, side_labels = [], {}, set()
-        for lst in events:
-            # the step: first to last event of the launching stream (the last
-            # one follows the join of the second stream); a call: its event
-            # to the next one on the same stream
-            by_stream = {}
-            for lab, ev, st in lst:
-                by_stream.setdefault(st, []).append((lab, ev))
-            main_seq = by_stream[lst[0][2]]
-            side_labels |= {lab for lab, _, st in lst if st != lst[0][2]}
-            step_ms.append(main_seq[0][1].elapsed_time(main_seq[-1][1]))
-            for seq in by_stream.values():
-                for (lab, ev), (_, nxt) in zip(seq[:-1], seq[1:]):
-                    per_label.setdefault(lab, []).append(ev.elapsed_time(nxt))
+        step_ms, per_label, side_labels = step_timings(events)
         return {"ms_per_step": allmax(statistics.mean(step_ms), dev),
                 "kernels_ms": {k: statistics.mean(v) for k, v in per_label.items()},
                 "side_labels": sorted(side_labels),

@@ -39,3 +39,31 @@ def test_bench_capacity_stats_by_hand():
     assert abs(st["padded_over_routed_rows"] - 15 / 12) < 1e-12
     # enough capacity: nothing dropped
     assert bench.capacity_stats([4, 4, 4], T=6, k=2, E=3)["dropped_rows"] == 0
+
+
+class _FakeEvent:
+    """A recorded CUDA event stand-in: a timestamp in ms."""
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_bench_step_timings_per_stream():
+    import bench
+    E = _FakeEvent
+    # one step: main stream 1 (a, wgrad, join, end), second stream 2 (unpermute, side_end)
+    step = [("a", E(0.0), 1), ("wgrad", E(1.0), 1), ("join", E(3.0), 1),
+            ("unpermute", E(1.2), 2), ("side_end", E(2.0), 2), ("end", E(3.5), 1)]
+    step_ms, per_label, side = bench.step_timings([step, step])
+    assert step_ms == [3.5, 3.5]                       # first to last mark of stream 1
+    assert per_label["a"] == [1.0, 1.0]
+    assert per_label["wgrad"] == [2.0, 2.0]            # to the next mark on its own stream
+    assert per_label["join"] == [0.5, 0.5]
+    assert per_label["unpermute"] == [0.8, 0.8]        # measured on stream 2 alone
+    assert "side_end" not in per_label and "end" not in per_label
+    assert side == {"unpermute", "side_end"}
+    # one stream: consecutive marks
+    step_ms, per_label, side = bench.step_timings([[("x", E(0.0), 7), ("y", E(0.25), 7), ("end", E(1.0), 7)]])
+    assert step_ms == [1.0] and per_label == {"x": [0.25], "y": [0.75]} and side == set()
