@@ -21,6 +21,11 @@ the expert-sorted buffers (its first C routed slots in token order, then zero
 rows), later slots are dropped, and the same grouped GEMMs run on all E * C
 rows (the ``_capacity`` route-map, dispatch and combine calls).
 
+With ``side_stream=True`` the combine(gates = None) and the router backward
+run on a second stream beside the wgrad GEMM, joined before the step ends
+(same results bit for bit; off by default: with steps queued back to back it
+was not faster).
+
 Nothing is copied back to the host and nothing waits on the host.
 """
 from __future__ import annotations
